@@ -1,0 +1,518 @@
+#!/usr/bin/env python3
+"""Benchmark of the vocabulary cross-entropy hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload linear|logits|both]
+
+One step is one forward + backward pass over one batch of synthetic inputs:
+
+* linear form (headline): lce_forward + lce_backward, N=4096 tokens, H=4096,
+  V=131072, BF16 X ~ N(0,1), W ~ N(0, 1/H), uniform targets, mean reduction.
+  Throughput counts four classifier GEMMs per step (8 N H V flops: forward
+  logits, backward recomputation, dX, dW), the convention of the Liger SM100
+  pull request ("Performance methodology").
+* logits form: ce_forward + ce_backward, N = 4 x 4096 rows, V = 128256 BF16
+  logits ~ N(0, 9), 5% ignored, label smoothing 0.1, mean reduction; reported
+  as HBM GB/s of algorithmic bytes in the ``logits_ce`` object.
+
+Both workloads are larger than the 129 MB L2 (W is 1 GiB, the logits 4.2 GB),
+so no L2 flush is needed between steps.  Device timing uses CUDA events on the
+launching stream; ``e2e`` repeats the step through the same public calls with
+the inputs copied from pinned host memory and the loss read back every step.
+With ``--gpus N`` (torchrun) every rank runs an independent replica: the path
+has no exchange step, so there is no collective on the data path.
+
+``--impl reference`` times the FP64 CPU oracle on a bounded sample of the same
+workload (a few tokens / rows per step) on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wk  # noqa: E402
+
+PUBLISHED_TP1_FB_TFLOPS = 1606.5  # Liger SM100 PR, M=4096 F+B, TP1, NVIDIA B300 (context)
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ---------------------------------------------------------------------------
+
+def dist_setup(n_gpus):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+        pg = dist
+    return rank, world, local, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def max_over_ranks(pg, x: float) -> float:
+    if pg is None:
+        return x
+    import torch
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class Clocks:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arms
+# ---------------------------------------------------------------------------
+
+def _torch_inputs_linear(wl, dev):
+    import torch
+    inp = wk.make_linear_inputs(wl)
+    host = dict(
+        X=torch.from_numpy(inp.x.view(np.int16)).view(torch.bfloat16),
+        W=torch.from_numpy(inp.w.view(np.int16)).view(torch.bfloat16),
+        target=torch.from_numpy(inp.target),
+        grad=torch.from_numpy(inp.grad),
+    )
+    devt = {k: v.to(dev) for k, v in host.items()}
+    return host, devt, inp
+
+
+class LinearStep:
+    """lce_forward + lce_backward with every buffer preallocated (no allocation per step)."""
+
+    def __init__(self, wl, dev):
+        import torch
+        import vocabulary_cross_entropy_gb300 as vce
+        self.vce = vce
+        self.wl = wl
+        self.host, self.d, _ = _torch_inputs_linear(wl, dev)
+        n, h, v = wl.n, wl.hidden, wl.vocab
+        self.loss = torch.empty(1 if wl.reduce_loss else n, dtype=torch.float32, device=dev)
+        self.lse = torch.empty(n, dtype=torch.float32, device=dev)
+        self.n_valid = torch.empty(1, dtype=torch.int64, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.dX = torch.empty(n, h, dtype=torch.bfloat16, device=dev)
+        self.dW = torch.empty(v, h, dtype=torch.bfloat16, device=dev)
+        self.ws_bytes = vce.lce_workspace_size(n, h, v, wl.reduce_loss)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        self.n_valid_count = int((self.host["target"] != wk.IGNORE_IDX).sum())
+
+    def forward(self):
+        wl = self.wl
+        self.vce.lce_forward(self.d["X"], self.d["W"], self.d["target"], wl.label_smoothing,
+                             wl.reduce_loss, loss=self.loss, lse=self.lse, n_valid=self.n_valid,
+                             workspace=self.ws, dev_status=self.status)
+
+    def backward(self):
+        wl = self.wl
+        self.vce.lce_backward(self.d["X"], self.d["W"], self.d["target"], self.lse, self.n_valid,
+                              self.d["grad"], wl.label_smoothing, wl.reduce_loss, dX=self.dX,
+                              dW=self.dW, workspace=self.ws, dev_status=self.status)
+
+    def flops(self):
+        wl = self.wl
+        return 8.0 * wl.n * wl.hidden * wl.vocab
+
+    def units(self):
+        return self.flops() / 1e12  # TFLOP per step
+
+
+class LogitsStep:
+    def __init__(self, wl, dev):
+        import torch
+        import vocabulary_cross_entropy_gb300 as vce
+        self.vce = vce
+        self.wl = wl
+        inp = wk.make_logits_inputs(wl)
+        self.host = dict(logits=torch.from_numpy(inp.logits.view(np.int16)).view(torch.bfloat16),
+                         target=torch.from_numpy(inp.target), grad=torch.from_numpy(inp.grad))
+        del inp
+        self.d = {k: v.to(dev) for k, v in self.host.items()}
+        n, v = wl.n_rows, wl.vocab
+        self.loss = torch.empty(1 if wl.reduce_loss else n, dtype=torch.float32, device=dev)
+        self.stats = torch.empty(n, 2, dtype=torch.float32, device=dev)
+        self.n_valid = torch.empty(1, dtype=torch.int64, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.dlogits = torch.empty_like(self.d["logits"])
+        self.ws = torch.empty(max(1, vce.ce_workspace_size(n, v, wl.reduce_loss)), dtype=torch.uint8,
+                              device=dev)
+        self.n_valid_count = int((self.host["target"] != wk.IGNORE_IDX).sum())
+
+    def forward(self):
+        wl = self.wl
+        self.vce.ce_forward(self.d["logits"], self.d["target"], wl.label_smoothing, wl.reduce_loss,
+                            loss=self.loss, stats=self.stats, n_valid=self.n_valid, workspace=self.ws,
+                            dev_status=self.status)
+
+    def backward(self):
+        wl = self.wl
+        self.vce.ce_backward(self.d["logits"], self.d["target"], self.stats, self.n_valid,
+                             self.d["grad"], wl.label_smoothing, wl.reduce_loss, dlogits=self.dlogits,
+                             dev_status=self.status)
+
+    def bytes_fwd(self):
+        return float(self.n_valid_count) * self.wl.vocab * 2
+
+    def bytes_bwd(self):
+        return float(self.n_valid_count) * self.wl.vocab * 2 + float(self.wl.n_rows) * self.wl.vocab * 2
+
+    def units(self):
+        return (self.bytes_fwd() + self.bytes_bwd()) / 1e9  # GB per step
+
+
+def time_steps(step, steps, warmup, pg, events_for=("forward", "backward")):
+    """Returns (total_ms max over ranks, {phase: mean ms per launch})."""
+    import torch
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        step.forward()
+        step.backward()
+    torch.cuda.synchronize()
+    barrier(pg)
+    torch.cuda.synchronize()
+    ev = {p: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)] for p in events_for}
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        ev["forward"][i][0].record(stream)
+        step.forward()
+        ev["forward"][i][1].record(stream)
+        ev["backward"][i][0].record(stream)
+        step.backward()
+        ev["backward"][i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(pg)
+    torch.cuda.synchronize()
+    total = max_over_ranks(pg, start.elapsed_time(end))
+    phases = {p: statistics.mean(a.elapsed_time(b) for a, b in ev[p]) for p in events_for}
+    return total, phases
+
+
+def time_e2e_linear(step, steps, warmup, pg):
+    """The same step through the public calls, inputs copied from pinned host memory each step."""
+    import torch
+    stream = torch.cuda.current_stream()
+    pinned = {k: v.pin_memory() for k, v in step.host.items()}
+    loss_host = torch.empty_like(step.loss, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+    d2h = loss_host.numel() * loss_host.element_size()
+
+    def one():
+        for k, t in pinned.items():
+            step.d[k].copy_(t, non_blocking=True)
+        step.forward()
+        step.backward()
+        loss_host.copy_(step.loss, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    barrier(pg)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        one()
+    e.record(stream)
+    torch.cuda.synchronize()
+    barrier(pg)
+    return max_over_ranks(pg, s.elapsed_time(e)), h2d, d2h
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline (the oracle, timed on a bounded sample)
+# ---------------------------------------------------------------------------
+
+def oracle_linear_sample(wl, tokens: int):
+    """One oracle forward + backward on the first ``tokens`` tokens of the workload (full W).
+
+    Returns (seconds, flops of the sample = 8 * tokens * H * V)."""
+    import oracle
+    x = wk.normal_rows(wl.seed, wk.TID_X, np.arange(tokens), wl.hidden, 1.0, True)
+    w = wk.normal_matrix(wl.seed, wk.TID_W, wl.vocab, wl.hidden, wk.linear_w_std(wl), True)
+    t = wk.linear_targets(wl)[:tokens]
+    g = np.ones(1) if wl.reduce_loss else wk.grad_rows(wl.seed, wl.n)[:tokens]
+    t0 = time.perf_counter()
+    f = oracle.lce_forward(x, w, t, wl.label_smoothing, wl.reduce_loss)
+    oracle.lce_backward(x, w, t, f["lse"], f["n_valid"], g, wl.label_smoothing, wl.reduce_loss, z=f["z"])
+    dt = time.perf_counter() - t0
+    return dt, 8.0 * tokens * wl.hidden * wl.vocab
+
+
+def oracle_logits_sample(wl, rows: int):
+    import oracle
+    r = np.arange(rows)
+    z = wk.logits_rows(wl, r)
+    t = wk.uniform_targets(wl.seed, wl.n_rows, wl.vocab, wl.ignore_frac)[:rows]
+    t0 = time.perf_counter()
+    f = oracle.ce_forward(z, t, wl.label_smoothing, wl.reduce_loss, dtype=wl.dtype)
+    oracle.ce_backward(z, t, f["lse"], f["n_valid"], np.ones(1), wl.label_smoothing, wl.reduce_loss,
+                       dtype=wl.dtype)
+    dt = time.perf_counter() - t0
+    nv = int((t != wk.IGNORE_IDX).sum())
+    nbytes = nv * wl.vocab * 2 * 2 + rows * wl.vocab * 2
+    return dt, nbytes
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+LIN_SAMPLE_TOKENS = 32
+LOGITS_SAMPLE_ROWS = 256
+
+
+def cpu_baseline_linear(wl):
+    dt, fl = oracle_linear_sample(wl, LIN_SAMPLE_TOKENS)
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
+            "sample": f"FP64 NumPy oracle forward+backward on the first {LIN_SAMPLE_TOKENS} tokens "
+                      f"of the workload against the full W ({wl.vocab}x{wl.hidden}); flops counted "
+                      f"as 8*tokens*H*V", "seconds": dt}
+
+
+def cpu_baseline_logits(wl):
+    dt, nb = oracle_logits_sample(wl, LOGITS_SAMPLE_ROWS)
+    return {"value": nb / dt / 1e9, "unit": "GB/s", "cores": host_cores(), "kind": "oracle",
+            "sample": f"FP64 NumPy oracle forward+backward on the first {LOGITS_SAMPLE_ROWS} rows",
+            "seconds": dt}
+
+
+# ---------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------
+
+def run_reference(args, rank, world, pg):
+    if rank != 0:
+        return 0
+    wl = wk.LINEAR_HEADLINE
+    times = []
+    for i in range(args.warmup + args.steps):
+        dt, fl = oracle_linear_sample(wl, LIN_SAMPLE_TOKENS)
+        if i >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    value = fl * len(times) / total / 1e12
+    cb = {"value": value, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
+          "sample": f"each step: FP64 NumPy oracle forward+backward on {LIN_SAMPLE_TOKENS} tokens of the "
+                    f"headline workload against the full W"}
+    line = {
+        "impl": "reference",
+        "metric": "linear-CE fwd+bwd TFLOP/s (4 classifier GEMMs)",
+        "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total / len(times) * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "n": wl.n, "h": wl.hidden, "v": wl.vocab,
+                   "sample_tokens": LIN_SAMPLE_TOKENS},
+        "cpu_baseline": cb,
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="both", choices=["linear", "logits", "both"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank, world, local, pg = dist_setup(args.gpus)
+    if args.impl == "reference":
+        return run_reference(args, rank, world, pg)
+
+    import torch
+    from vocabulary_cross_entropy_gb300 import build as vbuild
+    if rank == 0:
+        vbuild.build()
+    barrier(pg)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pk = peaks()
+    out = {}
+
+    logits_obj = None
+    if args.workload in ("logits", "both"):
+        st = LogitsStep(wk.LOGITS_MEMBOUND, dev)
+        with Clocks(local) as ck:
+            total, ph = time_steps(st, args.steps, args.warmup, pg)
+        clocks_l = ck.summary()
+        gb = st.units() * world * args.steps / (total / 1e3)
+        bwd_gbs = st.bytes_bwd() / (ph["backward"] / 1e3) / 1e9
+        fwd_gbs = st.bytes_fwd() / (ph["forward"] / 1e3) / 1e9
+        assert int(st.status.item()) == 0, "device status reported an error"
+        logits_obj = {
+            "metric": "logits-CE fwd+bwd HBM GB/s", "value": gb, "unit": "GB/s",
+            "ms_per_step": total / args.steps, "fwd_gbs": fwd_gbs, "bwd_gbs": bwd_gbs,
+            "fwd_ms": ph["forward"], "bwd_ms": ph["backward"],
+            "config": {"workload": st.wl.name, "n_rows": st.wl.n_rows, "vocab": st.wl.vocab,
+                       "dtype": "bf16", "label_smoothing": st.wl.label_smoothing,
+                       "reduce_loss": st.wl.reduce_loss, "n_valid": st.n_valid_count,
+                       "l2": "inputs larger than L2 (4.2 GB logits), no flush"},
+            "roofline": {"kernel": "ce_backward_rows", "bound": "hbm", "achieved": bwd_gbs,
+                         "peak": pk["hbm"], "unit": "GB/s", "frac": bwd_gbs / pk["hbm"],
+                         "traffic": None, "peak_source": pk["source"] + " hbm_gbs (copy)",
+                         "algorithmic_bytes": st.bytes_bwd()},
+            "roofline_fwd": {"kernel": "ce_forward_rows", "bound": "hbm", "achieved": fwd_gbs,
+                             "peak": pk["hbm"], "unit": "GB/s", "frac": fwd_gbs / pk["hbm"],
+                             "algorithmic_bytes": st.bytes_fwd()},
+            "gpu_launches": 3 * args.steps,
+            "clocks": clocks_l,
+        }
+        if rank == 0 and not args.no_cpu_baseline:
+            logits_obj["cpu_baseline"] = cpu_baseline_logits(st.wl)
+        del st
+        torch.cuda.empty_cache()
+
+    if args.workload == "logits":
+        line = dict(logits_obj)
+        line.update({"n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                     "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                     "dtype": "bf16", "data": "synthetic"})
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return 0
+
+    st = LinearStep(wk.LINEAR_HEADLINE, dev)
+    with Clocks(local) as ck:
+        total, ph = time_steps(st, args.steps, args.warmup, pg)
+    clocks = ck.summary()
+    assert int(st.status.item()) == 0, "device status reported an error"
+    value = st.units() * world * args.steps / (total / 1e3)
+    fwd_flops = 2.0 * st.wl.n * st.wl.hidden * st.wl.vocab
+    fwd_tf = fwd_flops / (ph["forward"] / 1e3) / 1e12
+    bwd_tf = 3 * fwd_flops / (ph["backward"] / 1e3) / 1e12
+    e2e_ms, h2d, d2h = time_e2e_linear(st, max(3, args.steps // 2), 3, pg)
+    e2e_steps = max(3, args.steps // 2)
+    e2e_val = st.units() * world * e2e_steps / (e2e_ms / 1e3)
+    line = {
+        "metric": "linear-CE fwd+bwd TFLOP/s (4 classifier GEMMs)",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": value / world / PUBLISHED_TP1_FB_TFLOPS,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": st.wl.name, "n": st.wl.n, "h": st.wl.hidden, "v": st.wl.vocab,
+                   "reduce_loss": True, "label_smoothing": 0.0,
+                   "l2": "inputs larger than L2 (W is 1 GiB), no flush",
+                   "workspace_bytes": st.ws_bytes},
+        "fwd_ms": ph["forward"], "bwd_ms": ph["backward"], "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
+        "roofline": {"kernel": "lce_forward (tcgen05 GEMM + softmax epilogue)", "bound": "tensor",
+                     "achieved": fwd_tf, "peak": pk["bf16"], "unit": "TFLOP/s",
+                     "frac": fwd_tf / pk["bf16"], "traffic": None,
+                     "peak_source": pk["source"] + " bf16_tflops (burst cuBLAS)",
+                     "algorithmic_flops": fwd_flops},
+        "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms / e2e_steps},
+        "gpu_launches": args.steps * (3 + 3),
+        "clocks": clocks,
+    }
+    if logits_obj is not None:
+        line["logits_ce"] = logits_obj
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_linear(st.wl)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

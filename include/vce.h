@@ -1,0 +1,207 @@
+/*
+ * vce.h -- C ABI of the GB300 (sm_103a) vocabulary cross-entropy library (libvce.so).
+ *
+ * Two forms of large-vocabulary softmax cross entropy, neither of which keeps a
+ * full-precision logit or gradient matrix:
+ *
+ *   logits form  ce_forward / ce_backward
+ *       Follows Transformer Engine's parallel_cross_entropy (API card
+ *       "Implementation:NVIDIA TransformerEngine Cross Entropy", sections
+ *       "Signature" and "I/O Contract": inp, target, label_smoothing,
+ *       reduce_loss, ignore_idx = -100, FP32 loss for BF16/FP32 input), minus the
+ *       process group.  Forward saves per-row statistics (max, log-sum-exp)
+ *       instead of the derivative, and backward rebuilds dlogits from them
+ *       (pull request "Minimize the memory usage of the fused cross entropy
+ *       kernel", section "Changes"); backward may write dlogits over the logits
+ *       (same pull request, the destructive buffer-reuse mode).
+ *
+ *   linear form  lce_forward / lce_backward
+ *       Loss from hidden states X [N, H] and classifier W [V, H]; the logits
+ *       X W^T are produced tile by tile and never stored (Cut Cross-Entropy
+ *       package card, "what_it_does"; Liger pull request "Add SM100
+ *       tensor-parallel fused scaled cross entropy", sections "Summary",
+ *       "Implementation": forward GEMM fused with NLL/LSE, backward = logits
+ *       recomputation, dX and dW).
+ *
+ * Common conventions
+ *   - Every pointer argument is a DEVICE pointer unless said otherwise; the
+ *     caller owns every buffer and the stream.  The library never allocates,
+ *     frees or synchronises, so every call can be captured in a CUDA graph.
+ *   - ``stream`` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   - The math: for a row n with logits z[n, 0..V) and target y_n,
+ *         lse_n  = log sum_v exp(z[n, v])
+ *         loss_n = (1 - eps) (lse_n - z[n, y_n]) + eps (lse_n - (1/V) sum_v z[n, v])
+ *         dz[n, v] = g_n (exp(z[n, v] - lse_n) - (1 - eps) [v = y_n] - eps / V)
+ *     with eps = label_smoothing spread over all V classes (the convention of
+ *     torch.nn.functional.cross_entropy, which the API card names as the op the
+ *     function replaces).  Loss and gradient arithmetic is FP32 whatever the
+ *     input dtype ("Description": "Loss and gradient computation in FP32").
+ *   - Rows whose target equals ``ignore_idx`` give loss 0 and gradient 0.
+ *   - ``reduce_loss`` != 0: the loss is sum_n loss_n / N_v, N_v = number of rows
+ *     whose target is not ignore_idx (NaN when N_v = 0), and backward uses
+ *     g_n = grad_output[0] / N_v.  Otherwise loss is per row and
+ *     g_n = grad_output[n].
+ *   - Host-detectable errors return a status before any launch and write
+ *     nothing.  Errors found on the device are ORed into ``*dev_status`` (a
+ *     device int the caller zeroes and reads after its own synchronisation;
+ *     may be NULL): VCE_DEVSTATUS_BAD_TARGET for a target outside [0, V) that
+ *     is not ignore_idx (that row's loss is NaN and its gradient row 0),
+ *     VCE_DEVSTATUS_TIMEOUT when a tensor-core pipeline wait gave up (the
+ *     outputs are then incomplete).
+ *   - The library runs on compute capability 10.3 (GB300) only; on any other
+ *     device every compute call returns VCE_ERR_ARCH.
+ */
+#ifndef VCE_H
+#define VCE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum vce_status {
+    VCE_OK = 0,
+    VCE_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad stride/option */
+    VCE_ERR_DTYPE = 2,       /* unsupported dtype code */
+    VCE_ERR_ALIGN = 3,       /* pointer or leading dimension violates the stated alignment */
+    VCE_ERR_WORKSPACE = 4,   /* workspace pointer NULL or smaller than required */
+    VCE_ERR_ARCH = 5,        /* current device is not compute capability 10.3 */
+    VCE_ERR_CUDA = 6         /* a CUDA runtime/driver call or a launch failed */
+} vce_status;
+
+typedef enum vce_dtype {
+    VCE_BF16 = 0,
+    VCE_F32 = 1
+} vce_dtype;
+
+#define VCE_DEVSTATUS_BAD_TARGET 1
+#define VCE_DEVSTATUS_TIMEOUT 2
+
+/* Human-readable name of a vce_status value (static string, never NULL). */
+const char* vce_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int vce_version(void);
+
+/* ------------------------------------------------------------------------ */
+/* logits form                                                              */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Bytes of device workspace ce_forward needs: n_rows * 4 (per-row losses,
+ * rounded up to 256 B) when reduce_loss != 0, else 0.
+ */
+size_t ce_workspace_size(int64_t n_rows, int64_t vocab, int reduce_loss);
+
+/*
+ * Forward of the logits form (API card "Signature"; pull request #3273
+ * "Changes": single-GPU path, one kernel computes the loss and the statistics).
+ *
+ *   logits      [n_rows, vocab] row-major, element (n, v) at logits[n * row_stride + v];
+ *               dtype BF16 or F32; must be aligned to its element size.  The
+ *               (B, SQ, V) and (SQ, B, V) layouts are both passed flattened to
+ *               n_rows = B * SQ rows, targets flattened in the same order.
+ *   row_stride  elements between rows, >= vocab.
+ *   target      [n_rows] int64.
+ *   label_smoothing in [0, 1].
+ *   loss        F32: [1] when reduce_loss, else [n_rows] (0 for ignored rows).
+ *   stats       F32 [n_rows, 2]: (max_v z, lse) per row, the only state backward
+ *               needs.  Rows with target == ignore_idx are never read and get (0, 0).
+ *   n_valid     int64 [1]: N_v, written when non-NULL; required when reduce_loss
+ *               (backward reads it).
+ *   ws/ws_bytes workspace of at least ce_workspace_size(...) bytes, 256-B aligned
+ *               (may be NULL when that size is 0).
+ */
+vce_status ce_forward(const void* logits, int dtype, int64_t n_rows, int64_t vocab,
+                      int64_t row_stride, const int64_t* target, float label_smoothing,
+                      int reduce_loss, int64_t ignore_idx, float* loss, float* stats,
+                      int64_t* n_valid, void* ws, size_t ws_bytes, int* dev_status,
+                      void* stream);
+
+/*
+ * Backward of the logits form: rebuilds dlogits from the logits and the saved
+ * statistics (pull request #3273 "Changes" and its sequence diagram: backward
+ * reads the saved input, targets, stats and grad_output).
+ *
+ *   logits, dtype, n_rows, vocab, row_stride, target, label_smoothing,
+ *   reduce_loss, ignore_idx: as passed to ce_forward.
+ *   stats       F32 [n_rows, 2] from ce_forward (only the lse column is read).
+ *   n_valid     int64 [1] from ce_forward (read only when reduce_loss).
+ *   grad_output F32 [1] when reduce_loss, else [n_rows].
+ *   dlogits     same dtype and layout (row_stride) as logits; MAY EQUAL logits,
+ *               in which case the logits are overwritten by their gradient (the
+ *               pull request's destructive mode: no extra buffer).  Any other
+ *               overlap is undefined.  Ignored rows are written as zeros.
+ */
+vce_status ce_backward(const void* logits, int dtype, int64_t n_rows, int64_t vocab,
+                       int64_t row_stride, const int64_t* target, const float* stats,
+                       const int64_t* n_valid, const float* grad_output,
+                       float label_smoothing, int reduce_loss, int64_t ignore_idx,
+                       void* dlogits, int* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* linear form (X, W and the gradients are BF16; accumulation is FP32)      */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Bytes of device workspace lce_forward and lce_backward need.
+ *
+ * Backward recomputes the logits one vocabulary slab at a time and keeps that
+ * slab's gradient dZ [n, slab] in BF16; ``max_slab_bytes`` caps that buffer
+ * (0 = no cap: one slab covers the whole vocabulary).  The slab is at least
+ * 256 vocabulary rows.  With more than one slab, dX is accumulated in an FP32
+ * [n, h] buffer inside the workspace.  The forward part holds per-tile
+ * softmax partials (12 B per token per 256 vocabulary ids) and the per-token
+ * target logit.  The same size passed to lce_backward selects the same slab.
+ */
+size_t lce_workspace_size(int64_t n, int64_t h, int64_t v, int reduce_loss,
+                          size_t max_slab_bytes);
+
+/*
+ * Forward of the linear form: loss and lse from X and W without storing X W^T
+ * (Cut Cross-Entropy card "what_it_does"; Liger pull request "Implementation",
+ * "Forward": classifier GEMM whose epilogue folds each vocabulary tile into a
+ * running max and sum).
+ *
+ *   X  BF16 [n, h] row-major; W BF16 [v, h] row-major.  h must be a multiple of 8
+ *      and both pointers 16-byte aligned (tensor-memory-access descriptors).
+ *   target int64 [n].
+ *   loss   F32 [1] (reduce_loss) or [n].
+ *   lse    F32 [n]: log-sum-exp of every row (ignored rows included), the state
+ *          lce_backward needs.
+ *   n_valid int64 [1], written when non-NULL; required when reduce_loss.
+ *   ws/ws_bytes at least lce_workspace_size(n, h, v, reduce_loss, *) bytes,
+ *          256-B aligned.
+ */
+vce_status lce_forward(const void* X, const void* W, int64_t n, int64_t h, int64_t v,
+                       const int64_t* target, float label_smoothing, int reduce_loss,
+                       int64_t ignore_idx, float* loss, float* lse, int64_t* n_valid,
+                       void* ws, size_t ws_bytes, int* dev_status, void* stream);
+
+/*
+ * Backward of the linear form (Liger pull request "Implementation", "Backward":
+ * dZ from recomputed logits, then dX = dZ W and dW = dZ^T X with FP32
+ * accumulation).
+ *
+ *   X, W, n, h, v, target, label_smoothing, reduce_loss, ignore_idx: as forward.
+ *   lse        F32 [n] from lce_forward.
+ *   n_valid    int64 [1] from lce_forward (read only when reduce_loss).
+ *   grad_output F32 [1] (reduce_loss) or [n].
+ *   dX         BF16 [n, h], 16-byte aligned; fully written.
+ *   dW         BF16 [v, h], 16-byte aligned; fully written.
+ *   ws/ws_bytes at least lce_workspace_size(n, h, v, reduce_loss, 0 or a cap);
+ *              the largest slab that fits in ws_bytes is used.
+ */
+vce_status lce_backward(const void* X, const void* W, int64_t n, int64_t h, int64_t v,
+                        const int64_t* target, const float* lse, const int64_t* n_valid,
+                        const float* grad_output, float label_smoothing, int reduce_loss,
+                        int64_t ignore_idx, void* dX, void* dW, void* ws, size_t ws_bytes,
+                        int* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VCE_H */

@@ -1,0 +1,264 @@
+"""Logits form on the GPU against the FP64 oracle (Transformer Engine
+parallel_cross_entropy semantics).  Tolerances:
+
+* FP32 logits: per-row loss |d| <= 1e-5 max(|ref|, 1), dlogits tensor-wise
+  ||d|| <= 1e-5 ||ref||;
+* BF16 logits: loss |d| <= 2e-3 (per row and the mean), dlogits norm-wise
+  ||d|| / ||ref|| <= 1e-2 (BF16 output rounding is 2^-9 relative);
+* ignore masks (zero loss, zero gradient rows) and N_v: bit-exact.
+"""
+import math
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wk
+import vocabulary_cross_entropy_gb300 as vce
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from vocabulary_cross_entropy_gb300 import build
+    build.build()
+
+
+def to_dev(logits_np, dtype):
+    if dtype == "bf16":
+        return torch.from_numpy(logits_np.view(np.int16)).to(DEV).view(torch.bfloat16)
+    return torch.from_numpy(logits_np).to(DEV)
+
+
+def bf16_np(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def run_gpu(logits, target, eps, red, grad, ignore_idx=-100, inplace=False, dlogits=None):
+    tgt = torch.from_numpy(target).to(DEV)
+    f = vce.ce_forward(logits, tgt, eps, red, ignore_idx)
+    g = torch.from_numpy(np.asarray(grad, np.float32)).to(DEV)
+    dz = vce.ce_backward(logits, tgt, f.stats, f.n_valid, g, eps, red, ignore_idx, inplace=inplace,
+                         dlogits=dlogits)
+    torch.cuda.synchronize()
+    return f, dz
+
+
+def dz_np(dz, dtype):
+    return oracle.widen(bf16_np(dz), "bf16") if dtype == "bf16" else dz.double().cpu().numpy()
+
+
+def check_rows(f, dz, ref_f, ref_dz, rows, dtype, red, target):
+    loss_tol_rel = 1e-5 if dtype == "f32" else 0.0
+    loss_tol_abs = 0.0 if dtype == "f32" else 2e-3
+    stats = f.stats.double().cpu().numpy()
+    valid = target[rows] != -100
+    if not red:
+        got = f.loss.double().cpu().numpy().reshape(-1)[rows]
+        ref = ref_f["loss_rows"]
+        assert np.all(got[~valid] == 0.0)
+        err = np.abs(got - ref)
+        # relative with a floor of 1 nat: a near-zero loss has no meaningful relative error
+        assert np.all(err <= loss_tol_abs + loss_tol_rel * np.maximum(np.abs(ref), 1.0)), err.max()
+    # statistics: max is an exact max of stored values; lse within loss tolerance
+    np.testing.assert_array_equal(stats[rows][valid, 0], ref_f["m"][valid])
+    np.testing.assert_allclose(stats[rows][valid, 1], ref_f["lse"][valid],
+                               rtol=loss_tol_rel, atol=loss_tol_abs + 1e-30)
+    assert np.all(stats[rows][~valid] == 0.0)
+    got_dz = dz_np(dz, dtype)[rows] if dz.shape[0] != len(rows) else dz_np(dz, dtype)
+    assert np.all(got_dz[~valid] == 0.0)
+    if dtype == "f32":
+        # tensor-wise relative error: a single row can be nearly zero (prediction
+        # close to the smoothed target) and there FP32 lse rounding alone exceeds 1e-5
+        err = np.linalg.norm(got_dz - ref_dz)
+        assert err <= 1e-5 * np.linalg.norm(ref_dz) + 1e-12, err / np.linalg.norm(ref_dz)
+    else:
+        # norm-wise; the absolute floor covers an all-zero reference (V = 1), where
+        # only FP32 rounding of the exponent argument z*log2(e) - lse*log2(e) remains
+        err = np.linalg.norm(got_dz - ref_dz)
+        assert err <= 1e-2 * np.linalg.norm(ref_dz) + 1e-6, (err, np.linalg.norm(ref_dz))
+
+
+# ---------------------------------------------------------------------------
+# tiny FP32 workload: N=128, V=1024, z ~ N(0, 2^2), 10% ignored
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("wl", wk.LOGITS_TINY, ids=lambda w: w.name)
+def test_tiny_fp32_full(wl):
+    inp = wk.make_logits_inputs(wl)
+    logits = to_dev(inp.logits, wl.dtype)
+    f, dz = run_gpu(logits, inp.target, wl.label_smoothing, wl.reduce_loss, inp.grad)
+    ref = oracle.ce_forward(inp.logits, inp.target, wl.label_smoothing, wl.reduce_loss)
+    ref_dz = oracle.ce_backward(inp.logits, inp.target, ref["lse"], ref["n_valid"], inp.grad,
+                                wl.label_smoothing, wl.reduce_loss)
+    assert int(f.n_valid.item()) == ref["n_valid"]
+    assert int(f.dev_status.item()) == 0
+    if wl.reduce_loss:
+        assert abs(f.loss.item() - ref["loss"]) <= 1e-5 * abs(ref["loss"])
+    rows = np.arange(wl.n_rows)
+    check_rows(f, dz, ref, ref_dz, rows, wl.dtype, wl.reduce_loss, inp.target)
+
+
+# ---------------------------------------------------------------------------
+# edge shapes: ragged / odd V, padded and misaligned rows, N = 1, both dtypes
+# ---------------------------------------------------------------------------
+
+EDGE = [
+    # (n, vocab, pad, dtype, eps, reduce)
+    (1, 1, 0, "f32", 0.0, False),
+    (3, 1, 0, "bf16", 0.1, True),
+    (5, 7, 0, "f32", 0.1, False),
+    (127, 7, 3, "bf16", 0.0, True),
+    (64, 1000, 0, "bf16", 0.1, False),
+    (33, 32001, 0, "bf16", 0.1, True),
+    (17, 32001, 5, "f32", 0.0, False),
+    (9, 128257, 0, "bf16", 0.1, True),
+    (4097, 129, 0, "f32", 0.1, True),
+    (6, 262144, 0, "bf16", 0.0, False),
+]
+
+
+@pytest.mark.parametrize("n,vocab,pad,dtype,eps,red", EDGE)
+def test_edge_shapes(n, vocab, pad, dtype, eps, red):
+    seed = n * 7 + vocab
+    stride = vocab + pad
+    full = wk.normal_matrix(seed, wk.TID_LOGITS, n, stride, 3.0, dtype == "bf16")
+    target = wk.uniform_targets(seed, n, vocab, 0.1)
+    grad = np.ones(1, np.float32) if red else wk.grad_rows(seed, n)
+    dev_full = to_dev(full, dtype)
+    logits = dev_full[:, :vocab]
+    dz_full = torch.full_like(dev_full, 7.0)
+    f, dz = run_gpu(logits, target, eps, red, grad, dlogits=dz_full[:, :vocab])
+    z = full[:, :vocab]
+    ref = oracle.ce_forward(z, target, eps, red, dtype=dtype)
+    ref_dz = oracle.ce_backward(z, target, ref["lse"], ref["n_valid"], grad, eps, red, dtype=dtype)
+    assert int(f.n_valid.item()) == ref["n_valid"]
+    assert int(f.dev_status.item()) == 0
+    if red and ref["n_valid"] > 0:
+        tol = 1e-5 * abs(ref["loss"]) if dtype == "f32" else 2e-3
+        assert abs(f.loss.item() - ref["loss"]) <= tol
+    check_rows(f, dz, ref, ref_dz, np.arange(n), dtype, red, target)
+    # the padding columns between rows are untouched by backward
+    if pad:
+        assert torch.all(dz_full[:, vocab:] == 7.0).item()
+
+
+def test_inplace_backward_matches_out_of_place():
+    n, vocab = 300, 50257
+    z = wk.normal_matrix(5, wk.TID_LOGITS, n, vocab, 3.0, True)
+    target = wk.uniform_targets(5, n, vocab, 0.05)
+    a = to_dev(z, "bf16")
+    b = a.clone()
+    fa, dza = run_gpu(a, target, 0.1, True, np.ones(1, np.float32))
+    fb, dzb = run_gpu(b, target, 0.1, True, np.ones(1, np.float32), inplace=True)
+    assert dzb.data_ptr() == b.data_ptr()
+    assert torch.equal(dza.view(torch.int16), dzb.view(torch.int16))
+    assert torch.equal(fa.stats, fb.stats)
+
+
+def test_all_ignored_gives_nan_and_zero_gradient():
+    n, vocab = 8, 333
+    z = wk.normal_matrix(1, wk.TID_LOGITS, n, vocab, 1.0, False)
+    target = np.full(n, -100, np.int64)
+    f, dz = run_gpu(to_dev(z, "f32"), target, 0.1, True, np.ones(1, np.float32))
+    assert int(f.n_valid.item()) == 0
+    assert math.isnan(f.loss.item())
+    assert torch.count_nonzero(dz).item() == 0
+
+
+def test_custom_ignore_index():
+    n, vocab = 40, 999
+    z = wk.normal_matrix(2, wk.TID_LOGITS, n, vocab, 2.0, True)
+    target = wk.uniform_targets(2, n, vocab, 0.0)
+    target[::3] = 5
+    f, dz = run_gpu(to_dev(z, "bf16"), target, 0.0, True, np.ones(1, np.float32), ignore_idx=5)
+    ref = oracle.ce_forward(z, target, 0.0, True, ignore_idx=5, dtype="bf16")
+    assert int(f.n_valid.item()) == ref["n_valid"]
+    assert abs(f.loss.item() - ref["loss"]) <= 2e-3
+    assert torch.count_nonzero(dz[::3].float()).item() == 0
+
+
+def test_bad_target_sets_status_and_nan():
+    n, vocab = 6, 100
+    z = wk.normal_matrix(3, wk.TID_LOGITS, n, vocab, 1.0, False)
+    target = np.array([1, 100, -1, -100, 99, 0], np.int64)
+    f, dz = run_gpu(to_dev(z, "f32"), target, 0.0, False, np.ones(n, np.float32))
+    loss = f.loss.cpu().numpy()
+    assert int(f.dev_status.item()) & vce.DEVSTATUS_BAD_TARGET
+    assert math.isnan(loss[1]) and math.isnan(loss[2]) and loss[3] == 0.0
+    assert np.isfinite(loss[[0, 4, 5]]).all()
+    assert torch.count_nonzero(dz[1:4]).item() == 0
+    assert int(f.n_valid.item()) == 5
+
+
+def test_zero_rows_reduce():
+    z = torch.empty(0, 10, device=DEV, dtype=torch.float32)
+    t = torch.empty(0, dtype=torch.int64, device=DEV)
+    f = vce.ce_forward(z, t, 0.0, True)
+    torch.cuda.synchronize()
+    assert int(f.n_valid.item()) == 0 and math.isnan(f.loss.item())
+
+
+def test_layout_sq_b_v_matches_flattened():
+    sq, b, vocab = 16, 3, 4099
+    z = wk.normal_matrix(4, wk.TID_LOGITS, sq * b, vocab, 3.0, True)
+    target = wk.uniform_targets(4, sq * b, vocab, 0.1)
+    t3 = to_dev(z, "bf16").view(sq, b, vocab)
+    tt = torch.from_numpy(target).to(DEV).view(sq, b)
+    f3 = vce.ce_forward(t3, tt.reshape(-1), 0.1, False)
+    f2 = vce.ce_forward(t3.view(-1, vocab), tt.reshape(-1), 0.1, False)
+    torch.cuda.synchronize()
+    assert f3.loss.shape == (sq, b)
+    assert torch.equal(f3.loss.reshape(-1), f2.loss)
+
+
+# ---------------------------------------------------------------------------
+# full-size memory-bound workload: B=4, SQ=4096, V=128256 BF16, 5% ignored
+# (the launch configuration the benchmark times); sampled rows + exact mean
+# ---------------------------------------------------------------------------
+
+def _oracle_rows_chunked(wl, target, rows_per_chunk=128):
+    """Per-row FP64 oracle loss for every row of the workload (rows regenerated in chunks)."""
+    n = wl.n_rows
+
+    def chunk(r0):
+        r1 = min(n, r0 + rows_per_chunk)
+        z = wk.logits_rows(wl, np.arange(r0, r1))
+        return oracle.ce_forward(z, target[r0:r1], wl.label_smoothing, False, dtype=wl.dtype)["loss_rows"]
+
+    with ThreadPoolExecutor(16) as ex:
+        parts = list(ex.map(chunk, range(0, n, rows_per_chunk)))
+    return np.concatenate(parts)
+
+
+def test_membound_full_size_sampled():
+    wl = wk.LOGITS_MEMBOUND
+    inp = wk.make_logits_inputs(wl)
+    logits = to_dev(inp.logits, wl.dtype)
+    del inp.logits
+    f, dz = run_gpu(logits, inp.target, wl.label_smoothing, wl.reduce_loss, inp.grad)
+    n_valid_ref = int((inp.target != -100).sum())
+    assert int(f.n_valid.item()) == n_valid_ref
+    assert int(f.dev_status.item()) == 0
+    # mean over every row, in FP64
+    loss_rows = _oracle_rows_chunked(wl, inp.target)
+    mean_ref = oracle.mean_loss(loss_rows, n_valid_ref)
+    assert abs(f.loss.item() - mean_ref) <= 2e-3
+    # ignore mask of the gradient: every ignored row is exactly zero
+    ign = torch.from_numpy(inp.target == -100).to(DEV)
+    assert torch.count_nonzero(dz[ign]).item() == 0
+    # sampled rows, compared element by element
+    rng = np.random.default_rng(0)
+    rows = np.unique(np.concatenate([rng.choice(wl.n_rows, 48, replace=False),
+                                     np.nonzero(inp.target == -100)[0][:4], [0, wl.n_rows - 1]]))
+    z = wk.logits_rows(wl, rows)
+    ref = oracle.ce_forward(z, inp.target[rows], wl.label_smoothing, False, dtype=wl.dtype)
+    ref_dz = oracle.ce_backward(z, inp.target[rows], ref["lse"], n_valid_ref, inp.grad,
+                                wl.label_smoothing, True, dtype=wl.dtype)
+    sel = torch.from_numpy(rows).to(DEV)
+    check_rows(f._replace(stats=f.stats), dz[sel], ref, ref_dz, rows, wl.dtype, True, inp.target)

@@ -1,0 +1,27 @@
+"""GB300-native vocabulary cross entropy: a thin Python binding over libvce.so.
+
+The functions here carry the names of the C ABI in ``include/vce.h`` and do
+argument marshalling only: torch tensors supply device memory and the current
+CUDA stream, every step of the computation runs in the library's sm_103a
+kernels.  There is no CPU or PyTorch fallback: if libvce.so is missing or the
+device is not a GB300 the calls raise.
+
+Build the library with ``python -m vocabulary_cross_entropy_gb300.build``.
+"""
+from ._binding import (  # noqa: F401
+    VceError,
+    BF16,
+    F32,
+    DEVSTATUS_BAD_TARGET,
+    DEVSTATUS_TIMEOUT,
+    library,
+    library_path,
+    vce_status_string,
+    vce_version,
+    ce_workspace_size,
+    ce_forward,
+    ce_backward,
+    lce_workspace_size,
+    lce_forward,
+    lce_backward,
+)

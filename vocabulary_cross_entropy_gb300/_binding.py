@@ -1,0 +1,250 @@
+"""ctypes marshalling between torch tensors and the C ABI of libvce.so."""
+from __future__ import annotations
+
+import ctypes
+import os
+from collections import namedtuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_HERE, "libvce.so")
+
+BF16 = 0
+F32 = 1
+DEVSTATUS_BAD_TARGET = 1
+DEVSTATUS_TIMEOUT = 2
+
+_c_i64 = ctypes.c_int64
+_c_int = ctypes.c_int
+_c_f32 = ctypes.c_float
+_c_p = ctypes.c_void_p
+_c_size = ctypes.c_size_t
+
+_lib = None
+
+
+class VceError(RuntimeError):
+    def __init__(self, func: str, status: int):
+        self.status = status
+        super().__init__(f"{func} failed: {vce_status_string(status)} ({status})")
+
+
+def library() -> ctypes.CDLL:
+    """Load libvce.so (raises if it has not been built: there is no fallback)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(library_path):
+        raise ImportError(f"{library_path} is missing; build it with "
+                          "`python -m vocabulary_cross_entropy_gb300.build`")
+    lib = ctypes.CDLL(library_path)
+    lib.vce_status_string.argtypes = [_c_int]
+    lib.vce_status_string.restype = ctypes.c_char_p
+    lib.vce_version.argtypes = []
+    lib.vce_version.restype = _c_int
+    lib.ce_workspace_size.argtypes = [_c_i64, _c_i64, _c_int]
+    lib.ce_workspace_size.restype = _c_size
+    lib.ce_forward.argtypes = [_c_p, _c_int, _c_i64, _c_i64, _c_i64, _c_p, _c_f32, _c_int, _c_i64,
+                               _c_p, _c_p, _c_p, _c_p, _c_size, _c_p, _c_p]
+    lib.ce_forward.restype = _c_int
+    lib.ce_backward.argtypes = [_c_p, _c_int, _c_i64, _c_i64, _c_i64, _c_p, _c_p, _c_p, _c_p, _c_f32,
+                                _c_int, _c_i64, _c_p, _c_p, _c_p]
+    lib.ce_backward.restype = _c_int
+    lib.lce_workspace_size.argtypes = [_c_i64, _c_i64, _c_i64, _c_int, _c_size]
+    lib.lce_workspace_size.restype = _c_size
+    lib.lce_forward.argtypes = [_c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_f32, _c_int, _c_i64,
+                                _c_p, _c_p, _c_p, _c_p, _c_size, _c_p, _c_p]
+    lib.lce_forward.restype = _c_int
+    lib.lce_backward.argtypes = [_c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_p, _c_p, _c_p, _c_f32,
+                                 _c_int, _c_i64, _c_p, _c_p, _c_p, _c_size, _c_p, _c_p]
+    lib.lce_backward.restype = _c_int
+    _lib = lib
+    return lib
+
+
+def vce_status_string(status: int) -> str:
+    return library().vce_status_string(int(status)).decode()
+
+
+def vce_version() -> int:
+    return int(library().vce_version())
+
+
+def _check(func: str, status: int):
+    if status != 0:
+        raise VceError(func, status)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device, stream):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"logits must be bfloat16 or float32, got {t.dtype}")
+
+
+def _rows_view(logits: torch.Tensor):
+    """(n_rows, vocab, row_stride) of a [..., V] tensor whose rows have one stride."""
+    if logits.dim() < 1 or logits.stride(-1) != 1:
+        raise ValueError("logits must be contiguous along the vocabulary dimension")
+    vocab = logits.shape[-1]
+    if logits.dim() == 1:
+        return 1, vocab, vocab
+    flat = logits.view(-1, vocab) if logits.is_contiguous() else None
+    if flat is None:
+        try:
+            flat = logits.view(-1, vocab)
+        except RuntimeError:
+            raise ValueError("the leading dimensions of logits must flatten to one row stride")
+    return flat.shape[0], vocab, flat.stride(0) if flat.shape[0] > 1 else vocab
+
+
+def _target(target: torch.Tensor, n: int):
+    if target.dtype != torch.int64 or not target.is_contiguous() or target.numel() != n:
+        raise ValueError("target must be a contiguous int64 tensor with one entry per row")
+    return target
+
+
+CEForward = namedtuple("CEForward", "loss stats n_valid dev_status")
+LCEForward = namedtuple("LCEForward", "loss lse n_valid dev_status")
+LCEBackward = namedtuple("LCEBackward", "dX dW dev_status")
+
+
+def ce_workspace_size(n_rows: int, vocab: int, reduce_loss: bool) -> int:
+    return int(library().ce_workspace_size(n_rows, vocab, int(bool(reduce_loss))))
+
+
+def ce_forward(logits, target, label_smoothing=0.0, reduce_loss=False, ignore_idx=-100, *,
+               loss=None, stats=None, n_valid=None, workspace=None, dev_status=None, stream=None):
+    """Logits-form forward.  Returns (loss, stats [N, 2] = (max, lse), n_valid, dev_status)."""
+    lib = library()
+    dev = logits.device
+    n, vocab, stride = _rows_view(logits)
+    target = _target(target, n)
+    if loss is None:
+        loss = torch.empty(1 if reduce_loss else n, dtype=torch.float32, device=dev)
+    if stats is None:
+        stats = torch.empty(n, 2, dtype=torch.float32, device=dev)
+    if n_valid is None:
+        n_valid = torch.empty(1, dtype=torch.int64, device=dev)
+    if dev_status is None:
+        dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws_bytes = ce_workspace_size(n, vocab, reduce_loss)
+    if workspace is None and ws_bytes:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        st = lib.ce_forward(_ptr(logits), _dtype_code(logits), n, vocab, stride, _ptr(target),
+                            float(label_smoothing), int(bool(reduce_loss)), int(ignore_idx),
+                            _ptr(loss), _ptr(stats), _ptr(n_valid), _ptr(workspace),
+                            0 if workspace is None else workspace.numel() * workspace.element_size(),
+                            _ptr(dev_status), _stream(dev, stream))
+    _check("ce_forward", st)
+    return CEForward(loss if reduce_loss else loss.view(logits.shape[:-1]), stats, n_valid, dev_status)
+
+
+def ce_backward(logits, target, stats, n_valid, grad_output, label_smoothing=0.0, reduce_loss=False,
+                ignore_idx=-100, *, dlogits=None, inplace=False, dev_status=None, stream=None):
+    """Logits-form backward: dlogits (written over ``logits`` when ``inplace``)."""
+    lib = library()
+    dev = logits.device
+    n, vocab, stride = _rows_view(logits)
+    target = _target(target, n)
+    if inplace:
+        dlogits = logits
+    elif dlogits is None:
+        dlogits = torch.empty_like(logits)
+    if dlogits.stride() != logits.stride() or dlogits.dtype != logits.dtype:
+        raise ValueError("dlogits must have the dtype and strides of logits")
+    grad_output = grad_output.to(device=dev, dtype=torch.float32).contiguous()
+    if dev_status is None:
+        dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        st = lib.ce_backward(_ptr(logits), _dtype_code(logits), n, vocab, stride, _ptr(target),
+                             _ptr(stats), _ptr(n_valid), _ptr(grad_output), float(label_smoothing),
+                             int(bool(reduce_loss)), int(ignore_idx), _ptr(dlogits),
+                             _ptr(dev_status), _stream(dev, stream))
+    _check("ce_backward", st)
+    return dlogits
+
+
+def _bf16_2d(t, name):
+    if t.dtype != torch.bfloat16 or t.dim() != 2 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous 2-D bfloat16 tensor")
+    return t
+
+
+def lce_workspace_size(n: int, h: int, v: int, reduce_loss: bool, max_slab_bytes: int = 0) -> int:
+    return int(library().lce_workspace_size(n, h, v, int(bool(reduce_loss)), int(max_slab_bytes)))
+
+
+def lce_forward(X, W, target, label_smoothing=0.0, reduce_loss=False, ignore_idx=-100, *,
+                loss=None, lse=None, n_valid=None, workspace=None, dev_status=None, stream=None):
+    """Linear-form forward.  Returns (loss, lse [N], n_valid, dev_status)."""
+    lib = library()
+    X = _bf16_2d(X, "X")
+    W = _bf16_2d(W, "W")
+    n, h = X.shape
+    v = W.shape[0]
+    if W.shape[1] != h:
+        raise ValueError("X and W must share the hidden dimension")
+    dev = X.device
+    target = _target(target, n)
+    if loss is None:
+        loss = torch.empty(1 if reduce_loss else n, dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty(n, dtype=torch.float32, device=dev)
+    if n_valid is None:
+        n_valid = torch.empty(1, dtype=torch.int64, device=dev)
+    if dev_status is None:
+        dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(1, lce_workspace_size(n, h, v, reduce_loss)), dtype=torch.uint8,
+                                device=dev)
+    with torch.cuda.device(dev):
+        st = lib.lce_forward(_ptr(X), _ptr(W), n, h, v, _ptr(target), float(label_smoothing),
+                             int(bool(reduce_loss)), int(ignore_idx), _ptr(loss), _ptr(lse),
+                             _ptr(n_valid), _ptr(workspace), workspace.numel(), _ptr(dev_status),
+                             _stream(dev, stream))
+    _check("lce_forward", st)
+    return LCEForward(loss, lse, n_valid, dev_status)
+
+
+def lce_backward(X, W, target, lse, n_valid, grad_output, label_smoothing=0.0, reduce_loss=False,
+                 ignore_idx=-100, *, dX=None, dW=None, workspace=None, max_slab_bytes=0,
+                 dev_status=None, stream=None):
+    """Linear-form backward.  Returns (dX [N, H], dW [V, H], dev_status), both bfloat16."""
+    lib = library()
+    X = _bf16_2d(X, "X")
+    W = _bf16_2d(W, "W")
+    n, h = X.shape
+    v = W.shape[0]
+    dev = X.device
+    target = _target(target, n)
+    if dX is None:
+        dX = torch.empty_like(X)
+    if dW is None:
+        dW = torch.empty_like(W)
+    grad_output = grad_output.to(device=dev, dtype=torch.float32).contiguous()
+    if dev_status is None:
+        dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(1, lce_workspace_size(n, h, v, reduce_loss, max_slab_bytes)),
+                                dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        st = lib.lce_backward(_ptr(X), _ptr(W), n, h, v, _ptr(target), _ptr(lse), _ptr(n_valid),
+                              _ptr(grad_output), float(label_smoothing), int(bool(reduce_loss)),
+                              int(ignore_idx), _ptr(dX), _ptr(dW), _ptr(workspace), workspace.numel(),
+                              _ptr(dev_status), _stream(dev, stream))
+    _check("lce_backward", st)
+    return LCEBackward(dX, dW, dev_status)

@@ -1,0 +1,426 @@
+// Logits-form cross entropy: memory-bound row kernels for sm_103a.
+//
+// Forward (Transformer Engine parallel_cross_entropy, API card "Description":
+// fused online softmax + cross entropy, FP32 loss for BF16/FP32 logits; pull
+// request #3273 "Changes": the single-GPU path is one forward kernel that
+// saves per-row statistics instead of the derivative):
+//   one CTA per row streams the row once with 16-byte vector loads, keeps a
+//   running (max, sum of exp) per thread, merges them with warp shuffles and a
+//   shared-memory pass, and writes the row loss and (max, lse).
+// Backward (same pull request: the gradient is rebuilt from the saved stats):
+//   one CTA per row streams the logits once more and writes
+//   dz = g (exp(z - lse) - (1 - eps) onehot(y) - eps / V), zeros for ignored rows.
+// Mean reduction: one CTA sums the per-row losses in a fixed order (run to run
+// identical) and counts the rows whose target is not ignore_idx.
+
+#include "vce_internal.cuh"
+
+#include <math.h>
+
+namespace vce {
+namespace {
+
+// ---------------------------------------------------------------------------
+// element access
+// ---------------------------------------------------------------------------
+
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+    static constexpr int kVec = 4;  // elements per 16-byte vector
+    __device__ static float load1(const float* p) { return __ldcs(p); }
+    __device__ static void unpack(const uint4& u, float (&v)[4]) {
+        v[0] = __uint_as_float(u.x); v[1] = __uint_as_float(u.y);
+        v[2] = __uint_as_float(u.z); v[3] = __uint_as_float(u.w);
+    }
+    __device__ static uint4 pack(const float (&v)[4]) {
+        return make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]),
+                          __float_as_uint(v[2]), __float_as_uint(v[3]));
+    }
+    __device__ static void store1(float* p, float x) { *p = x; }
+};
+template <> struct Elem<__nv_bfloat16> {
+    static constexpr int kVec = 8;
+    __device__ static float load1(const __nv_bfloat16* p) {
+        unsigned short b = __ldcs(reinterpret_cast<const unsigned short*>(p));
+        return __uint_as_float(uint32_t(b) << 16);
+    }
+    __device__ static void unpack(const uint4& u, float (&v)[8]) {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[2 * i] = __uint_as_float(w[i] << 16);
+            v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    }
+    __device__ static uint32_t pack2(float lo, float hi) {
+        __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&b);
+    }
+    __device__ static uint4 pack(const float (&v)[8]) {
+        return make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]));
+    }
+    __device__ static void store1(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+};
+
+// Split of a row into a scalar head (up to the first 16-byte boundary), whole
+// 16-byte vectors and a scalar tail.
+template <typename T>
+struct RowSplit {
+    int64_t head, nvec, tail0;
+    __device__ RowSplit(const T* p, int64_t vocab) {
+        const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+        head = int64_t((16 - (a & 15)) & 15) / int64_t(sizeof(T));
+        if (head > vocab) head = vocab;
+        nvec = (vocab - head) / Elem<T>::kVec;
+        tail0 = head + nvec * Elem<T>::kVec;
+    }
+};
+
+// ---------------------------------------------------------------------------
+// online softmax accumulator: s = sum exp(z - m) over the values seen
+// ---------------------------------------------------------------------------
+
+struct OnlineLse {
+    float m = -INFINITY;   // running max
+    float negm = 0.f;      // -m * log2(e), 0 while m = -inf
+    float s = 0.f;         // sum of exp(z - m)
+    float sum = 0.f;       // sum of z (label smoothing term)
+
+    template <int K, bool kSum>
+    __device__ __forceinline__ void push(const float (&v)[K]) {
+        float vm = v[0];
+#pragma unroll
+        for (int i = 1; i < K; ++i) vm = fmaxf(vm, v[i]);
+        if (vm > m) {
+            s = s * ex2f((m - vm) * kLog2e);  // s = 0 while m = -inf: stays 0
+            m = vm;
+            negm = -vm * kLog2e;
+        }
+        float t = 0.f;
+#pragma unroll
+        for (int i = 0; i < K; ++i) t += ex2f(fmaf(v[i], kLog2e, negm));
+        s += t;
+        if (kSum) {
+            float u = 0.f;
+#pragma unroll
+            for (int i = 0; i < K; ++i) u += v[i];
+            sum += u;
+        }
+    }
+
+    // merge another (m2, s2) pair into this one
+    __device__ __forceinline__ void merge(float m2, float s2, float sum2) {
+        const float mn = fmaxf(m, m2);
+        sum += sum2;
+        if (mn == -INFINITY) { m = mn; s = 0.f; return; }
+        s = s * ex2f((m - mn) * kLog2e) + s2 * ex2f((m2 - mn) * kLog2e);
+        m = mn;
+    }
+};
+
+template <int THREADS, bool kSum>
+__device__ __forceinline__ void block_merge(OnlineLse& a, float* sm_m, float* sm_s, float* sm_sum) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, a.m, off);
+        const float s2 = __shfl_xor_sync(0xffffffffu, a.s, off);
+        const float u2 = kSum ? __shfl_xor_sync(0xffffffffu, a.sum, off) : 0.f;
+        a.merge(m2, s2, u2);
+    }
+    if (lane == 0) { sm_m[warp] = a.m; sm_s[warp] = a.s; sm_sum[warp] = a.sum; }
+    __syncthreads();
+    if (warp == 0) {
+        constexpr int W = THREADS / 32;
+        OnlineLse b;
+        if (lane < W) { b.m = sm_m[lane]; b.s = sm_s[lane]; b.sum = sm_sum[lane]; }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float m2 = __shfl_xor_sync(0xffffffffu, b.m, off);
+            const float s2 = __shfl_xor_sync(0xffffffffu, b.s, off);
+            const float u2 = kSum ? __shfl_xor_sync(0xffffffffu, b.sum, off) : 0.f;
+            b.merge(m2, s2, u2);
+        }
+        a = b;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// K1: forward row kernel
+// ---------------------------------------------------------------------------
+
+template <int THREADS, typename T, bool kSmooth>
+__global__ void __launch_bounds__(THREADS)
+ce_forward_rows(const T* __restrict__ logits, int64_t n_rows, int64_t vocab, int64_t stride,
+                const int64_t* __restrict__ target, float eps, int64_t ignore_idx,
+                float* __restrict__ loss_rows, float2* __restrict__ stats, int* dev_status) {
+    using E = Elem<T>;
+    constexpr int V = E::kVec;
+    constexpr int U = 4;  // vectors in flight per thread per iteration
+    __shared__ float sm_m[32], sm_s[32], sm_sum[32];
+
+    for (int64_t row = blockIdx.x; row < n_rows; row += gridDim.x) {
+        const int64_t y = target[row];
+        if (y == ignore_idx) {
+            if (threadIdx.x == 0) {
+                loss_rows[row] = 0.f;
+                stats[row] = make_float2(0.f, 0.f);
+            }
+            continue;
+        }
+        const T* p = logits + row * stride;
+        const RowSplit<T> sp(p, vocab);
+        OnlineLse acc;
+        if (threadIdx.x < sp.head) {
+            float v[1] = {E::load1(p + threadIdx.x)};
+            acc.push<1, kSmooth>(v);
+        }
+        const uint4* pv = reinterpret_cast<const uint4*>(p + sp.head);
+        int64_t i = threadIdx.x;
+        for (; i + (U - 1) * THREADS < sp.nvec; i += U * THREADS) {
+            uint4 raw[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) raw[u] = __ldcs(pv + i + u * THREADS);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                float v[V];
+                E::unpack(raw[u], v);
+                acc.push<V, kSmooth>(v);
+            }
+        }
+        for (; i < sp.nvec; i += THREADS) {
+            float v[V];
+            E::unpack(__ldcs(pv + i), v);
+            acc.push<V, kSmooth>(v);
+        }
+        for (int64_t j = sp.tail0 + threadIdx.x; j < vocab; j += THREADS) {
+            float v[1] = {E::load1(p + j)};
+            acc.push<1, kSmooth>(v);
+        }
+        block_merge<THREADS, kSmooth>(acc, sm_m, sm_s, sm_sum);
+        if (threadIdx.x == 0) {
+            const float lse = acc.m + logf(acc.s);
+            float loss;
+            if (y >= 0 && y < vocab) {
+                const float zy = E::load1(p + y);
+                loss = lse - zy;
+                if (kSmooth) loss = (1.f - eps) * loss + eps * (lse - acc.sum / float(vocab));
+            } else {
+                loss = __int_as_float(0x7fc00000);  // NaN
+                report(dev_status, VCE_DEVSTATUS_BAD_TARGET);
+            }
+            loss_rows[row] = loss;
+            stats[row] = make_float2(acc.m, lse);
+        }
+        __syncthreads();  // shared scratch reused by the next row
+    }
+}
+
+// ---------------------------------------------------------------------------
+// K2: backward row kernel (dlogits may alias logits)
+// ---------------------------------------------------------------------------
+
+template <int THREADS, typename T>
+__global__ void __launch_bounds__(THREADS)
+ce_backward_rows(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride,
+                 const int64_t* __restrict__ target, const float2* __restrict__ stats,
+                 const int64_t* __restrict__ n_valid, const float* __restrict__ grad_output,
+                 float eps, int reduce_loss, int64_t ignore_idx, T* dlogits, int* dev_status) {
+    using E = Elem<T>;
+    constexpr int V = E::kVec;
+    constexpr int U = 2;
+
+    for (int64_t row = blockIdx.x; row < n_rows; row += gridDim.x) {
+        const int64_t y = target[row];
+        T* q = dlogits + row * stride;
+        const T* p = logits + row * stride;
+        const RowSplit<T> sp(q, vocab);
+        const bool ignored = (y == ignore_idx);
+        const bool bad = !ignored && (y < 0 || y >= vocab);
+        if (ignored || bad) {
+            if (bad && threadIdx.x == 0) report(dev_status, VCE_DEVSTATUS_BAD_TARGET);
+            if (threadIdx.x < sp.head) E::store1(q + threadIdx.x, 0.f);
+            uint4* qv = reinterpret_cast<uint4*>(q + sp.head);
+            for (int64_t i = threadIdx.x; i < sp.nvec; i += THREADS) qv[i] = make_uint4(0, 0, 0, 0);
+            for (int64_t j = sp.tail0 + threadIdx.x; j < vocab; j += THREADS) E::store1(q + j, 0.f);
+            continue;
+        }
+        const float g = reduce_loss ? grad_output[0] / float(n_valid[0]) : grad_output[row];
+        const float negl = -stats[row].y * kLog2e;
+        const float b = g * eps / float(vocab);   // eps / V share of every class
+        const float c = g * (1.f - eps);          // target class
+
+        auto grad1 = [&](int64_t j) {
+            const float z = E::load1(p + j);
+            float d = fmaf(g, ex2f(fmaf(z, kLog2e, negl)), -b);
+            if (j == y) d -= c;
+            E::store1(q + j, d);
+        };
+        if (threadIdx.x < sp.head) grad1(threadIdx.x);
+        const uint4* pv = reinterpret_cast<const uint4*>(p + sp.head);
+        uint4* qv = reinterpret_cast<uint4*>(q + sp.head);
+        auto gradv = [&](const uint4& raw, int64_t i) {
+            float v[V];
+            E::unpack(raw, v);
+#pragma unroll
+            for (int k = 0; k < V; ++k) v[k] = fmaf(g, ex2f(fmaf(v[k], kLog2e, negl)), -b);
+            const int64_t base = sp.head + i * V;
+            if (uint64_t(y - base) < uint64_t(V)) {
+#pragma unroll
+                for (int k = 0; k < V; ++k) v[k] -= (base + k == y) ? c : 0.f;
+            }
+            __stcs(qv + i, E::pack(v));
+        };
+        int64_t i = threadIdx.x;
+        for (; i + (U - 1) * THREADS < sp.nvec; i += U * THREADS) {
+            uint4 raw[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) raw[u] = __ldcs(pv + i + u * THREADS);
+#pragma unroll
+            for (int u = 0; u < U; ++u) gradv(raw[u], i + u * THREADS);
+        }
+        for (; i < sp.nvec; i += THREADS) gradv(__ldcs(pv + i), i);
+        for (int64_t j = sp.tail0 + threadIdx.x; j < vocab; j += THREADS) grad1(j);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// K8: mean over non-ignored rows (fixed summation order)
+// ---------------------------------------------------------------------------
+
+constexpr int kMeanThreads = 1024;
+
+__global__ void __launch_bounds__(kMeanThreads)
+mean_loss_kernel(const float* __restrict__ loss_rows, const int64_t* __restrict__ target,
+                 int64_t n, int64_t ignore_idx, float* __restrict__ loss_out,
+                 int64_t* __restrict__ n_valid) {
+    __shared__ double sm_s[32];
+    __shared__ long long sm_c[32];
+    double s = 0.0;
+    long long c = 0;
+    for (int64_t i = threadIdx.x; i < n; i += kMeanThreads) {
+        if (loss_rows) s += double(loss_rows[i]);
+        c += (target[i] != ignore_idx) ? 1 : 0;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        s += __shfl_xor_sync(0xffffffffu, s, off);
+        c += __shfl_xor_sync(0xffffffffu, c, off);
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) { sm_s[warp] = s; sm_c[warp] = c; }
+    __syncthreads();
+    if (warp == 0) {
+        s = sm_s[lane];
+        c = sm_c[lane];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            s += __shfl_xor_sync(0xffffffffu, s, off);
+            c += __shfl_xor_sync(0xffffffffu, c, off);
+        }
+        if (lane == 0) {
+            if (loss_out) loss_out[0] = float(s / double(c));  // 0/0 = NaN when every row is ignored
+            if (n_valid) n_valid[0] = c;
+        }
+    }
+}
+
+template <typename T, int THREADS>
+void fwd_launch(const void* logits, int64_t n_rows, int64_t vocab, int64_t stride,
+                const int64_t* target, float eps, int64_t ignore_idx, float* loss_rows,
+                float* stats, int* dev_status, cudaStream_t s, int grid) {
+    if (eps != 0.f)
+        ce_forward_rows<THREADS, T, true><<<grid, THREADS, 0, s>>>(
+            static_cast<const T*>(logits), n_rows, vocab, stride, target, eps, ignore_idx,
+            loss_rows, reinterpret_cast<float2*>(stats), dev_status);
+    else
+        ce_forward_rows<THREADS, T, false><<<grid, THREADS, 0, s>>>(
+            static_cast<const T*>(logits), n_rows, vocab, stride, target, eps, ignore_idx,
+            loss_rows, reinterpret_cast<float2*>(stats), dev_status);
+}
+
+template <typename T>
+void fwd_dispatch(const void* logits, int64_t n_rows, int64_t vocab, int64_t stride,
+                  const int64_t* target, float eps, int64_t ignore_idx, float* loss_rows,
+                  float* stats, int* dev_status, cudaStream_t s, int grid) {
+    const int64_t nvec = vocab / Elem<T>::kVec;
+    if (nvec <= 1024)
+        fwd_launch<T, 128>(logits, n_rows, vocab, stride, target, eps, ignore_idx, loss_rows, stats, dev_status, s, grid);
+    else if (nvec <= 4096)
+        fwd_launch<T, 256>(logits, n_rows, vocab, stride, target, eps, ignore_idx, loss_rows, stats, dev_status, s, grid);
+    else
+        fwd_launch<T, 512>(logits, n_rows, vocab, stride, target, eps, ignore_idx, loss_rows, stats, dev_status, s, grid);
+}
+
+template <typename T>
+void bwd_dispatch(const void* logits, int64_t n_rows, int64_t vocab, int64_t stride,
+                  const int64_t* target, const float* stats, const int64_t* n_valid,
+                  const float* grad_output, float eps, int reduce_loss, int64_t ignore_idx,
+                  void* dlogits, int* dev_status, cudaStream_t s, int grid) {
+    const int64_t nvec = vocab / Elem<T>::kVec;
+    const T* z = static_cast<const T*>(logits);
+    T* dz = static_cast<T*>(dlogits);
+    const float2* st = reinterpret_cast<const float2*>(stats);
+    if (nvec <= 1024)
+        ce_backward_rows<128, T><<<grid, 128, 0, s>>>(z, n_rows, vocab, stride, target, st, n_valid,
+                                                       grad_output, eps, reduce_loss, ignore_idx, dz, dev_status);
+    else if (nvec <= 4096)
+        ce_backward_rows<256, T><<<grid, 256, 0, s>>>(z, n_rows, vocab, stride, target, st, n_valid,
+                                                       grad_output, eps, reduce_loss, ignore_idx, dz, dev_status);
+    else
+        ce_backward_rows<512, T><<<grid, 512, 0, s>>>(z, n_rows, vocab, stride, target, st, n_valid,
+                                                       grad_output, eps, reduce_loss, ignore_idx, dz, dev_status);
+}
+
+int row_grid(int64_t n_rows) {
+    const int64_t cap = int64_t(1) << 30;
+    return int(n_rows < cap ? n_rows : cap);
+}
+
+}  // namespace
+
+vce_status launch_mean_loss(const float* loss_rows, const int64_t* target, int64_t n_rows,
+                            int64_t ignore_idx, float* loss_out, int64_t* n_valid, cudaStream_t s) {
+    mean_loss_kernel<<<1, kMeanThreads, 0, s>>>(loss_rows, target, n_rows, ignore_idx, loss_out, n_valid);
+    return cudaGetLastError() == cudaSuccess ? VCE_OK : VCE_ERR_CUDA;
+}
+
+vce_status launch_ce_forward(const void* logits, int dtype, int64_t n_rows, int64_t vocab,
+                             int64_t row_stride, const int64_t* target, float eps,
+                             int reduce_loss, int64_t ignore_idx, float* loss, float* stats,
+                             int64_t* n_valid, void* ws, int* dev_status, cudaStream_t s,
+                             const DeviceInfo&) {
+    float* loss_rows = reduce_loss ? static_cast<float*>(ws) : loss;
+    if (n_rows > 0) {
+        const int grid = row_grid(n_rows);
+        if (dtype == VCE_BF16)
+            fwd_dispatch<__nv_bfloat16>(logits, n_rows, vocab, row_stride, target, eps, ignore_idx,
+                                        loss_rows, stats, dev_status, s, grid);
+        else
+            fwd_dispatch<float>(logits, n_rows, vocab, row_stride, target, eps, ignore_idx,
+                                loss_rows, stats, dev_status, s, grid);
+        if (cudaGetLastError() != cudaSuccess) return VCE_ERR_CUDA;
+    }
+    if (reduce_loss || n_valid)
+        return launch_mean_loss(reduce_loss ? loss_rows : nullptr, target, n_rows, ignore_idx,
+                                reduce_loss ? loss : nullptr, n_valid, s);
+    return VCE_OK;
+}
+
+vce_status launch_ce_backward(const void* logits, int dtype, int64_t n_rows, int64_t vocab,
+                              int64_t row_stride, const int64_t* target, const float* stats,
+                              const int64_t* n_valid, const float* grad_output, float eps,
+                              int reduce_loss, int64_t ignore_idx, void* dlogits,
+                              int* dev_status, cudaStream_t s, const DeviceInfo&) {
+    if (n_rows == 0) return VCE_OK;
+    const int grid = row_grid(n_rows);
+    if (dtype == VCE_BF16)
+        bwd_dispatch<__nv_bfloat16>(logits, n_rows, vocab, row_stride, target, stats, n_valid,
+                                    grad_output, eps, reduce_loss, ignore_idx, dlogits, dev_status, s, grid);
+    else
+        bwd_dispatch<float>(logits, n_rows, vocab, row_stride, target, stats, n_valid, grad_output,
+                            eps, reduce_loss, ignore_idx, dlogits, dev_status, s, grid);
+    return cudaGetLastError() == cudaSuccess ? VCE_OK : VCE_ERR_CUDA;
+}
+
+}  // namespace vce

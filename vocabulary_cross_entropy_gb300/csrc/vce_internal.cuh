@@ -1,0 +1,73 @@
+// Internal declarations shared by the translation units of libvce.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "../../include/vce.h"
+
+namespace vce {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Hardware base-2 exponential (MUFU.EX2 through the PTX instruction); relative
+// error of a few ulp, well inside the loss/gradient tolerances.
+__device__ __forceinline__ float ex2f(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ void report(int* dev_status, int bits) {
+    if (dev_status) atomicOr(dev_status, bits);
+}
+
+// Round up to a multiple of 256 bytes (workspace carving).
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Device properties cached per device ordinal.
+struct DeviceInfo {
+    int ordinal = -1;
+    int cc_major = 0, cc_minor = 0;
+    int num_sms = 0;
+    size_t max_smem_optin = 0;
+};
+
+// Returns VCE_OK and fills ``info`` for the current device, VCE_ERR_CUDA if the
+// runtime cannot be queried, VCE_ERR_ARCH if the device is not CC 10.3.
+vce_status current_device(DeviceInfo& info);
+
+// ---- logits form launchers (ce_rows.cu) ----
+vce_status launch_ce_forward(const void* logits, int dtype, int64_t n_rows, int64_t vocab,
+                             int64_t row_stride, const int64_t* target, float eps,
+                             int reduce_loss, int64_t ignore_idx, float* loss, float* stats,
+                             int64_t* n_valid, void* ws, int* dev_status, cudaStream_t s,
+                             const DeviceInfo& dev);
+vce_status launch_ce_backward(const void* logits, int dtype, int64_t n_rows, int64_t vocab,
+                              int64_t row_stride, const int64_t* target, const float* stats,
+                              const int64_t* n_valid, const float* grad_output, float eps,
+                              int reduce_loss, int64_t ignore_idx, void* dlogits,
+                              int* dev_status, cudaStream_t s, const DeviceInfo& dev);
+// mean of per-row losses over rows whose target is not ignore_idx, and the count
+vce_status launch_mean_loss(const float* loss_rows, const int64_t* target, int64_t n_rows,
+                            int64_t ignore_idx, float* loss_out, int64_t* n_valid,
+                            cudaStream_t s);
+
+// ---- linear form (lce_tc.cu) ----
+size_t lce_forward_ws_bytes(int64_t n, int64_t v, int reduce_loss);
+int64_t lce_slab_for_ws(int64_t n, int64_t h, int64_t v, size_t ws_bytes);
+size_t lce_backward_ws_bytes(int64_t n, int64_t h, int64_t v, int64_t slab);
+vce_status launch_lce_forward(const void* X, const void* W, int64_t n, int64_t h, int64_t v,
+                              const int64_t* target, float eps, int reduce_loss,
+                              int64_t ignore_idx, float* loss, float* lse, int64_t* n_valid,
+                              void* ws, int* dev_status, cudaStream_t s, const DeviceInfo& dev);
+vce_status launch_lce_backward(const void* X, const void* W, int64_t n, int64_t h, int64_t v,
+                               const int64_t* target, const float* lse, const int64_t* n_valid,
+                               const float* grad_output, float eps, int reduce_loss,
+                               int64_t ignore_idx, void* dX, void* dW, void* ws, int64_t slab,
+                               int* dev_status, cudaStream_t s, const DeviceInfo& dev);
+
+}  // namespace vce
