@@ -141,6 +141,30 @@ vce_status ce_backward(const void* logits, int dtype, int64_t n_rows, int64_t vo
                        float label_smoothing, int reduce_loss, int64_t ignore_idx,
                        void* dlogits, int* dev_status, void* stream);
 
+/*
+ * ce_forward for callers that cannot allocate device memory.  The pages have no
+ * counterpart of this call; it exists for callers that are handed only their
+ * inputs and outputs (a plugin inside another runtime's execution plan, or a
+ * deployment that forbids device allocation once it has started) and so cannot
+ * provide the workspace ce_forward asks for when reduce_loss != 0.
+ *
+ * Arguments and results are those of ce_forward without ws/ws_bytes.  The
+ * per-row loss scratch is a fixed array compiled into the library
+ * (VCE_NOALLOC_MAX_ROWS floats = 4 MiB), present on every GPU that loads the
+ * library until the process exits.  With reduce_loss != 0, n_rows above
+ * VCE_NOALLOC_MAX_ROWS returns VCE_ERR_WORKSPACE before any launch.  The call
+ * allocates and frees nothing.  The first call on each device looks up the
+ * array's device address (with that device current); make that first call
+ * before any stream capture.  All calls share the array: each call writes
+ * every slot it reads, so nothing needs clearing, but calls that overlap on
+ * the GPU (different streams or host threads) race on it.
+ */
+#define VCE_NOALLOC_MAX_ROWS 1048576
+vce_status ce_forward_noalloc(const void* logits, int dtype, int64_t n_rows, int64_t vocab,
+                              int64_t row_stride, const int64_t* target, float label_smoothing,
+                              int reduce_loss, int64_t ignore_idx, float* loss, float* stats,
+                              int64_t* n_valid, int* dev_status, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* linear form (X, W and the gradients are BF16; accumulation is FP32)      */
 /* ------------------------------------------------------------------------ */

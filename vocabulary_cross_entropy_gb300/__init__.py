@@ -20,6 +20,7 @@ from ._binding import (  # noqa: F401
     vce_version,
     ce_workspace_size,
     ce_forward,
+    ce_forward_noalloc,
     ce_backward,
     lce_workspace_size,
     lce_forward,

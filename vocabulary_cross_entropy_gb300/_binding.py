@@ -48,6 +48,9 @@ def library() -> ctypes.CDLL:
     lib.ce_forward.argtypes = [_c_p, _c_int, _c_i64, _c_i64, _c_i64, _c_p, _c_f32, _c_int, _c_i64,
                                _c_p, _c_p, _c_p, _c_p, _c_size, _c_p, _c_p]
     lib.ce_forward.restype = _c_int
+    lib.ce_forward_noalloc.argtypes = [_c_p, _c_int, _c_i64, _c_i64, _c_i64, _c_p, _c_f32, _c_int,
+                                       _c_i64, _c_p, _c_p, _c_p, _c_p, _c_p]
+    lib.ce_forward_noalloc.restype = _c_int
     lib.ce_backward.argtypes = [_c_p, _c_int, _c_i64, _c_i64, _c_i64, _c_p, _c_p, _c_p, _c_p, _c_f32,
                                 _c_int, _c_i64, _c_p, _c_p, _c_p]
     lib.ce_backward.restype = _c_int
@@ -150,6 +153,32 @@ def ce_forward(logits, target, label_smoothing=0.0, reduce_loss=False, ignore_id
                             0 if workspace is None else workspace.numel() * workspace.element_size(),
                             _ptr(dev_status), _stream(dev, stream))
     _check("ce_forward", st)
+    return CEForward(loss if reduce_loss else loss.view(logits.shape[:-1]), stats, n_valid, dev_status)
+
+
+def ce_forward_noalloc(logits, target, label_smoothing=0.0, reduce_loss=False, ignore_idx=-100, *,
+                       loss=None, stats=None, n_valid=None, dev_status=None, stream=None):
+    """ce_forward without a workspace argument: the library's fixed scratch array holds
+    the per-row losses (for callers that cannot allocate; see include/vce.h).  Outputs
+    not passed in are allocated here by torch, before the call."""
+    lib = library()
+    dev = logits.device
+    n, vocab, stride = _rows_view(logits)
+    target = _target(target, n)
+    if loss is None:
+        loss = torch.empty(1 if reduce_loss else n, dtype=torch.float32, device=dev)
+    if stats is None:
+        stats = torch.empty(n, 2, dtype=torch.float32, device=dev)
+    if n_valid is None:
+        n_valid = torch.empty(1, dtype=torch.int64, device=dev)
+    if dev_status is None:
+        dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        st = lib.ce_forward_noalloc(_ptr(logits), _dtype_code(logits), n, vocab, stride, _ptr(target),
+                                    float(label_smoothing), int(bool(reduce_loss)), int(ignore_idx),
+                                    _ptr(loss), _ptr(stats), _ptr(n_valid), _ptr(dev_status),
+                                    _stream(dev, stream))
+    _check("ce_forward_noalloc", st)
     return CEForward(loss if reduce_loss else loss.view(logits.shape[:-1]), stats, n_valid, dev_status)
 
 

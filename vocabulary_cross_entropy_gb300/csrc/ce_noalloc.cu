@@ -1,0 +1,67 @@
+// ce_forward_noalloc: the logits-form forward for callers that cannot allocate
+// device memory.
+//
+// ce_forward with reduce_loss needs a workspace of n_rows floats for the
+// per-row losses it sums afterwards.  Some callers are handed only their
+// inputs and outputs and have no way to obtain that buffer: a plugin running
+// inside another runtime's execution plan, or a deployment that forbids
+// device allocation once it has started.  This entry point keeps that scratch
+// in a fixed array compiled into the library instead.
+//
+// The array below lives in global memory on every GPU that loads the library
+// and is held until the process exits (4 MiB per GPU).  Host code only knows
+// the array's name as a host-side stand-in, so the device address is fetched
+// with cudaGetSymbolAddress, once per device with that device current, on the
+// first call made on that device; make that first call before any stream
+// capture.  Every call uses the same array: each call writes every row slot it
+// reads, so no clearing is needed, but calls that overlap on the GPU (two
+// streams, or two host threads) race on it.
+
+#include "vce_internal.cuh"
+
+#include <mutex>
+
+namespace {
+
+constexpr int64_t kNoAllocMaxRows = VCE_NOALLOC_MAX_ROWS;  // 1,048,576 rows = 4 MiB of FP32
+
+static __device__ __align__(256) float g_row_loss_scratch[kNoAllocMaxRows];
+
+std::mutex g_scratch_mu;
+void* g_scratch_addr[64] = {};
+
+// Device address of g_row_loss_scratch on the current device (cached per ordinal).
+vce_status scratch_address(int ordinal, void** out) {
+    if (ordinal < 0 || ordinal >= 64) return VCE_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[ordinal]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_row_loss_scratch) != cudaSuccess || p == nullptr)
+            return VCE_ERR_CUDA;
+        g_scratch_addr[ordinal] = p;
+    }
+    *out = g_scratch_addr[ordinal];
+    return VCE_OK;
+}
+
+}  // namespace
+
+extern "C" vce_status ce_forward_noalloc(const void* logits, int dtype, int64_t n_rows,
+                                         int64_t vocab, int64_t row_stride,
+                                         const int64_t* target, float label_smoothing,
+                                         int reduce_loss, int64_t ignore_idx, float* loss,
+                                         float* stats, int64_t* n_valid, int* dev_status,
+                                         void* stream) {
+    if (reduce_loss && n_rows > kNoAllocMaxRows) return VCE_ERR_WORKSPACE;
+    vce::DeviceInfo dev;
+    if (vce_status st = vce::current_device(dev)) return st;
+    void* scratch = nullptr;
+    size_t scratch_bytes = 0;
+    if (reduce_loss) {
+        if (vce_status st = scratch_address(dev.ordinal, &scratch)) return st;
+        scratch_bytes = size_t(kNoAllocMaxRows) * sizeof(float);
+    }
+    return ce_forward(logits, dtype, n_rows, vocab, row_stride, target, label_smoothing,
+                      reduce_loss, ignore_idx, loss, stats, n_valid, scratch, scratch_bytes,
+                      dev_status, stream);
+}
