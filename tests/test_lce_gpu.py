@@ -1,0 +1,171 @@
+"""Linear form on the GPU against the FP64 oracle (Cut Cross-Entropy /
+Liger fused linear cross entropy semantics).  Tolerances (BF16 inputs, FP32
+accumulation, BF16 gradients):
+
+* loss and lse: |d| <= 2e-3 per row and for the mean;
+* dX, dW: norm-wise ||d|| / ||ref|| <= 1e-2;
+* N_v and the zero rows of ignored tokens in dX: bit-exact.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wk
+import vocabulary_cross_entropy_gb300 as vce
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from vocabulary_cross_entropy_gb300 import build
+    build.build()
+
+
+def dev_bf16(a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(DEV).view(torch.bfloat16)
+
+
+def host_f64(t):
+    return oracle.widen(t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16), "bf16")
+
+
+def rel(a, b):
+    nb = np.linalg.norm(b)
+    return np.linalg.norm(a - b) / nb if nb > 0 else np.linalg.norm(a)
+
+
+def run(x, w, target, eps, red, grad, max_slab_bytes=0):
+    xt, wt = dev_bf16(x), dev_bf16(w)
+    yt = torch.from_numpy(target).to(DEV)
+    f = vce.lce_forward(xt, wt, yt, eps, red)
+    g = torch.from_numpy(np.asarray(grad, np.float32)).to(DEV)
+    b = vce.lce_backward(xt, wt, yt, f.lse, f.n_valid, g, eps, red, max_slab_bytes=max_slab_bytes)
+    torch.cuda.synchronize()
+    return f, b
+
+
+def check_full(x, w, target, eps, red, grad, max_slab_bytes=0):
+    f, b = run(x, w, target, eps, red, grad, max_slab_bytes)
+    ref = oracle.lce_forward(x, w, target, eps, red)
+    dx, dw, _ = oracle.lce_backward(x, w, target, ref["lse"], ref["n_valid"], grad, eps, red, z=ref["z"])
+    assert int(f.dev_status.item()) == 0 and int(b.dev_status.item()) == 0
+    assert int(f.n_valid.item()) == ref["n_valid"]
+    lse = f.lse.double().cpu().numpy()
+    assert np.max(np.abs(lse - ref["lse"])) <= 2e-3
+    if red:
+        assert abs(f.loss.item() - ref["loss"]) <= 2e-3, (f.loss.item(), ref["loss"])
+    else:
+        assert np.max(np.abs(f.loss.double().cpu().numpy() - ref["loss"])) <= 2e-3
+    gx, gw = host_f64(b.dX), host_f64(b.dW)
+    ign = target == -100
+    assert np.all(gx[ign] == 0.0)
+    assert rel(gx, dx) <= 1e-2, rel(gx, dx)
+    assert rel(gw, dw) <= 1e-2, rel(gw, dw)
+
+
+SMALL = [
+    # n, h, v, eps, reduce, ignore fraction
+    (200, 128, 1000, 0.0, True, 0.05),
+    (1, 64, 7, 0.1, False, 0.0),
+    (129, 72, 300, 0.1, True, 0.1),
+    (300, 256, 513, 0.0, False, 0.02),
+    (257, 520, 2309, 0.1, True, 0.1),
+    (1000, 512, 4099, 0.0, True, 0.0),
+]
+
+
+@pytest.mark.parametrize("n,h,v,eps,red,ign", SMALL)
+def test_small_shapes_full(n, h, v, eps, red, ign):
+    seed = n + h + v
+    x = wk.normal_matrix(seed, wk.TID_X, n, h, 1.0, True)
+    w = wk.normal_matrix(seed, wk.TID_W, v, h, h ** -0.5, True)
+    y = wk.uniform_targets(seed, n, v, ign)
+    g = np.ones(1, np.float32) if red else wk.grad_rows(seed, n)
+    check_full(x, w, y, eps, red, g)
+
+
+@pytest.mark.parametrize("slab_rows", [256, 512])
+def test_vocab_slabs_accumulate_dx(slab_rows):
+    # a workspace cap that forces several vocabulary slabs (FP32 dX accumulation)
+    n, h, v = 384, 256, 1800
+    x = wk.normal_matrix(11, wk.TID_X, n, h, 1.0, True)
+    w = wk.normal_matrix(11, wk.TID_W, v, h, h ** -0.5, True)
+    y = wk.uniform_targets(11, n, v, 0.05)
+    check_full(x, w, y, 0.1, True, np.ones(1, np.float32), max_slab_bytes=n * 2 * slab_rows)
+
+
+def test_token_wave_boundaries():
+    # 4097- and 5000-token shapes (one token past a 4K wave; a two-wave tail)
+    for n in (4097, 5000):
+        h, v = 128, 700
+        x = wk.normal_matrix(n, wk.TID_X, n, h, 1.0, True)
+        w = wk.normal_matrix(n, wk.TID_W, v, h, h ** -0.5, True)
+        y = wk.uniform_targets(n, n, v, 0.02)
+        check_full(x, w, y, 0.0, True, np.ones(1, np.float32))
+
+
+def test_bad_target_status():
+    n, h, v = 64, 64, 300
+    x = wk.normal_matrix(1, wk.TID_X, n, h, 1.0, True)
+    w = wk.normal_matrix(1, wk.TID_W, v, h, 0.125, True)
+    y = wk.uniform_targets(1, n, v, 0.0)
+    y[5] = v
+    f, b = run(x, w, y, 0.0, False, np.ones(n, np.float32))
+    assert int(f.dev_status.item()) & vce.DEVSTATUS_BAD_TARGET
+    loss = f.loss.cpu().numpy()
+    assert math.isnan(loss[5]) and np.isfinite(np.delete(loss, 5)).all()
+    assert torch.count_nonzero(b.dX[5]).item() == 0
+
+
+def test_all_ignored():
+    n, h, v = 50, 64, 333
+    x = wk.normal_matrix(2, wk.TID_X, n, h, 1.0, True)
+    w = wk.normal_matrix(2, wk.TID_W, v, h, 0.125, True)
+    y = np.full(n, -100, np.int64)
+    f, b = run(x, w, y, 0.1, True, np.ones(1, np.float32))
+    assert int(f.n_valid.item()) == 0 and math.isnan(f.loss.item())
+    assert torch.count_nonzero(b.dX).item() == 0 and torch.count_nonzero(b.dW).item() == 0
+
+
+def test_small_linear_workload_full():
+    wl = wk.LINEAR_SMALL
+    inp = wk.make_linear_inputs(wl)
+    check_full(inp.x, inp.w, inp.target, wl.label_smoothing, wl.reduce_loss, inp.grad)
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads, run as the benchmark runs them; sampled rows against
+# the oracle (dW rows need the oracle's lse of every token: one FP64 forward)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("wl", [wk.LINEAR_HEADLINE, wk.LINEAR_LARGE], ids=lambda w: w.name)
+def test_full_size_sampled(wl):
+    inp = wk.make_linear_inputs(wl)
+    f, b = run(inp.x, inp.w, inp.target, wl.label_smoothing, wl.reduce_loss, inp.grad)
+    assert int(f.dev_status.item()) == 0 and int(b.dev_status.item()) == 0
+    n_valid = int((inp.target != -100).sum())
+    assert int(f.n_valid.item()) == n_valid
+    lse_all, loss_all = oracle.lce_lse_all(inp.x, inp.w, inp.target, wl.label_smoothing)
+    lse_gpu = f.lse.double().cpu().numpy()
+    assert np.max(np.abs(lse_gpu - lse_all)) <= 2e-3
+    assert abs(f.loss.item() - oracle.mean_loss(loss_all, n_valid)) <= 2e-3
+    g_all = oracle.upstream(inp.grad, wl.n, n_valid, wl.reduce_loss)
+    rng = np.random.default_rng(0)
+    rows = np.unique(np.concatenate([rng.choice(wl.n, 24, replace=False), [0, wl.n - 1]]))
+    dx_ref = oracle.lce_dx_rows(inp.x[rows], inp.w, inp.target[rows], lse_all[rows], g_all[rows],
+                                wl.label_smoothing)
+    gx = host_f64(b.dX[torch.from_numpy(rows).to(DEV)])
+    assert rel(gx, dx_ref) <= 1e-2, rel(gx, dx_ref)
+    ign = np.nonzero(inp.target == -100)[0]
+    if len(ign):
+        assert torch.count_nonzero(b.dX[torch.from_numpy(ign).to(DEV)]).item() == 0
+    vids = np.unique(np.concatenate([rng.choice(wl.vocab, 24, replace=False), [0, wl.vocab - 1],
+                                     inp.target[:4][inp.target[:4] >= 0]]))
+    dw_ref = oracle.lce_dw_rows(inp.x, inp.w, vids, inp.target, lse_all, g_all, wl.label_smoothing)
+    gw = host_f64(b.dW[torch.from_numpy(vids).to(DEV)])
+    assert rel(gw, dw_ref) <= 1e-2, rel(gw, dw_ref)

@@ -1,18 +1,578 @@
-// Linear-form cross entropy on tcgen05 tensor cores (sm_103a).
+// Linear-form cross entropy on the tcgen05 tensor cores of sm_103a.
+//
+// The logits Z = X W^T are never stored (Cut Cross-Entropy card,
+// "what_it_does": only the target logit and the log-sum-exp over the
+// vocabulary are kept).  Every product runs through one warp-specialised GEMM
+// kernel (Liger pull request "Implementation": a TMA warp feeds a multistage
+// shared-memory ring, one thread issues UMMA into tensor memory, epilogue warps
+// drain tensor memory), instantiated with three epilogues:
+//
+//   forward : Z tile -> per-(row, 256-wide vocab tile) softmax partials
+//             (running max, sum of exp, sum of logits) and the target logit;
+//             a small combine kernel turns the partials into lse and the loss.
+//   dZ      : recomputed Z tile -> dZ = g (exp(Z - lse) - (1-eps) onehot - eps/V),
+//             stored as BF16 for one vocabulary slab (backward "dZ" phase).
+//   store   : plain FP32 accumulator -> BF16 (dW = dZ^T X, dX = dZ W), or an
+//             FP32 running sum of dX across vocabulary slabs.
+//
+// Kernel shape: one CTA per SM (persistent, static round-robin over tiles),
+// 128 x 256 output tile (UMMA M=128, N=256, K=16, cta_group::1), K step 64 per
+// stage, 4 stages of 48 KiB, two 256-column FP32 accumulators in tensor memory
+// so the epilogue of one tile overlaps the main loop of the next.
+// Warp 0: TMA producer.  Warp 1: tensor-memory allocation and the MMA issuer.
+// Warps 2-5: epilogue, one output row per thread (tensor-memory lane).
+// Every mbarrier wait is bounded: past kTimeoutNs the CTA sets an abort flag,
+// the other roles stop, in-flight copies and MMAs are drained, tensor memory
+// is released and VCE_DEVSTATUS_TIMEOUT is reported.
+
 #include "vce_internal.cuh"
+#include "sm100_ptx.cuh"
+
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <mutex>
 
 namespace vce {
+namespace {
+
+using namespace sm100;
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int kStages = 4;
+constexpr uint32_t kABytes = BM * BK * 2;
+constexpr uint32_t kBBytes = BN * BK * 2;
+constexpr uint32_t kStageBytes = kABytes + kBBytes;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kThreads = 192;
+constexpr size_t kSmemBytes = size_t(kStages) * kStageBytes + 1024 + 256;
+constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
+
+struct GemmArgs {
+    int tiles_m, tiles_n, k_blocks;
+    int m_fastest;  // tile order: 1 = M index varies fastest
+    int* dev_status;
+};
+
+__device__ __forceinline__ void tile_coords(const GemmArgs& a, int t, int& tm, int& tn) {
+    if (a.m_fastest) {
+        tm = t % a.tiles_m;
+        tn = t / a.tiles_m;
+    } else {
+        tn = t % a.tiles_n;
+        tm = t / a.tiles_n;
+    }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&b);
+}
+
+// Store 32 consecutive floats of one row as BF16 (``left`` of them valid).
+__device__ __forceinline__ void store_row32_bf16(__nv_bfloat16* dst, const float (&d)[32], int64_t left) {
+    if (left >= 32) {
+        uint4* q = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            q[i] = make_uint4(pack_bf16x2(d[8 * i + 0], d[8 * i + 1]), pack_bf16x2(d[8 * i + 2], d[8 * i + 3]),
+                              pack_bf16x2(d[8 * i + 4], d[8 * i + 5]), pack_bf16x2(d[8 * i + 6], d[8 * i + 7]));
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (j < left) dst[j] = __float2bfloat16_rn(d[j]);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// epilogues: called by every epilogue thread for its row ``gm`` of output tile
+// column ``tn``; ``taddr`` is the tensor-memory address of the row's accumulator
+// ---------------------------------------------------------------------------
+
+// forward: softmax partials of one 256-wide vocabulary tile
+struct FwdEpi {
+    const int64_t* target;
+    int64_t M;       // tokens
+    int64_t V;       // vocabulary
+    float2* part_ms; // [tiles_n][M] (max, sum exp(z - max))
+    float* part_sum; // [tiles_n][M] sum of z (label smoothing), may be unused
+    float* zy;       // [M] target logit
+    int smooth;
+
+    __device__ __forceinline__ void operator()(int64_t gm, int tn, uint32_t taddr) const {
+        const bool row_ok = gm < M;
+        const int64_t y = row_ok ? target[gm] : -1;
+        const int64_t gn0 = int64_t(tn) * BN;
+        float m = -INFINITY, negm = 0.f, s = 0.f, sum = 0.f, zyv = 0.f;
+        bool hit = false;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(taddr + c * 32, r);
+            tmem_ld_wait();
+            const int64_t col0 = gn0 + c * 32;
+            const int64_t left = V - col0;
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+            if ((uint64_t)(y - col0) < 32ull) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (col0 + j == y) zyv = v[j];
+                hit = true;
+            }
+            if (left < 32) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (j >= left) v[j] = -INFINITY;
+            }
+            if (smooth) {
+                float u = 0.f;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) u += (j < left) ? v[j] : 0.f;
+                sum += u;
+            }
+            float vm = v[0];
+#pragma unroll
+            for (int j = 1; j < 32; ++j) vm = fmaxf(vm, v[j]);
+            if (vm > m) {
+                s = s * ex2f((m - vm) * kLog2e);
+                m = vm;
+                negm = -vm * kLog2e;
+            }
+            float t = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) t += ex2f(fmaf(v[j], kLog2e, negm));
+            s += t;
+        }
+        if (row_ok) {
+            part_ms[int64_t(tn) * M + gm] = make_float2(m, s);
+            if (smooth) part_sum[int64_t(tn) * M + gm] = sum;
+            if (hit) zy[gm] = zyv;
+        }
+    }
+};
+
+// backward: dZ of one slab, stored BF16 [M, slab] with leading dimension ld
+struct DzEpi {
+    const int64_t* target;
+    const float* lse;
+    const float* grad;
+    const int64_t* n_valid;
+    int reduce;
+    float eps;
+    int64_t M, V, slab0, slab_cols, ld, ignore_idx;
+    __nv_bfloat16* dz;
+    int* dev_status;
+
+    __device__ __forceinline__ void operator()(int64_t gm, int tn, uint32_t taddr) const {
+        const bool row_ok = gm < M;
+        bool live = false;
+        int64_t y = -1;
+        float g = 0.f, negl = 0.f;
+        if (row_ok) {
+            y = target[gm];
+            const bool ign = (y == ignore_idx);
+            const bool bad = !ign && (y < 0 || y >= V);
+            if (bad && tn == 0 && slab0 == 0) report(dev_status, VCE_DEVSTATUS_BAD_TARGET);
+            live = !ign && !bad;
+            if (live) {
+                g = reduce ? grad[0] / float(n_valid[0]) : grad[gm];
+                negl = -lse[gm] * kLog2e;
+            }
+        }
+        const float b = g * eps / float(V);
+        const float c1 = g * (1.f - eps);
+        const int64_t gn0 = int64_t(tn) * BN;
+        __nv_bfloat16* out = dz + (row_ok ? gm : 0) * ld;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(taddr + c * 32, r);
+            tmem_ld_wait();
+            const int64_t col0 = gn0 + c * 32;
+            const int64_t left = slab_cols - col0;
+            if (!row_ok || left <= 0) continue;
+            float d[32];
+            if (live) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) d[j] = fmaf(g, ex2f(fmaf(__uint_as_float(r[j]), kLog2e, negl)), -b);
+                const int64_t yy = y - slab0 - col0;
+                if ((uint64_t)yy < 32ull) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) d[j] -= (j == yy) ? c1 : 0.f;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) d[j] = 0.f;
+            }
+            store_row32_bf16(out + col0, d, left);
+        }
+    }
+};
+
+// plain accumulator epilogue
+struct StoreEpi {
+    __nv_bfloat16* out;  // BF16 [M, ld_out]
+    int64_t ld_out;
+    float* acc;          // FP32 [M, ld_acc] running sum across launches
+    int64_t ld_acc;
+    int mode;            // 0: out = D; 1: acc = D; 2: acc += D; 3: out = acc + D
+    int64_t M, N;
+
+    __device__ __forceinline__ void operator()(int64_t gm, int tn, uint32_t taddr) const {
+        const bool row_ok = gm < M;
+        const int64_t gn0 = int64_t(tn) * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(taddr + c * 32, r);
+            tmem_ld_wait();
+            const int64_t col0 = gn0 + c * 32;
+            const int64_t left = N - col0;
+            if (!row_ok || left <= 0) continue;
+            float d[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) d[j] = __uint_as_float(r[j]);
+            if (mode == 0) {
+                store_row32_bf16(out + gm * ld_out + col0, d, left);
+                continue;
+            }
+            float* a = acc + gm * ld_acc + col0;
+            if (left >= 32) {
+                float4* a4 = reinterpret_cast<float4*>(a);
+                if (mode == 1) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) a4[i] = make_float4(d[4 * i], d[4 * i + 1], d[4 * i + 2], d[4 * i + 3]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float4 p = a4[i];
+                        d[4 * i] += p.x; d[4 * i + 1] += p.y; d[4 * i + 2] += p.z; d[4 * i + 3] += p.w;
+                    }
+                    if (mode == 2) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            a4[i] = make_float4(d[4 * i], d[4 * i + 1], d[4 * i + 2], d[4 * i + 3]);
+                    } else {
+                        store_row32_bf16(out + gm * ld_out + col0, d, left);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    if (j >= left) continue;
+                    if (mode == 1) a[j] = d[j];
+                    else if (mode == 2) a[j] += d[j];
+                    else out[gm * ld_out + col0 + j] = __float2bfloat16_rn(a[j] + d[j]);
+                }
+            }
+        }
+    }
+};
+
+// ---------------------------------------------------------------------------
+// the GEMM: D[M, N] = A[M, K] * B[N, K]^T, BF16 in, FP32 accumulate
+// A and B are K-major ([rows][K] in memory) or MN-major ([K][rows] in memory)
+// ---------------------------------------------------------------------------
+
+template <class Epi, bool kAMn, bool kBMn>
+__global__ void __launch_bounds__(kThreads, 1)
+tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const GemmArgs args, const Epi epi) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(kStages) * kStageBytes);
+    uint64_t* empty = full + kStages;
+    uint64_t* tfull = empty + kStages;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int T = args.tiles_m * args.tiles_n;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 128);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer ----------------
+            tma_prefetch_desc(&tmA);
+            tma_prefetch_desc(&tmB);
+            uint32_t stage = 0, phase = 0, issued = 0, issued_phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < T; t += gridDim.x) {
+                int tm, tn;
+                tile_coords(args, t, tm, tn);
+                for (int kb = 0; kb < args.k_blocks; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, kTimeoutNs)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* sa = smem + size_t(stage) * kStageBytes;
+                    uint8_t* sb = sa + kABytes;
+                    mbar_arrive_expect_tx(&full[stage], kStageBytes);
+                    if (kAMn) {
+#pragma unroll
+                        for (int j = 0; j < BM / 64; ++j)
+                            tma_load_2d(sa + j * 8192, &tmA, &full[stage], tm * BM + j * 64, kb * BK);
+                    } else {
+                        tma_load_2d(sa, &tmA, &full[stage], kb * BK, tm * BM);
+                    }
+                    if (kBMn) {
+#pragma unroll
+                        for (int j = 0; j < BN / 64; ++j)
+                            tma_load_2d(sb + j * 8192, &tmB, &full[stage], tn * BN + j * 64, kb * BK);
+                    } else {
+                        tma_load_2d(sb, &tmB, &full[stage], kb * BK, tn * BN);
+                    }
+                    issued |= 1u << stage;
+                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // let copies already in flight land before shared memory is released
+                volatile int no_abort = 0;
+                for (int s = 0; s < kStages; ++s)
+                    if ((issued >> s) & 1u) mbar_wait(&full[s], (issued_phase >> s) & 1u, &no_abort, kTimeoutNs);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer ----------------
+            constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN, kAMn, kBMn);
+            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < T; t += gridDim.x) {
+                if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, kTimeoutNs)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int kb = 0; kb < args.k_blocks; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag, kTimeoutNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + size_t(stage) * kStageBytes);
+                    const uint32_t sb = sa + kABytes;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        const uint64_t ad = kAMn ? smem_desc_sw128(sa + kk * 2048, 8192, 1024)
+                                                 : smem_desc_sw128(sa + kk * 32, 16, 1024);
+                        const uint64_t bd = kBMn ? smem_desc_sw128(sb + kk * 2048, 8192, 1024)
+                                                 : smem_desc_sw128(sb + kk * 32, 16, 1024);
+                        umma_bf16(d_tmem, ad, bd, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    umma_commit(&empty[stage]);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(&tfull[acc]);
+                acc ^= 1u;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            // every MMA issued so far completes before tensor memory is released
+            umma_commit(drain);
+            volatile int no_abort = 0;
+            mbar_wait(drain, 0, &no_abort, kTimeoutNs);
+        }
+    } else {
+        // ---------------- epilogue (warps 2..5) ----------------
+        const int q = warp & 3;  // tensor-memory lane quadrant this warp may access
+        uint32_t acc = 0, acc_phase = 0;
+        for (int t = blockIdx.x; t < T; t += gridDim.x) {
+            bool ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, kTimeoutNs);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
+            int tm, tn;
+            tile_coords(args, t, tm, tn);
+            const uint32_t taddr = tmem_base + (uint32_t(q * 32) << 16) + acc * BN;
+            epi(int64_t(tm) * BM + q * 32 + lane, tn, taddr);
+            tc_fence_before();
+            mbar_arrive(&tempty[acc]);
+            acc ^= 1u;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag) report(args.dev_status, VCE_DEVSTATUS_TIMEOUT);
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// forward combine: partials of every vocabulary tile -> lse, loss
+// ---------------------------------------------------------------------------
+
+__global__ void lce_combine_kernel(const float2* __restrict__ part_ms, const float* __restrict__ part_sum,
+                                   const float* __restrict__ zy, const int64_t* __restrict__ target, int64_t n,
+                                   int64_t v, int nb, float eps, int64_t ignore_idx, float* __restrict__ lse_out,
+                                   float* __restrict__ loss_out, int* dev_status) {
+    const int64_t row = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (row >= n) return;
+    float m = -INFINITY;
+    for (int b = 0; b < nb; ++b) m = fmaxf(m, part_ms[int64_t(b) * n + row].x);
+    float s = 0.f;
+    for (int b = 0; b < nb; ++b) {
+        const float2 p = part_ms[int64_t(b) * n + row];
+        s += p.y * ex2f((p.x - m) * kLog2e);
+    }
+    const float lse = m + logf(s);
+    lse_out[row] = lse;
+    const int64_t y = target[row];
+    float loss;
+    if (y == ignore_idx) {
+        loss = 0.f;
+    } else if (y < 0 || y >= v) {
+        loss = __int_as_float(0x7fc00000);
+        report(dev_status, VCE_DEVSTATUS_BAD_TARGET);
+    } else {
+        loss = lse - zy[row];
+        if (eps != 0.f) {
+            float sum = 0.f;
+            for (int b = 0; b < nb; ++b) sum += part_sum[int64_t(b) * n + row];
+            loss = (1.f - eps) * loss + eps * (lse - sum / float(v));
+        }
+    }
+    loss_out[row] = loss;
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D BF16 tensor map: ``inner`` contiguous elements per row, ``outer`` rows of
+// ``row_bytes`` bytes; box of box_inner x box_outer elements, 128-byte swizzle,
+// zero fill out of bounds.
+bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+              uint32_t box_inner, uint32_t box_outer) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t es[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// K-major operand: rows of K elements; box = 64 K x ``rows_box`` rows
+bool map_kmajor(CUtensorMap* m, const void* base, int64_t k, int64_t rows, int64_t ld, uint32_t rows_box) {
+    return make_map(m, base, uint64_t(k), uint64_t(rows), uint64_t(ld) * 2, BK, rows_box);
+}
+
+// MN-major operand: rows of MN elements, one row per K index; box = 64 x 64
+bool map_mnmajor(CUtensorMap* m, const void* base, int64_t mn, int64_t k, int64_t ld) {
+    return make_map(m, base, uint64_t(mn), uint64_t(k), uint64_t(ld) * 2, 64, BK);
+}
+
+template <class Epi, bool kAMn, bool kBMn>
+vce_status launch_gemm(const CUtensorMap& a, const CUtensorMap& b, int64_t M, int64_t N, int64_t K, int m_fastest,
+                       const Epi& epi, int* dev_status, cudaStream_t s, const DeviceInfo& dev) {
+    auto kern = tc_gemm_kernel<Epi, kAMn, kBMn>;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
+    });
+    if (attr_err != cudaSuccess) return VCE_ERR_CUDA;
+    GemmArgs args;
+    args.tiles_m = int((M + BM - 1) / BM);
+    args.tiles_n = int((N + BN - 1) / BN);
+    args.k_blocks = int((K + BK - 1) / BK);
+    args.m_fastest = m_fastest;
+    args.dev_status = dev_status;
+    const int64_t tiles = int64_t(args.tiles_m) * args.tiles_n;
+    if (tiles <= 0 || args.k_blocks <= 0) return VCE_OK;
+    const int grid = int(tiles < dev.num_sms ? tiles : dev.num_sms);
+    kern<<<grid, kThreads, kSmemBytes, s>>>(a, b, args, epi);
+    return cudaGetLastError() == cudaSuccess ? VCE_OK : VCE_ERR_CUDA;
+}
+
+struct FwdWs {
+    float2* part_ms;
+    float* part_sum;
+    float* zy;
+    float* loss_rows;
+    size_t bytes;
+};
+
+FwdWs carve_forward(void* ws, int64_t n, int64_t v, int reduce_loss) {
+    const int64_t nb = (v + BN - 1) / BN;
+    FwdWs w{};
+    size_t off = 0;
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    w.part_ms = reinterpret_cast<float2*>(base + off);
+    off += align256(size_t(nb) * size_t(n) * 8);
+    w.part_sum = reinterpret_cast<float*>(base + off);
+    off += align256(size_t(nb) * size_t(n) * 4);
+    w.zy = reinterpret_cast<float*>(base + off);
+    off += align256(size_t(n) * 4);
+    w.loss_rows = reduce_loss ? reinterpret_cast<float*>(base + off) : nullptr;
+    if (reduce_loss) off += align256(size_t(n) * 4);
+    w.bytes = off;
+    return w;
+}
+
+int64_t slab_ld(int64_t slab) { return (slab + 7) / 8 * 8; }
+
+}  // namespace
 
 size_t lce_forward_ws_bytes(int64_t n, int64_t v, int reduce_loss) {
-    const int64_t nb = (v + 255) / 256;
-    size_t b = align256(size_t(nb) * size_t(n) * 12) + align256(size_t(n) * 4);
-    if (reduce_loss) b += align256(size_t(n) * 4);
-    return b;
+    return carve_forward(nullptr, n, v, reduce_loss).bytes;
 }
 
 size_t lce_backward_ws_bytes(int64_t n, int64_t h, int64_t v, int64_t slab) {
-    const int64_t ld = (slab + 7) / 8 * 8;
-    size_t b = align256(size_t(n) * size_t(ld) * 2);
+    size_t b = align256(size_t(n) * size_t(slab_ld(slab)) * 2);
     if (slab < v) b += align256(size_t(n) * size_t(h) * 4);
     return b;
 }
@@ -21,22 +581,76 @@ int64_t lce_slab_for_ws(int64_t n, int64_t h, int64_t v, size_t ws_bytes) {
     if (ws_bytes >= lce_backward_ws_bytes(n, h, v, v)) return v;
     const size_t acc = align256(size_t(n) * size_t(h) * 4);
     if (ws_bytes <= acc) return 0;
-    const int64_t cap = int64_t((ws_bytes - acc) / (size_t(n) * 2)) / 256 * 256;
+    int64_t cap = int64_t((ws_bytes - acc) / (size_t(n) * 2)) / 256 * 256;
+    while (cap >= 256 && lce_backward_ws_bytes(n, h, v, cap) > ws_bytes) cap -= 256;
     if (cap < 256) return 0;
     return cap < v ? cap : v;
 }
 
-vce_status launch_lce_forward(const void*, const void*, int64_t, int64_t, int64_t,
-                              const int64_t*, float, int, int64_t, float*, float*, int64_t*,
-                              void*, int*, cudaStream_t, const DeviceInfo&) {
-    return VCE_ERR_INVALID_ARG;
+vce_status launch_lce_forward(const void* X, const void* W, int64_t n, int64_t h, int64_t v,
+                              const int64_t* target, float eps, int reduce_loss, int64_t ignore_idx,
+                              float* loss, float* lse, int64_t* n_valid, void* ws, int* dev_status,
+                              cudaStream_t s, const DeviceInfo& dev) {
+    if (n == 0) {
+        if (reduce_loss || n_valid)
+            return launch_mean_loss(nullptr, target, 0, ignore_idx, reduce_loss ? loss : nullptr, n_valid, s);
+        return VCE_OK;
+    }
+    const FwdWs w = carve_forward(ws, n, v, reduce_loss);
+    CUtensorMap tx, tw;
+    if (!map_kmajor(&tx, X, h, n, h, BM) || !map_kmajor(&tw, W, h, v, h, BN)) return VCE_ERR_CUDA;
+    FwdEpi epi{target, n, v, w.part_ms, w.part_sum, w.zy, eps != 0.f ? 1 : 0};
+    if (vce_status st = launch_gemm<FwdEpi, false, false>(tx, tw, n, v, h, 1, epi, dev_status, s, dev)) return st;
+    const int nb = int((v + BN - 1) / BN);
+    float* loss_rows = reduce_loss ? w.loss_rows : loss;
+    lce_combine_kernel<<<int((n + 255) / 256), 256, 0, s>>>(w.part_ms, w.part_sum, w.zy, target, n, v, nb, eps,
+                                                             ignore_idx, lse, loss_rows, dev_status);
+    if (cudaGetLastError() != cudaSuccess) return VCE_ERR_CUDA;
+    if (reduce_loss || n_valid)
+        return launch_mean_loss(reduce_loss ? loss_rows : nullptr, target, n, ignore_idx,
+                                reduce_loss ? loss : nullptr, n_valid, s);
+    return VCE_OK;
 }
 
-vce_status launch_lce_backward(const void*, const void*, int64_t, int64_t, int64_t,
-                               const int64_t*, const float*, const int64_t*, const float*, float,
-                               int, int64_t, void*, void*, void*, int64_t, int*, cudaStream_t,
-                               const DeviceInfo&) {
-    return VCE_ERR_INVALID_ARG;
+vce_status launch_lce_backward(const void* X, const void* W, int64_t n, int64_t h, int64_t v,
+                               const int64_t* target, const float* lse, const int64_t* n_valid,
+                               const float* grad_output, float eps, int reduce_loss, int64_t ignore_idx,
+                               void* dX, void* dW, void* ws, int64_t slab, int* dev_status, cudaStream_t s,
+                               const DeviceInfo& dev) {
+    if (n == 0) {
+        return cudaMemsetAsync(dW, 0, size_t(v) * size_t(h) * 2, s) == cudaSuccess ? VCE_OK : VCE_ERR_CUDA;
+    }
+    const int64_t ld = slab_ld(slab);
+    auto* dz = static_cast<__nv_bfloat16*>(ws);
+    float* acc = slab < v ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + align256(size_t(n) * ld * 2))
+                          : nullptr;
+    const auto* Wb = static_cast<const __nv_bfloat16*>(W);
+    auto* dWb = static_cast<__nv_bfloat16*>(dW);
+    auto* dXb = static_cast<__nv_bfloat16*>(dX);
+    CUtensorMap tx_k, tx_mn;
+    if (!map_kmajor(&tx_k, X, h, n, h, BM) || !map_mnmajor(&tx_mn, X, h, n, h)) return VCE_ERR_CUDA;
+    for (int64_t v0 = 0; v0 < v; v0 += slab) {
+        const int64_t vs = (v - v0) < slab ? (v - v0) : slab;
+        const bool first = v0 == 0, last = v0 + vs >= v;
+        // dZ = epilogue(X W_slab^T): M = n, N = vs, K = h
+        CUtensorMap tws_k, tdz_k, tdz_mn, tws_mn;
+        if (!map_kmajor(&tws_k, Wb + v0 * h, h, vs, h, BN) || !map_kmajor(&tdz_k, dz, vs, n, ld, BM) ||
+            !map_mnmajor(&tdz_mn, dz, vs, n, ld) || !map_mnmajor(&tws_mn, Wb + v0 * h, h, vs, h))
+            return VCE_ERR_CUDA;
+        DzEpi de{target, lse, grad_output, n_valid, reduce_loss, eps, n, v, v0, vs, ld, ignore_idx, dz, dev_status};
+        if (vce_status st = launch_gemm<DzEpi, false, false>(tx_k, tws_k, n, vs, h, 1, de, dev_status, s, dev))
+            return st;
+        // dW_slab = dZ^T X: M = vs, N = h, K = n (both operands MN-major)
+        StoreEpi we{dWb + v0 * h, h, nullptr, 0, 0, vs, h};
+        if (vce_status st = launch_gemm<StoreEpi, true, true>(tdz_mn, tx_mn, vs, h, n, 0, we, dev_status, s, dev))
+            return st;
+        // dX (+)= dZ W_slab: M = n, N = h, K = vs (W_slab read MN-major)
+        const int mode = (first && last) ? 0 : first ? 1 : last ? 3 : 2;
+        StoreEpi xe{dXb, h, acc, h, mode, n, h};
+        if (vce_status st = launch_gemm<StoreEpi, false, true>(tdz_k, tws_mn, n, h, vs, 1, xe, dev_status, s, dev))
+            return st;
+    }
+    return VCE_OK;
 }
 
 }  // namespace vce
