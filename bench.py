@@ -426,6 +426,11 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="both", choices=["linear", "logits", "both"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
+    ap.add_argument("--shape", default=None,
+                    help="linear workload N,H,V instead of the headline (e.g. a small profiling case)")
+    ap.add_argument("--logits-rows", type=int, default=None,
+                    help="rows of the logits workload instead of 4 x 4096 (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -445,7 +450,12 @@ def main():
 
     logits_obj = None
     if args.workload in ("logits", "both"):
-        st = LogitsStep(wk.LOGITS_MEMBOUND, dev)
+        lwl = wk.LOGITS_MEMBOUND
+        if args.logits_rows:
+            import dataclasses
+            lwl = dataclasses.replace(lwl, n_rows=args.logits_rows,
+                                      name=f"logits_{args.logits_rows}x{lwl.vocab}")
+        st = LogitsStep(lwl, dev)
         with Clocks(local) as ck:
             total, ph = time_steps(st, args.steps, args.warmup, pg)
         clocks_l = ck.summary()
@@ -485,7 +495,11 @@ def main():
             print(json.dumps(line), flush=True)
         return 0
 
-    st = LinearStep(wk.LINEAR_HEADLINE, dev)
+    lin = wk.LINEAR_HEADLINE
+    if args.shape:
+        n_, h_, v_ = (int(x) for x in args.shape.split(","))
+        lin = wk.LinearWorkload(f"linear_{n_}x{h_}x{v_}", n_, h_, v_, reduce_loss=True)
+    st = LinearStep(lin, dev)
     with Clocks(local) as ck:
         total, ph = time_steps(st, args.steps, args.warmup, pg)
     clocks = ck.summary()
@@ -494,9 +508,14 @@ def main():
     fwd_flops = 2.0 * st.wl.n * st.wl.hidden * st.wl.vocab
     fwd_tf = fwd_flops / (ph["forward"] / 1e3) / 1e12
     bwd_tf = 3 * fwd_flops / (ph["backward"] / 1e3) / 1e12
-    e2e_ms, h2d, d2h = time_e2e_linear(st, max(3, args.steps // 2), 3, pg)
     e2e_steps = max(3, args.steps // 2)
-    e2e_val = st.units() * world * e2e_steps / (e2e_ms / 1e3)
+    if args.no_e2e:
+        e2e_obj = None
+    else:
+        e2e_ms, h2d, d2h = time_e2e_linear(st, e2e_steps, 3, pg)
+        e2e_val = st.units() * world * e2e_steps / (e2e_ms / 1e3)
+        e2e_obj = {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                   "ms_per_step": e2e_ms / e2e_steps}
     line = {
         "metric": "linear-CE fwd+bwd TFLOP/s (4 classifier GEMMs)",
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -513,8 +532,7 @@ def main():
                      "frac": fwd_tf / pk["bf16"], "traffic": None,
                      "peak_source": pk["source"] + " bf16_tflops (burst cuBLAS)",
                      "algorithmic_flops": fwd_flops},
-        "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms / e2e_steps},
+        "e2e": e2e_obj,
         "gpu_launches": args.steps * (3 + 3),
         "clocks": clocks,
     }

@@ -438,18 +438,40 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 // forward combine: partials of every vocabulary tile -> lse, loss
 // ---------------------------------------------------------------------------
 
-__global__ void lce_combine_kernel(const float2* __restrict__ part_ms, const float* __restrict__ part_sum,
-                                   const float* __restrict__ zy, const int64_t* __restrict__ target, int64_t n,
-                                   int64_t v, int nb, float eps, int64_t ignore_idx, float* __restrict__ lse_out,
-                                   float* __restrict__ loss_out, int* dev_status) {
-    const int64_t row = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (row >= n) return;
-    float m = -INFINITY;
-    for (int b = 0; b < nb; ++b) m = fmaxf(m, part_ms[int64_t(b) * n + row].x);
-    float s = 0.f;
-    for (int b = 0; b < nb; ++b) {
-        const float2 p = part_ms[int64_t(b) * n + row];
-        s += p.y * ex2f((p.x - m) * kLog2e);
+constexpr int kCombRows = 32;   // consecutive rows per CTA (coalesced partial reads)
+constexpr int kCombSplit = 8;   // partial-index splits per row, merged in a fixed order
+
+__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
+    const float mn = fmaxf(m, m2);
+    if (mn == -INFINITY) return;
+    s = s * ex2f((m - mn) * kLog2e) + s2 * ex2f((m2 - mn) * kLog2e);
+    m = mn;
+}
+
+__global__ void __launch_bounds__(kCombRows * kCombSplit)
+lce_combine_kernel(const float2* __restrict__ part_ms, const float* __restrict__ part_sum,
+                   const float* __restrict__ zy, const int64_t* __restrict__ target, int64_t n, int64_t v,
+                   int nb, float eps, int64_t ignore_idx, float* __restrict__ lse_out,
+                   float* __restrict__ loss_out, int* dev_status) {
+    __shared__ float sm_m[kCombSplit][kCombRows], sm_s[kCombSplit][kCombRows], sm_u[kCombSplit][kCombRows];
+    const int lr = threadIdx.x % kCombRows, sp = threadIdx.x / kCombRows;
+    const int64_t row = int64_t(blockIdx.x) * kCombRows + lr;
+    float m = -INFINITY, s = 0.f, u = 0.f;
+    if (row < n) {
+        for (int b = sp; b < nb; b += kCombSplit) {
+            const float2 p = part_ms[int64_t(b) * n + row];
+            lse_merge(m, s, p.x, p.y);
+            if (eps != 0.f) u += part_sum[int64_t(b) * n + row];
+        }
+    }
+    sm_m[sp][lr] = m;
+    sm_s[sp][lr] = s;
+    sm_u[sp][lr] = u;
+    __syncthreads();
+    if (sp != 0 || row >= n) return;
+    for (int k = 1; k < kCombSplit; ++k) {
+        lse_merge(m, s, sm_m[k][lr], sm_s[k][lr]);
+        u += sm_u[k][lr];
     }
     const float lse = m + logf(s);
     lse_out[row] = lse;
@@ -462,11 +484,7 @@ __global__ void lce_combine_kernel(const float2* __restrict__ part_ms, const flo
         report(dev_status, VCE_DEVSTATUS_BAD_TARGET);
     } else {
         loss = lse - zy[row];
-        if (eps != 0.f) {
-            float sum = 0.f;
-            for (int b = 0; b < nb; ++b) sum += part_sum[int64_t(b) * n + row];
-            loss = (1.f - eps) * loss + eps * (lse - sum / float(v));
-        }
+        if (eps != 0.f) loss = (1.f - eps) * loss + eps * (lse - u / float(v));
     }
     loss_out[row] = loss;
 }
@@ -603,8 +621,8 @@ vce_status launch_lce_forward(const void* X, const void* W, int64_t n, int64_t h
     if (vce_status st = launch_gemm<FwdEpi, false, false>(tx, tw, n, v, h, 1, epi, dev_status, s, dev)) return st;
     const int nb = int((v + BN - 1) / BN);
     float* loss_rows = reduce_loss ? w.loss_rows : loss;
-    lce_combine_kernel<<<int((n + 255) / 256), 256, 0, s>>>(w.part_ms, w.part_sum, w.zy, target, n, v, nb, eps,
-                                                             ignore_idx, lse, loss_rows, dev_status);
+    lce_combine_kernel<<<int((n + kCombRows - 1) / kCombRows), kCombRows * kCombSplit, 0, s>>>(
+        w.part_ms, w.part_sum, w.zy, target, n, v, nb, eps, ignore_idx, lse, loss_rows, dev_status);
     if (cudaGetLastError() != cudaSuccess) return VCE_ERR_CUDA;
     if (reduce_loss || n_valid)
         return launch_mean_loss(reduce_loss ? loss_rows : nullptr, target, n, ignore_idx,
