@@ -15,12 +15,19 @@
 //   store   : plain FP32 accumulator -> BF16 (dW = dZ^T X, dX = dZ W), or an
 //             FP32 running sum of dX across vocabulary slabs.
 //
-// Kernel shape: one CTA per SM (persistent, static round-robin over tiles),
-// 128 x 256 output tile (UMMA M=128, N=256, K=16, cta_group::1), K step 64 per
-// stage, 4 stages of 48 KiB, two 256-column FP32 accumulators in tensor memory
-// so the epilogue of one tile overlaps the main loop of the next.
-// Warp 0: TMA producer.  Warp 1: tensor-memory allocation and the MMA issuer.
-// Warps 2-5: epilogue, one output row per thread (tensor-memory lane).
+// Kernel shape: CTA pairs (clusters of 2) on tcgen05's cta_group::2 path.  A
+// pair computes a 256 x BN output tile (BN = 256, or 128 for the dX GEMM whose
+// output is small): each CTA stages its 128 rows of A and its BN/2 rows of B
+// per 64-wide K step, the even CTA issues UMMA M=256, N=BN, K=16 over both
+// CTAs' shared memory, and each CTA's tensor memory receives its 128 output
+// rows.  The pair halves the B bytes every SM stages and reads, which buys a
+// deeper ring (6 stages of 32 KiB, 8 of 24 KiB) in the same shared memory.
+// Persistent: one pair per two SMs, static round-robin over tiles; two FP32
+// accumulators in tensor memory so the epilogue of one tile overlaps the main
+// loop of the next.
+// Warp 0: TMA producer (both CTAs).  Warp 1: tensor-memory allocation (both
+// CTAs) and the MMA issuer (even CTA).  Warps 2-5: epilogue, one output row
+// per thread (tensor-memory lane).
 // Every mbarrier wait is bounded: past kTimeoutNs the CTA sets an abort flag,
 // the other roles stop, in-flight copies and MMAs are drained, tensor memory
 // is released and VCE_DEVSTATUS_TIMEOUT is reported.
@@ -37,25 +44,39 @@ namespace {
 
 using namespace sm100;
 
-constexpr int BM = 128;
-constexpr int BN = 256;
-constexpr int BK = 64;
-constexpr int kStages = 4;
-constexpr uint32_t kABytes = BM * BK * 2;
-constexpr uint32_t kBBytes = BN * BK * 2;
-constexpr uint32_t kStageBytes = kABytes + kBBytes;
-constexpr uint32_t kTmemCols = 512;
+constexpr int BM = 256;          // output rows per CTA pair
+constexpr int BM_CTA = 128;      // output rows per CTA (tensor-memory lanes)
+constexpr int BK = 64;           // K elements per stage (one 128-byte swizzle row)
+constexpr int kVocabTile = 256;  // forward/dZ vocabulary tile width
+constexpr uint32_t kABytes = BM_CTA * BK * 2;
 constexpr int kThreads = 192;
-constexpr size_t kSmemBytes = size_t(kStages) * kStageBytes + 1024 + 256;
+constexpr uint32_t kRingBytes = 196608;
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
+
+template <int BN>
+struct PairCfg {
+    static constexpr uint32_t kBBytes = (BN / 2) * BK * 2;  // this CTA's half of B
+    static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+    static constexpr int kStages = (kRingBytes / kStageBytes) > 8 ? 8 : int(kRingBytes / kStageBytes);
+    static constexpr uint32_t kTmemCols = 2 * BN;           // two accumulators
+    static constexpr size_t kSmemBytes = size_t(kStages) * kStageBytes + 1024 + 256;
+    static_assert(BN == 128 || BN == 256, "tile width");
+};
 
 struct GemmArgs {
     int tiles_m, tiles_n, k_blocks;
-    int m_fastest;  // tile order: 1 = M index varies fastest
+    int k_splits;      // the K range is cut into this many consecutive chunks (separate work units)
+    int kb_per_split;  // K blocks per chunk (the last chunk may be shorter)
+    int m_fastest;     // unit order: 1 = M index varies fastest, else N; the K chunk varies slowest
     int* dev_status;
 };
 
-__device__ __forceinline__ void tile_coords(const GemmArgs& a, int t, int& tm, int& tn) {
+// Work unit u -> output tile (tm, tn), K chunk ks and its K-block range [kb0, kb1).
+__device__ __forceinline__ void unit_coords(const GemmArgs& a, int u, int& tm, int& tn, int& ks, int& kb0,
+                                            int& kb1) {
+    const int per = a.tiles_m * a.tiles_n;
+    ks = u / per;
+    const int t = u - ks * per;
     if (a.m_fastest) {
         tm = t % a.tiles_m;
         tn = t / a.tiles_m;
@@ -63,6 +84,9 @@ __device__ __forceinline__ void tile_coords(const GemmArgs& a, int t, int& tm, i
         tn = t % a.tiles_n;
         tm = t / a.tiles_n;
     }
+    kb0 = ks * a.kb_per_split;
+    kb1 = kb0 + a.kb_per_split;
+    if (kb1 > a.k_blocks) kb1 = a.k_blocks;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -100,7 +124,9 @@ struct FwdEpi {
     float* zy;       // [M] target logit
     int smooth;
 
-    __device__ __forceinline__ void operator()(int64_t gm, int tn, uint32_t taddr) const {
+    template <int BN>
+    __device__ __forceinline__ void run(int64_t gm, int tn, int ks, uint32_t taddr) const {
+        static_assert(BN == kVocabTile, "partials are per 256-wide vocabulary tile");
         const bool row_ok = gm < M;
         const int64_t y = row_ok ? target[gm] : -1;
         const int64_t gn0 = int64_t(tn) * BN;
@@ -166,7 +192,8 @@ struct DzEpi {
     __nv_bfloat16* dz;
     int* dev_status;
 
-    __device__ __forceinline__ void operator()(int64_t gm, int tn, uint32_t taddr) const {
+    template <int BN>
+    __device__ __forceinline__ void run(int64_t gm, int tn, int ks, uint32_t taddr) const {
         const bool row_ok = gm < M;
         bool live = false;
         int64_t y = -1;
@@ -216,12 +243,14 @@ struct DzEpi {
 struct StoreEpi {
     __nv_bfloat16* out;  // BF16 [M, ld_out]
     int64_t ld_out;
-    float* acc;          // FP32 [M, ld_acc] running sum across launches
+    float* acc;          // FP32 [k_splits][M, ld_acc] running sums across launches
     int64_t ld_acc;
-    int mode;            // 0: out = D; 1: acc = D; 2: acc += D; 3: out = acc + D
+    int64_t split_stride;  // elements between the FP32 buffers of consecutive K chunks
+    int mode;            // 0: out = D; 1: acc = D; 2: acc += D
     int64_t M, N;
 
-    __device__ __forceinline__ void operator()(int64_t gm, int tn, uint32_t taddr) const {
+    template <int BN>
+    __device__ __forceinline__ void run(int64_t gm, int tn, int ks, uint32_t taddr) const {
         const bool row_ok = gm < M;
         const int64_t gn0 = int64_t(tn) * BN;
 #pragma unroll 1
@@ -239,7 +268,7 @@ struct StoreEpi {
                 store_row32_bf16(out + gm * ld_out + col0, d, left);
                 continue;
             }
-            float* a = acc + gm * ld_acc + col0;
+            float* a = acc + int64_t(ks) * split_stride + gm * ld_acc + col0;
             if (left >= 32) {
                 float4* a4 = reinterpret_cast<float4*>(a);
                 if (mode == 1) {
@@ -251,21 +280,15 @@ struct StoreEpi {
                         const float4 p = a4[i];
                         d[4 * i] += p.x; d[4 * i + 1] += p.y; d[4 * i + 2] += p.z; d[4 * i + 3] += p.w;
                     }
-                    if (mode == 2) {
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            a4[i] = make_float4(d[4 * i], d[4 * i + 1], d[4 * i + 2], d[4 * i + 3]);
-                    } else {
-                        store_row32_bf16(out + gm * ld_out + col0, d, left);
-                    }
+                    for (int i = 0; i < 8; ++i) a4[i] = make_float4(d[4 * i], d[4 * i + 1], d[4 * i + 2], d[4 * i + 3]);
                 }
             } else {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     if (j >= left) continue;
                     if (mode == 1) a[j] = d[j];
-                    else if (mode == 2) a[j] += d[j];
-                    else out[gm * ld_out + col0 + j] = __float2bfloat16_rn(a[j] + d[j]);
+                    else a[j] += d[j];
                 }
             }
         }
@@ -277,15 +300,17 @@ struct StoreEpi {
 // A and B are K-major ([rows][K] in memory) or MN-major ([K][rows] in memory)
 // ---------------------------------------------------------------------------
 
-template <class Epi, bool kAMn, bool kBMn>
-__global__ void __launch_bounds__(kThreads, 1)
+template <class Epi, bool kAMn, bool kBMn, int BN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const GemmArgs args, const Epi epi) {
+    using C = PairCfg<BN>;
+    constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(kStages) * kStageBytes);
-    uint64_t* empty = full + kStages;
-    uint64_t* tfull = empty + kStages;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(S) * C::kStageBytes);
+    uint64_t* empty = full + S;
+    uint64_t* tfull = empty + S;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -293,94 +318,105 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int T = args.tiles_m * args.tiles_n;
+    const uint32_t rank = cluster_ctarank();  // 0: issues the pair's MMAs
+    const bool leader = rank == 0;
+    const int cid = blockIdx.x >> 1;
+    const int ncl = gridDim.x >> 1;
+    const int T = args.tiles_m * args.tiles_n * args.k_splits;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], 128);
+            mbar_init(&tempty[b], 8);  // 4 epilogue warps in each CTA of the pair
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, kTmemCols);
-        tmem_relinquish();
+        tmem_alloc_pair(tmem_slot, C::kTmemCols);
+        tmem_relinquish_pair();
     }
     tc_fence_before();
-    __syncthreads();
+    __syncwarp();
+    cluster_sync();  // barriers of both CTAs initialised before any cross-CTA signal
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp == 0) {
         if (lane == 0) {
-            // ---------------- TMA producer ----------------
+            // ---------------- TMA producer (both CTAs) ----------------
             tma_prefetch_desc(&tmA);
             tma_prefetch_desc(&tmB);
             uint32_t stage = 0, phase = 0, issued = 0, issued_phase = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < T; t += gridDim.x) {
-                int tm, tn;
-                tile_coords(args, t, tm, tn);
-                for (int kb = 0; kb < args.k_blocks; ++kb) {
+            for (int t = cid; ok && t < T; t += ncl) {
+                int tm, tn, ks, kb0, kb1;
+                unit_coords(args, t, tm, tn, ks, kb0, kb1);
+                const int a_row = tm * BM + int(rank) * BM_CTA;
+                const int b_row = tn * BN + int(rank) * (BN / 2);
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, kTimeoutNs)) {
                         ok = false;
                         break;
                     }
-                    uint8_t* sa = smem + size_t(stage) * kStageBytes;
+                    uint8_t* sa = smem + size_t(stage) * C::kStageBytes;
                     uint8_t* sb = sa + kABytes;
-                    mbar_arrive_expect_tx(&full[stage], kStageBytes);
+                    // both CTAs' copies complete on the even CTA's barrier
+                    if (leader) mbar_arrive_expect_tx(&full[stage], 2 * C::kStageBytes);
+                    const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
                     if (kAMn) {
 #pragma unroll
-                        for (int j = 0; j < BM / 64; ++j)
-                            tma_load_2d(sa + j * 8192, &tmA, &full[stage], tm * BM + j * 64, kb * BK);
+                        for (int j = 0; j < BM_CTA / 64; ++j)
+                            tma_load_2d_pair(smem_u32(sa + j * 8192), &tmA, fb, a_row + j * 64, kb * BK);
                     } else {
-                        tma_load_2d(sa, &tmA, &full[stage], kb * BK, tm * BM);
+                        tma_load_2d_pair(smem_u32(sa), &tmA, fb, kb * BK, a_row);
                     }
                     if (kBMn) {
 #pragma unroll
-                        for (int j = 0; j < BN / 64; ++j)
-                            tma_load_2d(sb + j * 8192, &tmB, &full[stage], tn * BN + j * 64, kb * BK);
+                        for (int j = 0; j < (BN / 2) / 64; ++j)
+                            tma_load_2d_pair(smem_u32(sb + j * 8192), &tmB, fb, b_row + j * 64, kb * BK);
                     } else {
-                        tma_load_2d(sb, &tmB, &full[stage], kb * BK, tn * BN);
+                        tma_load_2d_pair(smem_u32(sb), &tmB, fb, kb * BK, b_row);
                     }
                     issued |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
-                    if (++stage == kStages) {
+                    if (++stage == uint32_t(S)) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
             }
-            if (!ok) {
+            if (!ok && leader) {
                 // let copies already in flight land before shared memory is released
                 volatile int no_abort = 0;
-                for (int s = 0; s < kStages; ++s)
+                for (int s = 0; s < S; ++s)
                     if ((issued >> s) & 1u) mbar_wait(&full[s], (issued_phase >> s) & 1u, &no_abort, kTimeoutNs);
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ---------------- MMA issuer ----------------
+        if (lane == 0 && leader) {
+            // ---------------- MMA issuer (even CTA) ----------------
             constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN, kAMn, kBMn);
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < T; t += gridDim.x) {
+            for (int t = cid; ok && t < T; t += ncl) {
+                int tm, tn, ks, kb0, kb1;
+                unit_coords(args, t, tm, tn, ks, kb0, kb1);
                 if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, kTimeoutNs)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int kb = 0; kb < args.k_blocks; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(&full[stage], phase, abort_flag, kTimeoutNs)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = smem_u32(smem + size_t(stage) * kStageBytes);
+                    const uint32_t sa = smem_u32(smem + size_t(stage) * C::kStageBytes);
                     const uint32_t sb = sa + kABytes;
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
@@ -388,38 +424,40 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                                                  : smem_desc_sw128(sa + kk * 32, 16, 1024);
                         const uint64_t bd = kBMn ? smem_desc_sw128(sb + kk * 2048, 8192, 1024)
                                                  : smem_desc_sw128(sb + kk * 32, 16, 1024);
-                        umma_bf16(d_tmem, ad, bd, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+                        umma_bf16_pair(d_tmem, ad, bd, kIdesc, (kb > kb0 || kk > 0) ? 1u : 0u);
                     }
-                    umma_commit(&empty[stage]);
-                    if (++stage == kStages) {
+                    umma_commit_pair(&empty[stage], 0x3);  // frees the stage in both CTAs
+                    if (++stage == uint32_t(S)) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                umma_commit(&tfull[acc]);
+                umma_commit_pair(&tfull[acc], 0x3);
                 acc ^= 1u;
                 if (acc == 0) acc_phase ^= 1u;
             }
             // every MMA issued so far completes before tensor memory is released
-            umma_commit(drain);
+            umma_commit_pair(drain, 0x1);
             volatile int no_abort = 0;
             mbar_wait(drain, 0, &no_abort, kTimeoutNs);
         }
     } else {
-        // ---------------- epilogue (warps 2..5) ----------------
+        // ---------------- epilogue (warps 2..5 of both CTAs) ----------------
         const int q = warp & 3;  // tensor-memory lane quadrant this warp may access
+        const uint32_t tempty_leader[2] = {mapa_shared(smem_u32(&tempty[0]), 0), mapa_shared(smem_u32(&tempty[1]), 0)};
         uint32_t acc = 0, acc_phase = 0;
-        for (int t = blockIdx.x; t < T; t += gridDim.x) {
+        for (int t = cid; t < T; t += ncl) {
             bool ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, kTimeoutNs);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
-            int tm, tn;
-            tile_coords(args, t, tm, tn);
+            int tm, tn, ks, kb0, kb1;
+            unit_coords(args, t, tm, tn, ks, kb0, kb1);
             const uint32_t taddr = tmem_base + (uint32_t(q * 32) << 16) + acc * BN;
-            epi(int64_t(tm) * BM + q * 32 + lane, tn, taddr);
+            epi.template run<BN>(int64_t(tm) * BM + int64_t(rank) * BM_CTA + q * 32 + lane, tn, ks, taddr);
             tc_fence_before();
-            mbar_arrive(&tempty[acc]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tempty_leader[acc]);
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
         }
@@ -427,10 +465,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
     __syncthreads();
     if (threadIdx.x == 0 && *abort_flag) report(args.dev_status, VCE_DEVSTATUS_TIMEOUT);
+    tc_fence_before();
+    __syncwarp();
+    cluster_sync();  // the pair is done: no more MMAs, copies or remote arrivals
     if (warp == 1) {
-        __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem_base, kTmemCols);
+        tmem_dealloc_pair(tmem_base, C::kTmemCols);
     }
 }
 
@@ -533,27 +573,65 @@ bool map_mnmajor(CUtensorMap* m, const void* base, int64_t mn, int64_t k, int64_
     return make_map(m, base, uint64_t(mn), uint64_t(k), uint64_t(ld) * 2, 64, BK);
 }
 
-template <class Epi, bool kAMn, bool kBMn>
+template <class Epi, bool kAMn, bool kBMn, int BN>
 vce_status launch_gemm(const CUtensorMap& a, const CUtensorMap& b, int64_t M, int64_t N, int64_t K, int m_fastest,
-                       const Epi& epi, int* dev_status, cudaStream_t s, const DeviceInfo& dev) {
-    auto kern = tc_gemm_kernel<Epi, kAMn, kBMn>;
+                       int k_splits, const Epi& epi, int* dev_status, cudaStream_t s, const DeviceInfo& dev) {
+    using C = PairCfg<BN>;
+    auto kern = tc_gemm_kernel<Epi, kAMn, kBMn, BN>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::kSmemBytes));
     });
     if (attr_err != cudaSuccess) return VCE_ERR_CUDA;
     GemmArgs args;
     args.tiles_m = int((M + BM - 1) / BM);
     args.tiles_n = int((N + BN - 1) / BN);
     args.k_blocks = int((K + BK - 1) / BK);
+    if (k_splits < 1) k_splits = 1;
+    if (k_splits > args.k_blocks) k_splits = args.k_blocks;
+    args.kb_per_split = (args.k_blocks + k_splits - 1) / k_splits;
+    args.k_splits = (args.k_blocks + args.kb_per_split - 1) / args.kb_per_split;  // every chunk non-empty
     args.m_fastest = m_fastest;
     args.dev_status = dev_status;
-    const int64_t tiles = int64_t(args.tiles_m) * args.tiles_n;
-    if (tiles <= 0 || args.k_blocks <= 0) return VCE_OK;
-    const int grid = int(tiles < dev.num_sms ? tiles : dev.num_sms);
-    kern<<<grid, kThreads, kSmemBytes, s>>>(a, b, args, epi);
+    const int64_t units = int64_t(args.tiles_m) * args.tiles_n * args.k_splits;
+    if (units <= 0 || args.k_blocks <= 0) return VCE_OK;
+    const int64_t pairs = dev.num_sms / 2;
+    const int grid = 2 * int(units < pairs ? units : pairs);
+    kern<<<grid, kThreads, C::kSmemBytes, s>>>(a, b, args, epi);
     return cudaGetLastError() == cudaSuccess ? VCE_OK : VCE_ERR_CUDA;
+}
+
+// Number of K chunks for the dX GEMM (K = vocabulary slab): the smallest count
+// in 1..4 whose work units fill the CTA pairs' last round best.
+int dx_k_splits(int64_t n, int64_t h, int num_sms) {
+    const int64_t tiles = ((n + BM - 1) / BM) * ((h + 255) / 256);
+    const int64_t pairs = num_sms / 2;
+    int best = 1;
+    double best_eff = 0.0;
+    for (int s = 1; s <= 4; ++s) {
+        const int64_t units = tiles * s;
+        const int64_t rounds = (units + pairs - 1) / pairs;
+        const double eff = double(units) / double(rounds * pairs);
+        if (eff > best_eff + 0.02) {
+            best_eff = eff;
+            best = s;
+        }
+    }
+    return best;
+}
+
+// dX = sum of the FP32 partials of every K chunk, rounded to BF16 (fixed order).
+__global__ void dx_finalize_kernel(const float* __restrict__ acc, int splits, int64_t split_stride,
+                                   int64_t count4, __nv_bfloat16* __restrict__ dx) {
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < count4; i += int64_t(gridDim.x) * blockDim.x) {
+        float4 v = reinterpret_cast<const float4*>(acc)[i];
+        for (int k = 1; k < splits; ++k) {
+            const float4 w = reinterpret_cast<const float4*>(acc + k * split_stride)[i];
+            v.x += w.x; v.y += w.y; v.z += w.z; v.w += w.w;
+        }
+        reinterpret_cast<uint2*>(dx)[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+    }
 }
 
 struct FwdWs {
@@ -565,7 +643,7 @@ struct FwdWs {
 };
 
 FwdWs carve_forward(void* ws, int64_t n, int64_t v, int reduce_loss) {
-    const int64_t nb = (v + BN - 1) / BN;
+    const int64_t nb = (v + kVocabTile - 1) / kVocabTile;
     FwdWs w{};
     size_t off = 0;
     uint8_t* base = static_cast<uint8_t*>(ws);
@@ -583,6 +661,36 @@ FwdWs carve_forward(void* ws, int64_t n, int64_t v, int reduce_loss) {
 
 int64_t slab_ld(int64_t slab) { return (slab + 7) / 8 * 8; }
 
+// Backward workspace: the BF16 dZ slab, then (unless one slab and one K chunk
+// let dX be written directly) the FP32 dX partial sums of every K chunk.
+struct BwdPlan {
+    int64_t ld;      // dZ slab leading dimension
+    int splits;      // K chunks of the dX GEMM
+    bool direct;     // dX written as BF16 by the GEMM itself
+    size_t dz_bytes, acc_bytes;
+};
+
+BwdPlan plan_backward(int64_t n, int64_t h, int64_t v, int64_t slab, int num_sms) {
+    BwdPlan p;
+    p.ld = slab_ld(slab);
+    // the chunk count the dX launch of the first (widest) slab really uses:
+    // at most one chunk per 64-wide K block, every chunk non-empty
+    const int64_t kb = ((slab < v ? slab : v) + BK - 1) / BK;
+    int splits = dx_k_splits(n, h, num_sms);
+    if (splits > kb) splits = int(kb);
+    const int64_t per = (kb + splits - 1) / splits;
+    p.splits = int((kb + per - 1) / per);
+    p.direct = slab >= v && p.splits == 1;
+    p.dz_bytes = align256(size_t(n) * size_t(p.ld) * 2);
+    p.acc_bytes = p.direct ? 0 : align256(size_t(p.splits) * size_t(n) * size_t(h) * 4);
+    return p;
+}
+
+int planning_sms() {
+    DeviceInfo d;
+    return current_device(d) == VCE_OK ? d.num_sms : 152;
+}
+
 }  // namespace
 
 size_t lce_forward_ws_bytes(int64_t n, int64_t v, int reduce_loss) {
@@ -590,17 +698,18 @@ size_t lce_forward_ws_bytes(int64_t n, int64_t v, int reduce_loss) {
 }
 
 size_t lce_backward_ws_bytes(int64_t n, int64_t h, int64_t v, int64_t slab) {
-    size_t b = align256(size_t(n) * size_t(slab_ld(slab)) * 2);
-    if (slab < v) b += align256(size_t(n) * size_t(h) * 4);
-    return b;
+    const BwdPlan p = plan_backward(n, h, v, slab, planning_sms());
+    return p.dz_bytes + p.acc_bytes;
 }
 
 int64_t lce_slab_for_ws(int64_t n, int64_t h, int64_t v, size_t ws_bytes) {
     if (ws_bytes >= lce_backward_ws_bytes(n, h, v, v)) return v;
-    const size_t acc = align256(size_t(n) * size_t(h) * 4);
-    if (ws_bytes <= acc) return 0;
-    int64_t cap = int64_t((ws_bytes - acc) / (size_t(n) * 2)) / 256 * 256;
-    while (cap >= 256 && lce_backward_ws_bytes(n, h, v, cap) > ws_bytes) cap -= 256;
+    int64_t cap = v / 256 * 256;
+    if (cap < 256) cap = 256;
+    while (cap >= 256 && lce_backward_ws_bytes(n, h, v, cap) > ws_bytes) {
+        const int64_t guess = int64_t(ws_bytes / (size_t(n) * 2)) / 256 * 256;
+        cap = (guess < cap - 256) ? guess : cap - 256;
+    }
     if (cap < 256) return 0;
     return cap < v ? cap : v;
 }
@@ -616,10 +725,11 @@ vce_status launch_lce_forward(const void* X, const void* W, int64_t n, int64_t h
     }
     const FwdWs w = carve_forward(ws, n, v, reduce_loss);
     CUtensorMap tx, tw;
-    if (!map_kmajor(&tx, X, h, n, h, BM) || !map_kmajor(&tw, W, h, v, h, BN)) return VCE_ERR_CUDA;
+    if (!map_kmajor(&tx, X, h, n, h, BM_CTA) || !map_kmajor(&tw, W, h, v, h, kVocabTile / 2)) return VCE_ERR_CUDA;
     FwdEpi epi{target, n, v, w.part_ms, w.part_sum, w.zy, eps != 0.f ? 1 : 0};
-    if (vce_status st = launch_gemm<FwdEpi, false, false>(tx, tw, n, v, h, 1, epi, dev_status, s, dev)) return st;
-    const int nb = int((v + BN - 1) / BN);
+    if (vce_status st = launch_gemm<FwdEpi, false, false, kVocabTile>(tx, tw, n, v, h, 1, 1, epi, dev_status, s, dev))
+        return st;
+    const int nb = int((v + kVocabTile - 1) / kVocabTile);
     float* loss_rows = reduce_loss ? w.loss_rows : loss;
     lce_combine_kernel<<<int((n + kCombRows - 1) / kCombRows), kCombRows * kCombSplit, 0, s>>>(
         w.part_ms, w.part_sum, w.zy, target, n, v, nb, eps, ignore_idx, lse, loss_rows, dev_status);
@@ -638,35 +748,42 @@ vce_status launch_lce_backward(const void* X, const void* W, int64_t n, int64_t 
     if (n == 0) {
         return cudaMemsetAsync(dW, 0, size_t(v) * size_t(h) * 2, s) == cudaSuccess ? VCE_OK : VCE_ERR_CUDA;
     }
-    const int64_t ld = slab_ld(slab);
+    const BwdPlan plan = plan_backward(n, h, v, slab, dev.num_sms);
+    const int64_t ld = plan.ld;
     auto* dz = static_cast<__nv_bfloat16*>(ws);
-    float* acc = slab < v ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + align256(size_t(n) * ld * 2))
-                          : nullptr;
+    float* acc = plan.direct ? nullptr : reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + plan.dz_bytes);
+    const int64_t split_stride = n * h;
     const auto* Wb = static_cast<const __nv_bfloat16*>(W);
     auto* dWb = static_cast<__nv_bfloat16*>(dW);
     auto* dXb = static_cast<__nv_bfloat16*>(dX);
     CUtensorMap tx_k, tx_mn;
-    if (!map_kmajor(&tx_k, X, h, n, h, BM) || !map_mnmajor(&tx_mn, X, h, n, h)) return VCE_ERR_CUDA;
+    if (!map_kmajor(&tx_k, X, h, n, h, BM_CTA) || !map_mnmajor(&tx_mn, X, h, n, h)) return VCE_ERR_CUDA;
     for (int64_t v0 = 0; v0 < v; v0 += slab) {
         const int64_t vs = (v - v0) < slab ? (v - v0) : slab;
-        const bool first = v0 == 0, last = v0 + vs >= v;
         // dZ = epilogue(X W_slab^T): M = n, N = vs, K = h
         CUtensorMap tws_k, tdz_k, tdz_mn, tws_mn;
-        if (!map_kmajor(&tws_k, Wb + v0 * h, h, vs, h, BN) || !map_kmajor(&tdz_k, dz, vs, n, ld, BM) ||
+        if (!map_kmajor(&tws_k, Wb + v0 * h, h, vs, h, kVocabTile / 2) || !map_kmajor(&tdz_k, dz, vs, n, ld, BM_CTA) ||
             !map_mnmajor(&tdz_mn, dz, vs, n, ld) || !map_mnmajor(&tws_mn, Wb + v0 * h, h, vs, h))
             return VCE_ERR_CUDA;
         DzEpi de{target, lse, grad_output, n_valid, reduce_loss, eps, n, v, v0, vs, ld, ignore_idx, dz, dev_status};
-        if (vce_status st = launch_gemm<DzEpi, false, false>(tx_k, tws_k, n, vs, h, 1, de, dev_status, s, dev))
+        if (vce_status st =
+                launch_gemm<DzEpi, false, false, kVocabTile>(tx_k, tws_k, n, vs, h, 1, 1, de, dev_status, s, dev))
             return st;
         // dW_slab = dZ^T X: M = vs, N = h, K = n (both operands MN-major)
-        StoreEpi we{dWb + v0 * h, h, nullptr, 0, 0, vs, h};
-        if (vce_status st = launch_gemm<StoreEpi, true, true>(tdz_mn, tx_mn, vs, h, n, 0, we, dev_status, s, dev))
+        StoreEpi we{dWb + v0 * h, h, nullptr, 0, 0, 0, vs, h};
+        if (vce_status st = launch_gemm<StoreEpi, true, true, 256>(tdz_mn, tx_mn, vs, h, n, 0, 1, we, dev_status, s, dev))
             return st;
-        // dX (+)= dZ W_slab: M = n, N = h, K = vs (W_slab read MN-major)
-        const int mode = (first && last) ? 0 : first ? 1 : last ? 3 : 2;
-        StoreEpi xe{dXb, h, acc, h, mode, n, h};
-        if (vce_status st = launch_gemm<StoreEpi, false, true>(tdz_k, tws_mn, n, h, vs, 1, xe, dev_status, s, dev))
+        // dX (+)= dZ W_slab: M = n, N = h, K = vs (W_slab read MN-major), K cut into plan.splits chunks
+        StoreEpi xe{dXb, h, acc, h, split_stride, plan.direct ? 0 : (v0 == 0 ? 1 : 2), n, h};
+        if (vce_status st = launch_gemm<StoreEpi, false, true, 256>(tdz_k, tws_mn, n, h, vs, 1, plan.splits, xe,
+                                                                    dev_status, s, dev))
             return st;
+    }
+    if (!plan.direct) {
+        const int64_t count4 = n * h / 4;  // h is a multiple of 8
+        const int blocks = int((count4 + 255) / 256 < 4096 ? (count4 + 255) / 256 : 4096);
+        dx_finalize_kernel<<<blocks, 256, 0, s>>>(acc, plan.splits, split_stride, count4, dXb);
+        if (cudaGetLastError() != cudaSuccess) return VCE_ERR_CUDA;
     }
     return VCE_OK;
 }
