@@ -143,10 +143,13 @@ def test_small_linear_workload_full():
 # the oracle (dW rows need the oracle's lse of every token: one FP64 forward)
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("wl", [wk.LINEAR_HEADLINE, wk.LINEAR_LARGE], ids=lambda w: w.name)
-def test_full_size_sampled(wl):
+# the benchmark's launch configurations: the headline in one vocabulary slab, the
+# large workload with its dZ slab capped at 1 GiB (4 slabs, FP32 dX accumulation)
+@pytest.mark.parametrize("wl,slab_cap", [(wk.LINEAR_HEADLINE, 0), (wk.LINEAR_LARGE, 1 << 30)],
+                         ids=["headline", "large_slab1GiB"])
+def test_full_size_sampled(wl, slab_cap):
     inp = wk.make_linear_inputs(wl)
-    f, b = run(inp.x, inp.w, inp.target, wl.label_smoothing, wl.reduce_loss, inp.grad)
+    f, b = run(inp.x, inp.w, inp.target, wl.label_smoothing, wl.reduce_loss, inp.grad, slab_cap)
     assert int(f.dev_status.item()) == 0 and int(b.dev_status.item()) == 0
     n_valid = int((inp.target != -100).sum())
     assert int(f.n_valid.item()) == n_valid

@@ -1,0 +1,55 @@
+"""The multi-process (N > 1) path of bench.py on CPU with the gloo backend.
+
+The hot path does not shard: --gpus N runs N independent replicas, joined only
+by a barrier and a max-over-ranks of the timings.  These tests run that
+plumbing with world_size 2 on the host."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+    import torch.distributed as dist
+    r, w, local, pg = bench.dist_setup(world)
+    assert (r, w) == (rank, world) and pg is not None
+    bench.barrier(pg)
+    out[rank] = bench.max_over_ranks(pg, float(10 + rank * 7))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_barrier_gloo():
+    import torch.multiprocessing as mp
+    mgr = mp.Manager()
+    out = mgr.dict()
+    mp.spawn(_worker, args=(2, free_port(), out), nprocs=2, join=True)
+    assert dict(out) == {0: 17.0, 1: 17.0}
+
+
+def test_torchrun_two_replicas_reference_arm_prints_one_line():
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
+           "--master-addr=127.0.0.1", f"--master-port={free_port()}", os.path.join(ROOT, "bench.py"),
+           "--gpus", "2", "--impl", "reference", "--shape", "64,256,2048", "--steps", "1", "--warmup", "3"]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, env=env, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle"

@@ -218,8 +218,12 @@ def lce_workspace_size(n: int, h: int, v: int, reduce_loss: bool, max_slab_bytes
 
 
 def lce_forward(X, W, target, label_smoothing=0.0, reduce_loss=False, ignore_idx=-100, *,
-                loss=None, lse=None, n_valid=None, workspace=None, dev_status=None, stream=None):
-    """Linear-form forward.  Returns (loss, lse [N], n_valid, dev_status)."""
+                loss=None, lse=None, n_valid=None, workspace=None, max_slab_bytes=0, dev_status=None,
+                stream=None):
+    """Linear-form forward.  Returns (loss, lse [N], n_valid, dev_status).
+
+    A workspace not passed in is allocated with lce_workspace_size(..., max_slab_bytes), the
+    size one workspace shared by lce_forward and lce_backward needs."""
     lib = library()
     X = _bf16_2d(X, "X")
     W = _bf16_2d(W, "W")
@@ -238,8 +242,8 @@ def lce_forward(X, W, target, label_smoothing=0.0, reduce_loss=False, ignore_idx
     if dev_status is None:
         dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
     if workspace is None:
-        workspace = torch.empty(max(1, lce_workspace_size(n, h, v, reduce_loss)), dtype=torch.uint8,
-                                device=dev)
+        workspace = torch.empty(max(1, lce_workspace_size(n, h, v, reduce_loss, max_slab_bytes)),
+                                dtype=torch.uint8, device=dev)
     with torch.cuda.device(dev):
         st = lib.lce_forward(_ptr(X), _ptr(W), n, h, v, _ptr(target), float(label_smoothing),
                              int(bool(reduce_loss)), int(ignore_idx), _ptr(loss), _ptr(lse),
