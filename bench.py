@@ -326,6 +326,31 @@ def peak_extra_memory(step):
     return torch.cuda.max_memory_allocated() - base
 
 
+def time_fused_logits(step, steps, warmup, pg):
+    """Mean ms of ce_forward_backward over ``steps`` timed calls (separate output buffer)."""
+    import torch
+    wl = step.wl
+    stream = torch.cuda.current_stream()
+
+    def one():
+        step.vce.ce_forward_backward(step.d["logits"], step.d["target"], step.d["grad"], wl.label_smoothing,
+                                     wl.reduce_loss, dlogits=step.dlogits, loss=step.loss, stats=step.stats,
+                                     n_valid=step.n_valid, workspace=step.ws, dev_status=step.status)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    barrier(pg)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        one()
+    e.record(stream)
+    torch.cuda.synchronize()
+    barrier(pg)
+    return max_over_ranks(pg, s.elapsed_time(e)) / steps
+
+
 def time_e2e_linear(step, steps, warmup, pg):
     """The same step through the public calls, inputs copied from pinned host memory each step."""
     import torch
@@ -516,6 +541,8 @@ def main():
         bwd_gbs = st.bytes_bwd() / (ph["backward"] / 1e3) / 1e9
         fwd_gbs = st.bytes_fwd() / (ph["forward"] / 1e3) / 1e9
         assert int(st.status.item()) == 0, "device status reported an error"
+        fused_ms = time_fused_logits(st, args.steps, args.warmup, pg)
+        fused_gbs = st.bytes_bwd() / (fused_ms / 1e3) / 1e9
         logits_obj = {
             "metric": "logits-CE fwd+bwd HBM GB/s", "value": gb, "unit": "GB/s",
             "ms_per_step": total / args.steps, "fwd_gbs": fwd_gbs, "bwd_gbs": bwd_gbs,
@@ -533,6 +560,11 @@ def main():
                              "algorithmic_bytes": st.bytes_fwd()},
             "gpu_launches": 3 * args.steps,
             "clocks": clocks_l,
+            # ce_forward_backward: the same results as one forward + backward step with
+            # one HBM read and one write per logit (timed separately, same workload)
+            "fused": {"ms_per_step": fused_ms, "value": fused_gbs, "unit": "GB/s",
+                      "algorithmic_bytes": st.bytes_bwd(), "frac": fused_gbs / pk["hbm"],
+                      "speedup_vs_separate": (total / args.steps) / fused_ms},
         }
         if rank == 0 and not args.no_cpu_baseline:
             logits_obj["cpu_baseline"] = cpu_baseline_logits(st.wl)

@@ -142,6 +142,29 @@ vce_status ce_backward(const void* logits, int dtype, int64_t n_rows, int64_t vo
                        void* dlogits, int* dev_status, void* stream);
 
 /*
+ * Forward and backward of the logits form in one pass, for a caller that knows
+ * the upstream gradient before the loss is computed (the usual training step:
+ * the loss is the objective and grad_output is 1 or a loss scale).  This takes
+ * the pull request's destructive buffer reuse ("Minimize the memory usage of
+ * the fused cross entropy kernel", opt-in mode that reuses the input storage)
+ * one step further: each logit row is read from HBM once, its statistics are
+ * formed, and the same row, still in L2, is turned into its gradient and
+ * written once, so the pair costs one read and one write per logit instead of
+ * two reads and one write.
+ *
+ *   Arguments are those of ce_forward and ce_backward combined; the results are
+ *   the same as ce_forward followed by ce_backward with the same grad_output
+ *   (loss, stats, n_valid, dlogits).  dlogits MAY EQUAL logits (in place).
+ *   grad_output F32 [1] when reduce_loss, else [n_rows].
+ *   ws/ws_bytes: ce_workspace_size(n_rows, vocab, reduce_loss) bytes.
+ */
+vce_status ce_forward_backward(const void* logits, int dtype, int64_t n_rows, int64_t vocab,
+                               int64_t row_stride, const int64_t* target, float label_smoothing,
+                               int reduce_loss, int64_t ignore_idx, const float* grad_output,
+                               float* loss, float* stats, int64_t* n_valid, void* dlogits, void* ws,
+                               size_t ws_bytes, int* dev_status, void* stream);
+
+/*
  * ce_forward for callers that cannot allocate device memory.  The pages have no
  * counterpart of this call; it exists for callers that are handed only their
  * inputs and outputs (a plugin inside another runtime's execution plan, or a

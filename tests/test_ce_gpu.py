@@ -262,3 +262,71 @@ def test_membound_full_size_sampled():
                                 wl.label_smoothing, True, dtype=wl.dtype)
     sel = torch.from_numpy(rows).to(DEV)
     check_rows(f._replace(stats=f.stats), dz[sel], ref, ref_dz, rows, wl.dtype, True, inp.target)
+
+
+# ---------------------------------------------------------------------------
+# fused forward + backward (ce_forward_backward)
+# ---------------------------------------------------------------------------
+
+def run_fused(logits, target, eps, red, grad, ignore_idx=-100, inplace=False):
+    tgt = torch.from_numpy(target).to(DEV)
+    g = torch.from_numpy(np.asarray(grad, np.float32)).to(DEV)
+    r = vce.ce_forward_backward(logits, tgt, g, eps, red, ignore_idx, inplace=inplace)
+    torch.cuda.synchronize()
+    return r
+
+
+FUSED = [
+    # n, vocab, dtype, eps, reduce, inplace
+    (128, 1024, "f32", 0.0, False, False),
+    (128, 1024, "f32", 0.1, True, True),
+    (5, 7, "bf16", 0.1, True, False),
+    (300, 50257, "bf16", 0.1, True, True),
+    (33, 32001, "f32", 0.0, False, True),
+    (6, 262144, "bf16", 0.0, True, False),
+]
+
+
+@pytest.mark.parametrize("n,vocab,dtype,eps,red,inplace", FUSED)
+def test_fused_matches_oracle_and_separate_path(n, vocab, dtype, eps, red, inplace):
+    seed = 3 * n + vocab
+    z = wk.normal_matrix(seed, wk.TID_LOGITS, n, vocab, 3.0, dtype == "bf16")
+    target = wk.uniform_targets(seed, n, vocab, 0.1)
+    grad = np.full(1, 1.5, np.float32) if red else wk.grad_rows(seed, n)
+    a = to_dev(z, dtype)
+    sep_f, sep_dz = run_gpu(a, target, eps, red, grad)
+    b = to_dev(z, dtype)
+    r = run_fused(b, target, eps, red, grad, inplace=inplace)
+    if inplace:
+        assert r.dlogits.data_ptr() == b.data_ptr()
+    # same arithmetic as ce_forward + ce_backward: bit-identical results
+    assert torch.equal(r.stats, sep_f.stats)
+    assert torch.equal(r.loss, sep_f.loss)
+    assert int(r.n_valid.item()) == int(sep_f.n_valid.item())
+    assert torch.equal(r.dlogits.view(torch.int16) if dtype == "bf16" else r.dlogits,
+                       sep_dz.view(torch.int16) if dtype == "bf16" else sep_dz)
+    ref = oracle.ce_forward(z, target, eps, red, dtype=dtype)
+    ref_dz = oracle.ce_backward(z, target, ref["lse"], ref["n_valid"], grad, eps, red, dtype=dtype)
+    check_rows(r, r.dlogits, ref, ref_dz, np.arange(n), dtype, red, target)
+
+
+def test_fused_membound_full_size_inplace():
+    wl = wk.LOGITS_MEMBOUND
+    inp = wk.make_logits_inputs(wl)
+    logits = to_dev(inp.logits, wl.dtype)
+    del inp.logits
+    r = run_fused(logits, inp.target, wl.label_smoothing, wl.reduce_loss, inp.grad, inplace=True)
+    n_valid_ref = int((inp.target != -100).sum())
+    assert int(r.n_valid.item()) == n_valid_ref and int(r.dev_status.item()) == 0
+    loss_rows = _oracle_rows_chunked(wl, inp.target)
+    assert abs(r.loss.item() - oracle.mean_loss(loss_rows, n_valid_ref)) <= 2e-3
+    ign = torch.from_numpy(inp.target == -100).to(DEV)
+    assert torch.count_nonzero(r.dlogits[ign]).item() == 0
+    rng = np.random.default_rng(1)
+    rows = np.unique(np.concatenate([rng.choice(wl.n_rows, 32, replace=False), [0, wl.n_rows - 1]]))
+    z = wk.logits_rows(wl, rows)
+    ref = oracle.ce_forward(z, inp.target[rows], wl.label_smoothing, False, dtype=wl.dtype)
+    ref_dz = oracle.ce_backward(z, inp.target[rows], ref["lse"], n_valid_ref, inp.grad,
+                                wl.label_smoothing, True, dtype=wl.dtype)
+    sel = torch.from_numpy(rows).to(DEV)
+    check_rows(r, r.dlogits[sel], ref, ref_dz, rows, wl.dtype, True, inp.target)

@@ -35,7 +35,7 @@ def _worker(rank, world, port, out):
 
 def test_max_over_ranks_and_barrier_gloo():
     import torch.multiprocessing as mp
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()
     out = mgr.dict()
     mp.spawn(_worker, args=(2, free_port(), out), nprocs=2, join=True)
     assert dict(out) == {0: 17.0, 1: 17.0}

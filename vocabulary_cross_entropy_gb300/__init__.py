@@ -22,6 +22,7 @@ from ._binding import (  # noqa: F401
     ce_forward,
     ce_forward_noalloc,
     ce_backward,
+    ce_forward_backward,
     lce_workspace_size,
     lce_forward,
     lce_backward,

@@ -54,6 +54,9 @@ def library() -> ctypes.CDLL:
     lib.ce_backward.argtypes = [_c_p, _c_int, _c_i64, _c_i64, _c_i64, _c_p, _c_p, _c_p, _c_p, _c_f32,
                                 _c_int, _c_i64, _c_p, _c_p, _c_p]
     lib.ce_backward.restype = _c_int
+    lib.ce_forward_backward.argtypes = [_c_p, _c_int, _c_i64, _c_i64, _c_i64, _c_p, _c_f32, _c_int,
+                                        _c_i64, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_size, _c_p, _c_p]
+    lib.ce_forward_backward.restype = _c_int
     lib.lce_workspace_size.argtypes = [_c_i64, _c_i64, _c_i64, _c_int, _c_size]
     lib.lce_workspace_size.restype = _c_size
     lib.lce_forward.argtypes = [_c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_f32, _c_int, _c_i64,
@@ -205,6 +208,48 @@ def ce_backward(logits, target, stats, n_valid, grad_output, label_smoothing=0.0
                              _ptr(dev_status), _stream(dev, stream))
     _check("ce_backward", st)
     return dlogits
+
+
+CEForwardBackward = namedtuple("CEForwardBackward", "loss stats n_valid dlogits dev_status")
+
+
+def ce_forward_backward(logits, target, grad_output, label_smoothing=0.0, reduce_loss=False,
+                        ignore_idx=-100, *, inplace=False, dlogits=None, loss=None, stats=None,
+                        n_valid=None, workspace=None, dev_status=None, stream=None):
+    """Fused logits-form forward + backward (one HBM read and one write per logit).
+    Returns (loss, stats, n_valid, dlogits, dev_status); dlogits is ``logits`` when ``inplace``."""
+    lib = library()
+    dev = logits.device
+    n, vocab, stride = _rows_view(logits)
+    target = _target(target, n)
+    if inplace:
+        dlogits = logits
+    elif dlogits is None:
+        dlogits = torch.empty_like(logits)
+    if dlogits.stride() != logits.stride() or dlogits.dtype != logits.dtype:
+        raise ValueError("dlogits must have the dtype and strides of logits")
+    grad_output = grad_output.to(device=dev, dtype=torch.float32).contiguous()
+    if loss is None:
+        loss = torch.empty(1 if reduce_loss else n, dtype=torch.float32, device=dev)
+    if stats is None:
+        stats = torch.empty(n, 2, dtype=torch.float32, device=dev)
+    if n_valid is None:
+        n_valid = torch.empty(1, dtype=torch.int64, device=dev)
+    if dev_status is None:
+        dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws_bytes = ce_workspace_size(n, vocab, reduce_loss)
+    if workspace is None and ws_bytes:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        st = lib.ce_forward_backward(_ptr(logits), _dtype_code(logits), n, vocab, stride, _ptr(target),
+                                     float(label_smoothing), int(bool(reduce_loss)), int(ignore_idx),
+                                     _ptr(grad_output), _ptr(loss), _ptr(stats), _ptr(n_valid),
+                                     _ptr(dlogits), _ptr(workspace),
+                                     0 if workspace is None else workspace.numel(),
+                                     _ptr(dev_status), _stream(dev, stream))
+    _check("ce_forward_backward", st)
+    return CEForwardBackward(loss if reduce_loss else loss.view(logits.shape[:-1]), stats, n_valid,
+                             dlogits, dev_status)
 
 
 def _bf16_2d(t, name):

@@ -372,6 +372,183 @@ void bwd_dispatch(const void* logits, int64_t n_rows, int64_t vocab, int64_t str
                                                        grad_output, eps, reduce_loss, ignore_idx, dz, dev_status);
 }
 
+// ---------------------------------------------------------------------------
+// fused forward + backward (one HBM read, one HBM write per element)
+// ---------------------------------------------------------------------------
+
+// Streams one row through the online (max, sum exp) accumulator.
+template <int THREADS, int U, typename T, bool kSmooth>
+__device__ __forceinline__ void row_online_lse(const T* p, const RowSplit<T>& sp, int64_t vocab, OnlineLse& acc) {
+    using E = Elem<T>;
+    constexpr int V = E::kVec;
+    if (threadIdx.x < sp.head) {
+        float v[1] = {E::load1(p + threadIdx.x)};
+        acc.push<1, kSmooth>(v);
+    }
+    const uint4* pv = reinterpret_cast<const uint4*>(p + sp.head);
+    int64_t i = threadIdx.x;
+    for (; i + (U - 1) * THREADS < sp.nvec; i += U * THREADS) {
+        uint4 raw[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) raw[u] = pv[i + u * THREADS];  // default caching: the row is read again
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            float v[V];
+            E::unpack(raw[u], v);
+            acc.push<V, kSmooth>(v);
+        }
+    }
+    for (; i < sp.nvec; i += THREADS) {
+        float v[V];
+        E::unpack(pv[i], v);
+        acc.push<V, kSmooth>(v);
+    }
+    for (int64_t j = sp.tail0 + threadIdx.x; j < vocab; j += THREADS) {
+        float v[1] = {E::load1(p + j)};
+        acc.push<1, kSmooth>(v);
+    }
+}
+
+template <int THREADS, typename T>
+__device__ __forceinline__ void row_zero(T* q, const RowSplit<T>& sp, int64_t vocab) {
+    using E = Elem<T>;
+    if (threadIdx.x < sp.head) E::store1(q + threadIdx.x, 0.f);
+    uint4* qv = reinterpret_cast<uint4*>(q + sp.head);
+    for (int64_t i = threadIdx.x; i < sp.nvec; i += THREADS) qv[i] = make_uint4(0, 0, 0, 0);
+    for (int64_t j = sp.tail0 + threadIdx.x; j < vocab; j += THREADS) E::store1(q + j, 0.f);
+}
+
+// Row kernel doing the forward and, with the row still in L2, the backward:
+// loss, (max, lse) and dlogits = g (softmax - (1-eps) onehot - eps/V) from one
+// pass over HBM in each direction.  A persistent grid of two CTAs per SM keeps
+// about 2 x 152 rows in flight, small enough for their second read to hit L2.
+// dlogits may equal logits (the row is overwritten by its gradient).
+template <int THREADS, int MINB, int U1, typename T, bool kSmooth>
+__global__ void __launch_bounds__(THREADS, MINB)
+ce_fused_rows(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, const int64_t* __restrict__ target,
+              float eps, int64_t ignore_idx, const int64_t* __restrict__ n_valid,
+              const float* __restrict__ grad_output, int reduce_loss, float* __restrict__ loss_rows,
+              float2* __restrict__ stats, T* dlogits, int* dev_status) {
+    using E = Elem<T>;
+    constexpr int V = E::kVec;
+    constexpr int U = 2;
+    __shared__ float sm_m[32], sm_s[32], sm_sum[32];
+    __shared__ float sm_lse;
+
+    for (int64_t row = blockIdx.x; row < n_rows; row += gridDim.x) {
+        const int64_t y = target[row];
+        const T* p = logits + row * stride;
+        T* q = dlogits + row * stride;
+        const RowSplit<T> sp(p, vocab);
+        if (y == ignore_idx) {
+            if (threadIdx.x == 0) {
+                loss_rows[row] = 0.f;
+                stats[row] = make_float2(0.f, 0.f);
+            }
+            row_zero<THREADS, T>(q, sp, vocab);
+            continue;
+        }
+        OnlineLse acc;
+        row_online_lse<THREADS, U1, T, kSmooth>(p, sp, vocab, acc);
+        block_merge<THREADS, kSmooth>(acc, sm_m, sm_s, sm_sum);
+        const bool bad = y < 0 || y >= vocab;
+        if (threadIdx.x == 0) {
+            const float lse = acc.m + logf(acc.s);
+            float loss;
+            if (!bad) {
+                const float zy = E::load1(p + y);
+                loss = lse - zy;
+                if (kSmooth) loss = (1.f - eps) * loss + eps * (lse - acc.sum / float(vocab));
+            } else {
+                loss = __int_as_float(0x7fc00000);
+                report(dev_status, VCE_DEVSTATUS_BAD_TARGET);
+            }
+            loss_rows[row] = loss;
+            stats[row] = make_float2(acc.m, lse);
+            sm_lse = lse;
+        }
+        __syncthreads();
+        if (bad) {
+            row_zero<THREADS, T>(q, sp, vocab);
+            __syncthreads();
+            continue;
+        }
+        const float g = reduce_loss ? grad_output[0] / float(n_valid[0]) : grad_output[row];
+        const float negl = -sm_lse * kLog2e;
+        const float b = g * eps / float(vocab);
+        const float c = g * (1.f - eps);
+        auto grad1 = [&](int64_t j) {
+            const float z = E::load1(p + j);
+            float d = fmaf(g, ex2f(fmaf(z, kLog2e, negl)), -b);
+            if (j == y) d -= c;
+            E::store1(q + j, d);
+        };
+        if (threadIdx.x < sp.head) grad1(threadIdx.x);
+        const uint4* pv = reinterpret_cast<const uint4*>(p + sp.head);
+        uint4* qv = reinterpret_cast<uint4*>(q + sp.head);
+        auto gradv = [&](const uint4& raw, int64_t i) {
+            float v[V];
+            E::unpack(raw, v);
+#pragma unroll
+            for (int k = 0; k < V; ++k) v[k] = fmaf(g, ex2f(fmaf(v[k], kLog2e, negl)), -b);
+            const int64_t base = sp.head + i * V;
+            if (uint64_t(y - base) < uint64_t(V)) {
+#pragma unroll
+                for (int k = 0; k < V; ++k) v[k] -= (base + k == y) ? c : 0.f;
+            }
+            __stcs(qv + i, E::pack(v));
+        };
+        int64_t i = threadIdx.x;
+        for (; i + (U - 1) * THREADS < sp.nvec; i += U * THREADS) {
+            uint4 raw[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) raw[u] = __ldcs(pv + i + u * THREADS);
+#pragma unroll
+            for (int u = 0; u < U; ++u) gradv(raw[u], i + u * THREADS);
+        }
+        for (; i < sp.nvec; i += THREADS) gradv(__ldcs(pv + i), i);
+        for (int64_t j = sp.tail0 + threadIdx.x; j < vocab; j += THREADS) grad1(j);
+        __syncthreads();  // shared scratch reused by the next row
+    }
+}
+
+template <typename T, int THREADS, int MINB, int U1>
+void fused_launch(const void* logits, int64_t n_rows, int64_t vocab, int64_t stride, const int64_t* target,
+                  float eps, int64_t ignore_idx, const int64_t* n_valid, const float* grad_output,
+                  int reduce_loss, float* loss_rows, float* stats, void* dlogits, int* dev_status,
+                  cudaStream_t s, int num_sms) {
+    const T* z = static_cast<const T*>(logits);
+    T* dz = static_cast<T*>(dlogits);
+    float2* st = reinterpret_cast<float2*>(stats);
+    const int64_t cap = int64_t(num_sms) * MINB;
+    const int grid = int(n_rows < cap ? n_rows : cap);
+    if (eps != 0.f)
+        ce_fused_rows<THREADS, MINB, U1, T, true><<<grid, THREADS, 0, s>>>(
+            z, n_rows, vocab, stride, target, eps, ignore_idx, n_valid, grad_output, reduce_loss, loss_rows, st,
+            dz, dev_status);
+    else
+        ce_fused_rows<THREADS, MINB, U1, T, false><<<grid, THREADS, 0, s>>>(
+            z, n_rows, vocab, stride, target, eps, ignore_idx, n_valid, grad_output, reduce_loss, loss_rows, st,
+            dz, dev_status);
+}
+
+template <typename T>
+void fused_dispatch(const void* logits, int64_t n_rows, int64_t vocab, int64_t stride, const int64_t* target,
+                    float eps, int64_t ignore_idx, const int64_t* n_valid, const float* grad_output,
+                    int reduce_loss, float* loss_rows, float* stats, void* dlogits, int* dev_status,
+                    cudaStream_t s, int num_sms) {
+    const int64_t nvec = vocab / Elem<T>::kVec;
+    if (nvec <= 1024)
+        fused_launch<T, 128, 8, 4>(logits, n_rows, vocab, stride, target, eps, ignore_idx, n_valid, grad_output,
+                                      reduce_loss, loss_rows, stats, dlogits, dev_status, s, num_sms);
+    else if (nvec <= 4096)
+        fused_launch<T, 256, 4, 4>(logits, n_rows, vocab, stride, target, eps, ignore_idx, n_valid, grad_output,
+                                      reduce_loss, loss_rows, stats, dlogits, dev_status, s, num_sms);
+    else
+        fused_launch<T, 512, 2, 4>(logits, n_rows, vocab, stride, target, eps, ignore_idx, n_valid, grad_output,
+                                      reduce_loss, loss_rows, stats, dlogits, dev_status, s, num_sms);
+}
+
 int row_grid(int64_t n_rows) {
     const int64_t cap = int64_t(1) << 30;
     return int(n_rows < cap ? n_rows : cap);
@@ -421,6 +598,32 @@ vce_status launch_ce_backward(const void* logits, int dtype, int64_t n_rows, int
         bwd_dispatch<float>(logits, n_rows, vocab, row_stride, target, stats, n_valid, grad_output,
                             eps, reduce_loss, ignore_idx, dlogits, dev_status, s, grid);
     return cudaGetLastError() == cudaSuccess ? VCE_OK : VCE_ERR_CUDA;
+}
+
+vce_status launch_ce_forward_backward(const void* logits, int dtype, int64_t n_rows, int64_t vocab,
+                                      int64_t row_stride, const int64_t* target, float eps, int reduce_loss,
+                                      int64_t ignore_idx, const float* grad_output, float* loss, float* stats,
+                                      int64_t* n_valid, void* dlogits, void* ws, int* dev_status,
+                                      cudaStream_t s, const DeviceInfo& dev) {
+    float* loss_rows = reduce_loss ? static_cast<float*>(ws) : loss;
+    if (n_rows > 0) {
+        // N_v first: the mean's upstream gradient g / N_v is needed inside the row pass
+        if (reduce_loss)
+            if (vce_status st = launch_mean_loss(nullptr, target, n_rows, ignore_idx, nullptr, n_valid, s))
+                return st;
+        if (dtype == VCE_BF16)
+            fused_dispatch<__nv_bfloat16>(logits, n_rows, vocab, row_stride, target, eps, ignore_idx, n_valid,
+                                          grad_output, reduce_loss, loss_rows, stats, dlogits, dev_status, s,
+                                          dev.num_sms);
+        else
+            fused_dispatch<float>(logits, n_rows, vocab, row_stride, target, eps, ignore_idx, n_valid,
+                                  grad_output, reduce_loss, loss_rows, stats, dlogits, dev_status, s, dev.num_sms);
+        if (cudaGetLastError() != cudaSuccess) return VCE_ERR_CUDA;
+    }
+    if (reduce_loss || n_valid)
+        return launch_mean_loss(reduce_loss ? loss_rows : nullptr, target, n_rows, ignore_idx,
+                                reduce_loss ? loss : nullptr, n_valid, s);
+    return VCE_OK;
 }
 
 }  // namespace vce

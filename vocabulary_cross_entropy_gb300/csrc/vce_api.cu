@@ -115,6 +115,31 @@ vce_status ce_backward(const void* logits, int dtype, int64_t n_rows, int64_t vo
                               dev_status, static_cast<cudaStream_t>(stream), dev);
 }
 
+vce_status ce_forward_backward(const void* logits, int dtype, int64_t n_rows, int64_t vocab,
+                               int64_t row_stride, const int64_t* target, float label_smoothing,
+                               int reduce_loss, int64_t ignore_idx, const float* grad_output,
+                               float* loss, float* stats, int64_t* n_valid, void* dlogits, void* ws,
+                               size_t ws_bytes, int* dev_status, void* stream) {
+    if (dtype != VCE_BF16 && dtype != VCE_F32) return VCE_ERR_DTYPE;
+    if (n_rows < 0 || vocab < 1 || row_stride < vocab || !eps_ok(label_smoothing))
+        return VCE_ERR_INVALID_ARG;
+    if (!loss || (n_rows > 0 && (!logits || !target || !stats || !grad_output || !dlogits)))
+        return VCE_ERR_INVALID_ARG;
+    if (reduce_loss && !n_valid) return VCE_ERR_INVALID_ARG;
+    const size_t es = elem_size(dtype);
+    if (!aligned(logits, es) || !aligned(dlogits, es) || !aligned(stats, 8)) return VCE_ERR_ALIGN;
+    if (((reinterpret_cast<uintptr_t>(logits) ^ reinterpret_cast<uintptr_t>(dlogits)) & 15) != 0)
+        return VCE_ERR_ALIGN;
+    const size_t need = ce_workspace_size(n_rows, vocab, reduce_loss);
+    if (need > 0 && (!ws || ws_bytes < need)) return VCE_ERR_WORKSPACE;
+    if (ws && !aligned(ws, 256)) return VCE_ERR_ALIGN;
+    DeviceInfo dev;
+    if (vce_status st = current_device(dev)) return st;
+    return launch_ce_forward_backward(logits, dtype, n_rows, vocab, row_stride, target, label_smoothing,
+                                      reduce_loss, ignore_idx, grad_output, loss, stats, n_valid, dlogits, ws,
+                                      dev_status, static_cast<cudaStream_t>(stream), dev);
+}
+
 size_t lce_workspace_size(int64_t n, int64_t h, int64_t v, int reduce_loss,
                           size_t max_slab_bytes) {
     if (n <= 0 || h <= 0 || v <= 0) return 0;

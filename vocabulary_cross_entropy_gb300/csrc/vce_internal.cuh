@@ -51,6 +51,11 @@ vce_status launch_ce_backward(const void* logits, int dtype, int64_t n_rows, int
                               const int64_t* n_valid, const float* grad_output, float eps,
                               int reduce_loss, int64_t ignore_idx, void* dlogits,
                               int* dev_status, cudaStream_t s, const DeviceInfo& dev);
+vce_status launch_ce_forward_backward(const void* logits, int dtype, int64_t n_rows, int64_t vocab,
+                                      int64_t row_stride, const int64_t* target, float eps, int reduce_loss,
+                                      int64_t ignore_idx, const float* grad_output, float* loss, float* stats,
+                                      int64_t* n_valid, void* dlogits, void* ws, int* dev_status,
+                                      cudaStream_t s, const DeviceInfo& dev);
 // mean of per-row losses over rows whose target is not ignore_idx, and the count
 vce_status launch_mean_loss(const float* loss_rows, const int64_t* target, int64_t n_rows,
                             int64_t ignore_idx, float* loss_out, int64_t* n_valid,
