@@ -37,10 +37,11 @@
  *     function replaces).  Loss and gradient arithmetic is FP32 whatever the
  *     input dtype ("Description": "Loss and gradient computation in FP32").
  *   - Rows whose target equals ``ignore_idx`` give loss 0 and gradient 0.
- *   - ``reduce_loss`` != 0: the loss is sum_n loss_n / N_v, N_v = number of rows
- *     whose target is not ignore_idx (NaN when N_v = 0), and backward uses
- *     g_n = grad_output[0] / N_v.  Otherwise loss is per row and
- *     g_n = grad_output[n].
+ *   - ``reduce_loss``: VCE_REDUCE_MEAN (1): the loss is sum_n loss_n / N_v,
+ *     N_v = number of rows whose target is not ignore_idx (NaN when N_v = 0),
+ *     and backward uses g_n = grad_output[0] / N_v.  VCE_REDUCE_SUM (2): the
+ *     loss is sum_n loss_n and g_n = grad_output[0].  VCE_REDUCE_NONE (0): the
+ *     loss is per row and g_n = grad_output[n].  Other values are rejected.
  *   - Host-detectable errors return a status before any launch and write
  *     nothing.  Errors found on the device are ORed into ``*dev_status`` (a
  *     device int the caller zeroes and reads after its own synchronisation;
@@ -79,6 +80,11 @@ typedef enum vce_dtype {
 #define VCE_DEVSTATUS_BAD_TARGET 1
 #define VCE_DEVSTATUS_TIMEOUT 2
 
+/* reduce_loss values */
+#define VCE_REDUCE_NONE 0 /* per-row loss */
+#define VCE_REDUCE_MEAN 1 /* sum over rows / N_v (the API card's reduce_loss=True) */
+#define VCE_REDUCE_SUM 2  /* sum over rows (the Cut Cross-Entropy card's reduction='sum') */
+
 /* Human-readable name of a vce_status value (static string, never NULL). */
 const char* vce_status_string(int status);
 
@@ -90,8 +96,8 @@ int vce_version(void);
 /* ------------------------------------------------------------------------ */
 
 /*
- * Bytes of device workspace ce_forward needs: n_rows * 4 (per-row losses,
- * rounded up to 256 B) when reduce_loss != 0, else 0.
+ * Bytes of device workspace ce_forward and ce_forward_backward need: n_rows * 4
+ * (per-row losses, rounded up to 256 B) when reduce_loss != 0, else 0.
  */
 size_t ce_workspace_size(int64_t n_rows, int64_t vocab, int reduce_loss);
 
@@ -106,10 +112,10 @@ size_t ce_workspace_size(int64_t n_rows, int64_t vocab, int reduce_loss);
  *   row_stride  elements between rows, >= vocab.
  *   target      [n_rows] int64.
  *   label_smoothing in [0, 1].
- *   loss        F32: [1] when reduce_loss, else [n_rows] (0 for ignored rows).
+ *   loss        F32: [1] when reduce_loss != 0, else [n_rows] (0 for ignored rows).
  *   stats       F32 [n_rows, 2]: (max_v z, lse) per row, the only state backward
  *               needs.  Rows with target == ignore_idx are never read and get (0, 0).
- *   n_valid     int64 [1]: N_v, written when non-NULL; required when reduce_loss
+ *   n_valid     int64 [1]: N_v, written when non-NULL; required for VCE_REDUCE_MEAN
  *               (backward reads it).
  *   ws/ws_bytes workspace of at least ce_workspace_size(...) bytes, 256-B aligned
  *               (may be NULL when that size is 0).
@@ -128,8 +134,8 @@ vce_status ce_forward(const void* logits, int dtype, int64_t n_rows, int64_t voc
  *   logits, dtype, n_rows, vocab, row_stride, target, label_smoothing,
  *   reduce_loss, ignore_idx: as passed to ce_forward.
  *   stats       F32 [n_rows, 2] from ce_forward (only the lse column is read).
- *   n_valid     int64 [1] from ce_forward (read only when reduce_loss).
- *   grad_output F32 [1] when reduce_loss, else [n_rows].
+ *   n_valid     int64 [1] from ce_forward (read only for VCE_REDUCE_MEAN).
+ *   grad_output F32 [1] when reduce_loss != 0, else [n_rows].
  *   dlogits     same dtype and layout (row_stride) as logits; MAY EQUAL logits,
  *               in which case the logits are overwritten by their gradient (the
  *               pull request's destructive mode: no extra buffer).  Any other
@@ -201,7 +207,8 @@ vce_status ce_forward_noalloc(const void* logits, int dtype, int64_t n_rows, int
  * 256 vocabulary rows.  With more than one slab, dX is accumulated in an FP32
  * [n, h] buffer inside the workspace.  The forward part holds per-tile
  * softmax partials (12 B per token per 256 vocabulary ids) and the per-token
- * target logit.  The same size passed to lce_backward selects the same slab.
+ * target logit, and the per-tile entropy partials (4 B more per token per 256
+ * ids).  The same size passed to lce_backward selects the same slab.
  */
 size_t lce_workspace_size(int64_t n, int64_t h, int64_t v, int reduce_loss,
                           size_t max_slab_bytes);
@@ -218,14 +225,18 @@ size_t lce_workspace_size(int64_t n, int64_t h, int64_t v, int reduce_loss,
  *   loss   F32 [1] (reduce_loss) or [n].
  *   lse    F32 [n]: log-sum-exp of every row (ignored rows included), the state
  *          lce_backward needs.
- *   n_valid int64 [1], written when non-NULL; required when reduce_loss.
+ *   entropy F32 [n] or NULL: per-token entropy of the softmax,
+ *          H_n = -sum_v p_v log p_v = lse_n - sum_v p_v z[n, v], for every row
+ *          (the Liger pull request's optional entropy output, "Summary").
+ *   n_valid int64 [1], written when non-NULL; required for VCE_REDUCE_MEAN.
  *   ws/ws_bytes at least lce_workspace_size(n, h, v, reduce_loss, *) bytes,
  *          256-B aligned.
  */
 vce_status lce_forward(const void* X, const void* W, int64_t n, int64_t h, int64_t v,
                        const int64_t* target, float label_smoothing, int reduce_loss,
-                       int64_t ignore_idx, float* loss, float* lse, int64_t* n_valid,
-                       void* ws, size_t ws_bytes, int* dev_status, void* stream);
+                       int64_t ignore_idx, float* loss, float* lse, float* entropy,
+                       int64_t* n_valid, void* ws, size_t ws_bytes, int* dev_status,
+                       void* stream);
 
 /*
  * Backward of the linear form (Liger pull request "Implementation", "Backward":
@@ -234,8 +245,8 @@ vce_status lce_forward(const void* X, const void* W, int64_t n, int64_t h, int64
  *
  *   X, W, n, h, v, target, label_smoothing, reduce_loss, ignore_idx: as forward.
  *   lse        F32 [n] from lce_forward.
- *   n_valid    int64 [1] from lce_forward (read only when reduce_loss).
- *   grad_output F32 [1] (reduce_loss) or [n].
+ *   n_valid    int64 [1] from lce_forward (read only for VCE_REDUCE_MEAN).
+ *   grad_output F32 [1] (reduce_loss != 0) or [n].
  *   dX         BF16 [n, h], 16-byte aligned; fully written.
  *   dW         BF16 [v, h], 16-byte aligned; fully written.
  *   ws/ws_bytes at least lce_workspace_size(n, h, v, reduce_loss, 0 or a cap);

@@ -23,9 +23,11 @@ Logits form -- Transformer Engine ``parallel_cross_entropy`` (API card,
   row is never read: their saved statistics are written as (0, 0);
 * a target that is neither ``ignore_idx`` nor in [0, V) is an error: that row's
   loss is NaN, its gradient row is 0, and ``bad`` flags it;
-* ``reduce_loss`` returns sum_n loss_n / N_v with N_v the number of rows whose
-  target is not ``ignore_idx`` (NaN when N_v = 0), and then the per-row upstream
-  gradient is g / N_v;
+* ``reduce_loss`` = 1 (mean) returns sum_n loss_n / N_v with N_v the number of
+  rows whose target is not ``ignore_idx`` (NaN when N_v = 0), and then the
+  per-row upstream gradient is g / N_v; ``reduce_loss`` = 2 (sum, the Cut
+  Cross-Entropy card's reduction modes beside 'none') returns sum_n loss_n with
+  upstream gradient g for every row; 0 (none) returns the per-row losses;
 * the saved state is the per-row statistics (m_n, lse_n) instead of the full
   derivative (pull request #3273, "Changes"); backward rebuilds
     dz[n, v] = g_n * (exp(z[n, v] - lse_n) - (1 - eps) [v = y_n] - eps / V).
@@ -37,7 +39,9 @@ log-sum-exp over the vocabulary kept) and the Liger SM100 pull request
 
 * z = X @ W^T  (X [N, H], W [V, H]); loss and lse as above, lse kept for every
   row (the logits of ignored rows are computed anyway);
-* dZ by the formula above, dX = dZ @ W, dW = dZ^T @ X.
+* dZ by the formula above, dX = dZ @ W, dW = dZ^T @ X;
+* optional per-token entropy of the softmax (Liger pull request, "Summary":
+  optional entropy): H_n = -sum_v p_v log p_v = lse_n - sum_v p_v z[n, v].
 
 Inputs are the exact stored values (bfloat16 or float32) widened to float64.
 The matrix products use NumPy's float64 matmul as a library step; every other
@@ -56,7 +60,7 @@ __all__ = [
     "widen", "row_stats", "row_loss", "grad_columns",
     "ce_forward", "ce_backward", "lce_logits", "lce_forward", "lce_backward",
     "lce_forward_rows", "lce_dx_rows", "lce_lse_all", "lce_dw_rows",
-    "mean_loss",
+    "mean_loss", "reduce", "row_entropy", "upstream",
 ]
 
 
@@ -129,8 +133,10 @@ def grad_columns(z_cols: np.ndarray, cols: np.ndarray, vocab: int, target: np.nd
     return dz
 
 
-def _upstream(grad_output, n: int, n_valid: int, reduce_loss: bool) -> np.ndarray:
+def _upstream(grad_output, n: int, n_valid: int, reduce_loss) -> np.ndarray:
     grad_output = np.asarray(grad_output, dtype=np.float64).reshape(-1)
+    if int(reduce_loss) == 2:
+        return np.full(n, grad_output[0])
     if reduce_loss:
         if n_valid == 0:
             return np.zeros(n)
@@ -142,6 +148,20 @@ def mean_loss(loss_rows: np.ndarray, n_valid: int) -> float:
     """sum_n loss_n / N_v (0/0 = NaN when every row is ignored)."""
     with np.errstate(invalid="ignore", divide="ignore"):
         return float(np.float64(loss_rows.sum()) / np.float64(n_valid))
+
+
+def reduce(loss_rows: np.ndarray, n_valid: int, reduce_loss):
+    """The loss a call returns: per-row (0), mean over non-ignored rows (1) or sum (2)."""
+    if int(reduce_loss) == 2:
+        return float(loss_rows.sum())
+    return mean_loss(loss_rows, n_valid) if reduce_loss else loss_rows
+
+
+def row_entropy(z: np.ndarray, lse: np.ndarray) -> np.ndarray:
+    """H_n = lse_n - sum_v p_v z[n, v] with p_v = exp(z[n, v] - lse_n)."""
+    with np.errstate(invalid="ignore", over="ignore"):
+        p = np.exp(z - lse[:, None])
+    return lse - (p * z).sum(axis=1)
 
 
 # ---------------------------------------------------------------------------
@@ -160,7 +180,7 @@ def ce_forward(z, target, label_smoothing: float = 0.0, reduce_loss: bool = Fals
     m = np.where(ignored, 0.0, m)
     lse = np.where(ignored, 0.0, lse)
     n_valid = int((~ignored).sum())
-    loss = mean_loss(loss_rows, n_valid) if reduce_loss else loss_rows
+    loss = reduce(loss_rows, n_valid, reduce_loss)
     return dict(loss=loss, loss_rows=loss_rows, m=m, lse=lse, n_valid=n_valid, bad=bad)
 
 
@@ -193,8 +213,9 @@ def lce_forward(x, w, target, label_smoothing: float = 0.0, reduce_loss: bool = 
     _, lse = row_stats(z)
     loss_rows = row_loss(z, target, lse, label_smoothing, ignore_idx)
     n_valid = int((~ignored).sum())
-    loss = mean_loss(loss_rows, n_valid) if reduce_loss else loss_rows
-    return dict(loss=loss, loss_rows=loss_rows, lse=lse, n_valid=n_valid, bad=bad, z=z)
+    loss = reduce(loss_rows, n_valid, reduce_loss)
+    return dict(loss=loss, loss_rows=loss_rows, lse=lse, n_valid=n_valid, bad=bad, z=z,
+                entropy=row_entropy(z, lse))
 
 
 def lce_backward(x, w, target, lse, n_valid: int, grad_output, label_smoothing: float = 0.0,
@@ -221,20 +242,24 @@ def lce_forward_rows(x_rows, w, target_rows, label_smoothing: float = 0.0,
 
 
 def lce_lse_all(x, w, target, label_smoothing: float = 0.0, ignore_idx: int = -100,
-                rows_per_chunk: int = 512):
-    """lse and loss for every token, rows processed in independent chunks (each row whole)."""
+                rows_per_chunk: int = 512, entropy: bool = False):
+    """lse and loss (and optionally the entropy) for every token, rows processed in
+    independent chunks (each row whole)."""
     n = x.shape[0]
     wd = widen(w)
     target = np.asarray(target, dtype=np.int64)
     lse = np.empty(n)
     loss = np.empty(n)
+    ent = np.empty(n)
     for r0 in range(0, n, rows_per_chunk):
         r1 = min(n, r0 + rows_per_chunk)
         z = widen(x[r0:r1]) @ wd.T
         _, l = row_stats(z)
         lse[r0:r1] = l
         loss[r0:r1] = row_loss(z, target[r0:r1], l, label_smoothing, ignore_idx)
-    return lse, loss
+        if entropy:
+            ent[r0:r1] = row_entropy(z, l)
+    return lse, loss, (ent if entropy else None)
 
 
 def lce_dx_rows(x_rows, w, target_rows, lse_rows, g_rows, label_smoothing: float = 0.0,

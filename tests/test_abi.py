@@ -89,7 +89,7 @@ def test_lce_host_validation(lib):
 
     def call(x=FAKE, w=FAKE, n=16, h=64, v=100, ws=FAKE, ws_bytes=1 << 30):
         return f(P(x), P(w), I64(n), I64(h), I64(v), P(FAKE), ctypes.c_float(0.0), 0, I64(-100),
-                 P(FAKE), P(FAKE), P(FAKE), P(ws), ctypes.c_size_t(ws_bytes), P(None), P(None))
+                 P(FAKE), P(FAKE), P(None), P(FAKE), P(ws), ctypes.c_size_t(ws_bytes), P(None), P(None))
 
     assert call(h=60) == ALIGN         # h must be a multiple of 8 (16-byte TMA strides)
     assert call(x=FAKE + 8) == ALIGN

@@ -39,10 +39,10 @@ def rel(a, b):
     return np.linalg.norm(a - b) / nb if nb > 0 else np.linalg.norm(a)
 
 
-def run(x, w, target, eps, red, grad, max_slab_bytes=0):
+def run(x, w, target, eps, red, grad, max_slab_bytes=0, entropy=True):
     xt, wt = dev_bf16(x), dev_bf16(w)
     yt = torch.from_numpy(target).to(DEV)
-    f = vce.lce_forward(xt, wt, yt, eps, red)
+    f = vce.lce_forward(xt, wt, yt, eps, red, entropy=entropy)
     g = torch.from_numpy(np.asarray(grad, np.float32)).to(DEV)
     b = vce.lce_backward(xt, wt, yt, f.lse, f.n_valid, g, eps, red, max_slab_bytes=max_slab_bytes)
     torch.cuda.synchronize()
@@ -57,7 +57,12 @@ def check_full(x, w, target, eps, red, grad, max_slab_bytes=0):
     assert int(f.n_valid.item()) == ref["n_valid"]
     lse = f.lse.double().cpu().numpy()
     assert np.max(np.abs(lse - ref["lse"])) <= 2e-3
-    if red:
+    ent = f.entropy.double().cpu().numpy()
+    assert np.max(np.abs(ent - ref["entropy"])) <= 2e-3
+    if red == 2:
+        # a sum over N rows: 2e-3 per row
+        assert abs(f.loss.item() - ref["loss"]) <= 2e-3 * max(1, ref["n_valid"]), (f.loss.item(), ref["loss"])
+    elif red:
         assert abs(f.loss.item() - ref["loss"]) <= 2e-3, (f.loss.item(), ref["loss"])
     else:
         assert np.max(np.abs(f.loss.double().cpu().numpy() - ref["loss"])) <= 2e-3
@@ -76,6 +81,7 @@ SMALL = [
     (300, 256, 513, 0.0, False, 0.02),
     (257, 520, 2309, 0.1, True, 0.1),
     (1000, 512, 4099, 0.0, True, 0.0),
+    (333, 128, 3000, 0.1, 2, 0.1),     # reduction='sum'
 ]
 
 
@@ -85,7 +91,7 @@ def test_small_shapes_full(n, h, v, eps, red, ign):
     x = wk.normal_matrix(seed, wk.TID_X, n, h, 1.0, True)
     w = wk.normal_matrix(seed, wk.TID_W, v, h, h ** -0.5, True)
     y = wk.uniform_targets(seed, n, v, ign)
-    g = np.ones(1, np.float32) if red else wk.grad_rows(seed, n)
+    g = np.full(1, 0.75, np.float32) if red else wk.grad_rows(seed, n)
     check_full(x, w, y, eps, red, g)
 
 
@@ -145,17 +151,21 @@ def test_small_linear_workload_full():
 
 # the benchmark's launch configurations: the headline in one vocabulary slab, the
 # large workload with its dZ slab capped at 1 GiB (4 slabs, FP32 dX accumulation)
-@pytest.mark.parametrize("wl,slab_cap", [(wk.LINEAR_HEADLINE, 0), (wk.LINEAR_LARGE, 1 << 30)],
-                         ids=["headline", "large_slab1GiB"])
-def test_full_size_sampled(wl, slab_cap):
+@pytest.mark.parametrize("wl,slab_cap,entropy", [(wk.LINEAR_HEADLINE, 0, False),
+                                                 (wk.LINEAR_LARGE, 1 << 30, True)],
+                         ids=["headline", "large_slab1GiB_entropy"])
+def test_full_size_sampled(wl, slab_cap, entropy):
     inp = wk.make_linear_inputs(wl)
-    f, b = run(inp.x, inp.w, inp.target, wl.label_smoothing, wl.reduce_loss, inp.grad, slab_cap)
+    f, b = run(inp.x, inp.w, inp.target, wl.label_smoothing, wl.reduce_loss, inp.grad, slab_cap, entropy)
     assert int(f.dev_status.item()) == 0 and int(b.dev_status.item()) == 0
     n_valid = int((inp.target != -100).sum())
     assert int(f.n_valid.item()) == n_valid
-    lse_all, loss_all = oracle.lce_lse_all(inp.x, inp.w, inp.target, wl.label_smoothing)
+    lse_all, loss_all, ent_all = oracle.lce_lse_all(inp.x, inp.w, inp.target, wl.label_smoothing,
+                                                    entropy=entropy)
     lse_gpu = f.lse.double().cpu().numpy()
     assert np.max(np.abs(lse_gpu - lse_all)) <= 2e-3
+    if entropy:
+        assert np.max(np.abs(f.entropy.double().cpu().numpy() - ent_all)) <= 2e-3
     assert abs(f.loss.item() - oracle.mean_loss(loss_all, n_valid)) <= 2e-3
     g_all = oracle.upstream(inp.grad, wl.n, n_valid, wl.reduce_loss)
     rng = np.random.default_rng(0)

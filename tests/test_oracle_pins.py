@@ -343,7 +343,7 @@ def test_sampled_forms_agree_with_full_forms():
     lse_r, loss_r = oracle.lce_forward_rows(x[rows], w, y[rows], eps)
     np.testing.assert_allclose(lse_r, f["lse"][rows], rtol=1e-14)
     np.testing.assert_allclose(loss_r, f["loss_rows"][rows], rtol=1e-13, atol=1e-15)
-    lse_all, loss_all = oracle.lce_lse_all(x, w, y, eps, rows_per_chunk=7)
+    lse_all, loss_all, _ = oracle.lce_lse_all(x, w, y, eps, rows_per_chunk=7)
     np.testing.assert_allclose(lse_all, f["lse"], rtol=1e-14)
     np.testing.assert_allclose(loss_all, f["loss_rows"], rtol=1e-13, atol=1e-15)
     np.testing.assert_allclose(oracle.lce_dx_rows(x[rows], w, y[rows], f["lse"][rows], g[rows], eps),
@@ -351,3 +351,56 @@ def test_sampled_forms_agree_with_full_forms():
     vids = np.array([0, 5, 299])
     np.testing.assert_allclose(oracle.lce_dw_rows(x, w, vids, y, f["lse"], g, eps),
                                dw[vids], rtol=1e-12, atol=1e-15)
+
+
+# ---------------------------------------------------------------------------
+# reduction='sum' and the per-token entropy
+# ---------------------------------------------------------------------------
+
+def test_sum_reduction_and_its_gradient():
+    torch = pytest.importorskip("torch")
+    import torch.nn.functional as F
+    n, vocab = 23, 57
+    z = rng.standard_normal((n, vocab)) * 2
+    y = rng.integers(0, vocab, n)
+    y[::5] = -100
+    for eps in (0.0, 0.1):
+        out = oracle.ce_forward(z, y, eps, 2)
+        zt = torch.tensor(z, requires_grad=True)
+        ref = F.cross_entropy(zt, torch.tensor(y), ignore_index=-100, label_smoothing=eps, reduction="sum")
+        assert abs(out["loss"] - ref.item()) <= 1e-12 * abs(ref.item())
+        ref.backward(torch.tensor(0.7, dtype=torch.float64))
+        dz = oracle.ce_backward(z, y, out["lse"], out["n_valid"], [0.7], eps, 2)
+        np.testing.assert_allclose(dz, zt.grad.numpy(), rtol=1e-11, atol=1e-15)
+
+
+@pytest.mark.parametrize("vocab", [1, 2, 13, 1000])
+def test_entropy_closed_forms(vocab):
+    # uniform logits: H = log V; one dominant logit: H -> 0
+    z = np.full((3, vocab), 1.5)
+    _, lse = oracle.row_stats(z)
+    np.testing.assert_allclose(oracle.row_entropy(z, lse), math.log(vocab), atol=1e-13)
+    z2 = np.zeros((1, vocab))
+    z2[0, 0] = 60.0
+    _, lse2 = oracle.row_stats(z2)
+    assert abs(oracle.row_entropy(z2, lse2)[0]) < 1e-20 * vocab + 1e-22 or vocab == 1
+
+
+def test_entropy_matches_scipy():
+    from scipy.stats import entropy
+    from scipy.special import softmax
+    z = rng.standard_normal((9, 77)) * 3
+    _, lse = oracle.row_stats(z)
+    expect = entropy(softmax(z, axis=1), axis=1)
+    np.testing.assert_allclose(oracle.row_entropy(z, lse), expect, rtol=1e-12)
+
+
+def test_linear_forward_entropy_equals_logits_entropy():
+    x = rng.standard_normal((5, 12))
+    w = rng.standard_normal((31, 12))
+    out = oracle.lce_forward(x, w, np.zeros(5, np.int64), 0.0, False)
+    z = oracle.lce_logits(x, w)
+    _, lse = oracle.row_stats(z)
+    np.testing.assert_allclose(out["entropy"], oracle.row_entropy(z, lse), rtol=1e-13)
+    _, _, ent = oracle.lce_lse_all(x, w, np.zeros(5, np.int64), entropy=True, rows_per_chunk=2)
+    np.testing.assert_allclose(ent, out["entropy"], rtol=1e-13)

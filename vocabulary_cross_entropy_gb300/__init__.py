@@ -14,6 +14,9 @@ from ._binding import (  # noqa: F401
     F32,
     DEVSTATUS_BAD_TARGET,
     DEVSTATUS_TIMEOUT,
+    REDUCE_NONE,
+    REDUCE_MEAN,
+    REDUCE_SUM,
     library,
     library_path,
     vce_status_string,

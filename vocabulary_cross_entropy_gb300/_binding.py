@@ -14,6 +14,7 @@ BF16 = 0
 F32 = 1
 DEVSTATUS_BAD_TARGET = 1
 DEVSTATUS_TIMEOUT = 2
+REDUCE_NONE, REDUCE_MEAN, REDUCE_SUM = 0, 1, 2
 
 _c_i64 = ctypes.c_int64
 _c_int = ctypes.c_int
@@ -60,7 +61,7 @@ def library() -> ctypes.CDLL:
     lib.lce_workspace_size.argtypes = [_c_i64, _c_i64, _c_i64, _c_int, _c_size]
     lib.lce_workspace_size.restype = _c_size
     lib.lce_forward.argtypes = [_c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_f32, _c_int, _c_i64,
-                                _c_p, _c_p, _c_p, _c_p, _c_size, _c_p, _c_p]
+                                _c_p, _c_p, _c_p, _c_p, _c_p, _c_size, _c_p, _c_p]
     lib.lce_forward.restype = _c_int
     lib.lce_backward.argtypes = [_c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_p, _c_p, _c_p, _c_f32,
                                  _c_int, _c_i64, _c_p, _c_p, _c_p, _c_size, _c_p, _c_p]
@@ -116,6 +117,16 @@ def _rows_view(logits: torch.Tensor):
     return flat.shape[0], vocab, flat.stride(0) if flat.shape[0] > 1 else vocab
 
 
+def _reduce(reduce_loss) -> int:
+    """reduce_loss as the ABI code: False/0/'none', True/1/'mean', 2/'sum'."""
+    if isinstance(reduce_loss, str):
+        codes = {"none": REDUCE_NONE, "mean": REDUCE_MEAN, "sum": REDUCE_SUM}
+        if reduce_loss not in codes:
+            raise ValueError(f"reduce_loss must be one of {sorted(codes)}")
+        return codes[reduce_loss]
+    return int(reduce_loss)
+
+
 def _target(target: torch.Tensor, n: int):
     if target.dtype != torch.int64 or not target.is_contiguous() or target.numel() != n:
         raise ValueError("target must be a contiguous int64 tensor with one entry per row")
@@ -123,12 +134,12 @@ def _target(target: torch.Tensor, n: int):
 
 
 CEForward = namedtuple("CEForward", "loss stats n_valid dev_status")
-LCEForward = namedtuple("LCEForward", "loss lse n_valid dev_status")
+LCEForward = namedtuple("LCEForward", "loss lse n_valid dev_status entropy")
 LCEBackward = namedtuple("LCEBackward", "dX dW dev_status")
 
 
 def ce_workspace_size(n_rows: int, vocab: int, reduce_loss: bool) -> int:
-    return int(library().ce_workspace_size(n_rows, vocab, int(bool(reduce_loss))))
+    return int(library().ce_workspace_size(n_rows, vocab, _reduce(reduce_loss)))
 
 
 def ce_forward(logits, target, label_smoothing=0.0, reduce_loss=False, ignore_idx=-100, *,
@@ -139,7 +150,7 @@ def ce_forward(logits, target, label_smoothing=0.0, reduce_loss=False, ignore_id
     n, vocab, stride = _rows_view(logits)
     target = _target(target, n)
     if loss is None:
-        loss = torch.empty(1 if reduce_loss else n, dtype=torch.float32, device=dev)
+        loss = torch.empty(1 if _reduce(reduce_loss) else n, dtype=torch.float32, device=dev)
     if stats is None:
         stats = torch.empty(n, 2, dtype=torch.float32, device=dev)
     if n_valid is None:
@@ -151,12 +162,12 @@ def ce_forward(logits, target, label_smoothing=0.0, reduce_loss=False, ignore_id
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     with torch.cuda.device(dev):
         st = lib.ce_forward(_ptr(logits), _dtype_code(logits), n, vocab, stride, _ptr(target),
-                            float(label_smoothing), int(bool(reduce_loss)), int(ignore_idx),
+                            float(label_smoothing), _reduce(reduce_loss), int(ignore_idx),
                             _ptr(loss), _ptr(stats), _ptr(n_valid), _ptr(workspace),
                             0 if workspace is None else workspace.numel() * workspace.element_size(),
                             _ptr(dev_status), _stream(dev, stream))
     _check("ce_forward", st)
-    return CEForward(loss if reduce_loss else loss.view(logits.shape[:-1]), stats, n_valid, dev_status)
+    return CEForward(loss if _reduce(reduce_loss) else loss.view(logits.shape[:-1]), stats, n_valid, dev_status)
 
 
 def ce_forward_noalloc(logits, target, label_smoothing=0.0, reduce_loss=False, ignore_idx=-100, *,
@@ -169,7 +180,7 @@ def ce_forward_noalloc(logits, target, label_smoothing=0.0, reduce_loss=False, i
     n, vocab, stride = _rows_view(logits)
     target = _target(target, n)
     if loss is None:
-        loss = torch.empty(1 if reduce_loss else n, dtype=torch.float32, device=dev)
+        loss = torch.empty(1 if _reduce(reduce_loss) else n, dtype=torch.float32, device=dev)
     if stats is None:
         stats = torch.empty(n, 2, dtype=torch.float32, device=dev)
     if n_valid is None:
@@ -178,11 +189,11 @@ def ce_forward_noalloc(logits, target, label_smoothing=0.0, reduce_loss=False, i
         dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
     with torch.cuda.device(dev):
         st = lib.ce_forward_noalloc(_ptr(logits), _dtype_code(logits), n, vocab, stride, _ptr(target),
-                                    float(label_smoothing), int(bool(reduce_loss)), int(ignore_idx),
+                                    float(label_smoothing), _reduce(reduce_loss), int(ignore_idx),
                                     _ptr(loss), _ptr(stats), _ptr(n_valid), _ptr(dev_status),
                                     _stream(dev, stream))
     _check("ce_forward_noalloc", st)
-    return CEForward(loss if reduce_loss else loss.view(logits.shape[:-1]), stats, n_valid, dev_status)
+    return CEForward(loss if _reduce(reduce_loss) else loss.view(logits.shape[:-1]), stats, n_valid, dev_status)
 
 
 def ce_backward(logits, target, stats, n_valid, grad_output, label_smoothing=0.0, reduce_loss=False,
@@ -204,7 +215,7 @@ def ce_backward(logits, target, stats, n_valid, grad_output, label_smoothing=0.0
     with torch.cuda.device(dev):
         st = lib.ce_backward(_ptr(logits), _dtype_code(logits), n, vocab, stride, _ptr(target),
                              _ptr(stats), _ptr(n_valid), _ptr(grad_output), float(label_smoothing),
-                             int(bool(reduce_loss)), int(ignore_idx), _ptr(dlogits),
+                             _reduce(reduce_loss), int(ignore_idx), _ptr(dlogits),
                              _ptr(dev_status), _stream(dev, stream))
     _check("ce_backward", st)
     return dlogits
@@ -230,7 +241,7 @@ def ce_forward_backward(logits, target, grad_output, label_smoothing=0.0, reduce
         raise ValueError("dlogits must have the dtype and strides of logits")
     grad_output = grad_output.to(device=dev, dtype=torch.float32).contiguous()
     if loss is None:
-        loss = torch.empty(1 if reduce_loss else n, dtype=torch.float32, device=dev)
+        loss = torch.empty(1 if _reduce(reduce_loss) else n, dtype=torch.float32, device=dev)
     if stats is None:
         stats = torch.empty(n, 2, dtype=torch.float32, device=dev)
     if n_valid is None:
@@ -242,13 +253,13 @@ def ce_forward_backward(logits, target, grad_output, label_smoothing=0.0, reduce
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     with torch.cuda.device(dev):
         st = lib.ce_forward_backward(_ptr(logits), _dtype_code(logits), n, vocab, stride, _ptr(target),
-                                     float(label_smoothing), int(bool(reduce_loss)), int(ignore_idx),
+                                     float(label_smoothing), _reduce(reduce_loss), int(ignore_idx),
                                      _ptr(grad_output), _ptr(loss), _ptr(stats), _ptr(n_valid),
                                      _ptr(dlogits), _ptr(workspace),
                                      0 if workspace is None else workspace.numel(),
                                      _ptr(dev_status), _stream(dev, stream))
     _check("ce_forward_backward", st)
-    return CEForwardBackward(loss if reduce_loss else loss.view(logits.shape[:-1]), stats, n_valid,
+    return CEForwardBackward(loss if _reduce(reduce_loss) else loss.view(logits.shape[:-1]), stats, n_valid,
                              dlogits, dev_status)
 
 
@@ -259,13 +270,15 @@ def _bf16_2d(t, name):
 
 
 def lce_workspace_size(n: int, h: int, v: int, reduce_loss: bool, max_slab_bytes: int = 0) -> int:
-    return int(library().lce_workspace_size(n, h, v, int(bool(reduce_loss)), int(max_slab_bytes)))
+    return int(library().lce_workspace_size(n, h, v, _reduce(reduce_loss), int(max_slab_bytes)))
 
 
 def lce_forward(X, W, target, label_smoothing=0.0, reduce_loss=False, ignore_idx=-100, *,
-                loss=None, lse=None, n_valid=None, workspace=None, max_slab_bytes=0, dev_status=None,
-                stream=None):
-    """Linear-form forward.  Returns (loss, lse [N], n_valid, dev_status).
+                loss=None, lse=None, n_valid=None, entropy=None, workspace=None, max_slab_bytes=0,
+                dev_status=None, stream=None):
+    """Linear-form forward.  Returns (loss, lse [N], n_valid, dev_status, entropy).
+
+    ``entropy``: None (not computed), True (allocate [N] FP32) or an [N] FP32 tensor.
 
     A workspace not passed in is allocated with lce_workspace_size(..., max_slab_bytes), the
     size one workspace shared by lce_forward and lce_backward needs."""
@@ -279,23 +292,27 @@ def lce_forward(X, W, target, label_smoothing=0.0, reduce_loss=False, ignore_idx
     dev = X.device
     target = _target(target, n)
     if loss is None:
-        loss = torch.empty(1 if reduce_loss else n, dtype=torch.float32, device=dev)
+        loss = torch.empty(1 if _reduce(reduce_loss) else n, dtype=torch.float32, device=dev)
     if lse is None:
         lse = torch.empty(n, dtype=torch.float32, device=dev)
     if n_valid is None:
         n_valid = torch.empty(1, dtype=torch.int64, device=dev)
     if dev_status is None:
         dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
+    if entropy is True:
+        entropy = torch.empty(n, dtype=torch.float32, device=dev)
+    elif entropy is False:
+        entropy = None
     if workspace is None:
         workspace = torch.empty(max(1, lce_workspace_size(n, h, v, reduce_loss, max_slab_bytes)),
                                 dtype=torch.uint8, device=dev)
     with torch.cuda.device(dev):
         st = lib.lce_forward(_ptr(X), _ptr(W), n, h, v, _ptr(target), float(label_smoothing),
-                             int(bool(reduce_loss)), int(ignore_idx), _ptr(loss), _ptr(lse),
+                             _reduce(reduce_loss), int(ignore_idx), _ptr(loss), _ptr(lse), _ptr(entropy),
                              _ptr(n_valid), _ptr(workspace), workspace.numel(), _ptr(dev_status),
                              _stream(dev, stream))
     _check("lce_forward", st)
-    return LCEForward(loss, lse, n_valid, dev_status)
+    return LCEForward(loss, lse, n_valid, dev_status, entropy)
 
 
 def lce_backward(X, W, target, lse, n_valid, grad_output, label_smoothing=0.0, reduce_loss=False,
@@ -321,7 +338,7 @@ def lce_backward(X, W, target, lse, n_valid, grad_output, label_smoothing=0.0, r
                                 dtype=torch.uint8, device=dev)
     with torch.cuda.device(dev):
         st = lib.lce_backward(_ptr(X), _ptr(W), n, h, v, _ptr(target), _ptr(lse), _ptr(n_valid),
-                              _ptr(grad_output), float(label_smoothing), int(bool(reduce_loss)),
+                              _ptr(grad_output), float(label_smoothing), _reduce(reduce_loss),
                               int(ignore_idx), _ptr(dX), _ptr(dW), _ptr(workspace), workspace.numel(),
                               _ptr(dev_status), _stream(dev, stream))
     _check("lce_backward", st)

@@ -245,7 +245,7 @@ ce_backward_rows(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride,
             for (int64_t j = sp.tail0 + threadIdx.x; j < vocab; j += THREADS) E::store1(q + j, 0.f);
             continue;
         }
-        const float g = reduce_loss ? grad_output[0] / float(n_valid[0]) : grad_output[row];
+        const float g = upstream_grad(reduce_loss, grad_output, n_valid, row);
         const float negl = -stats[row].y * kLog2e;
         const float b = g * eps / float(vocab);   // eps / V share of every class
         const float c = g * (1.f - eps);          // target class
@@ -292,7 +292,7 @@ constexpr int kMeanThreads = 1024;
 
 __global__ void __launch_bounds__(kMeanThreads)
 mean_loss_kernel(const float* __restrict__ loss_rows, const int64_t* __restrict__ target,
-                 int64_t n, int64_t ignore_idx, float* __restrict__ loss_out,
+                 int64_t n, int64_t ignore_idx, int reduce, float* __restrict__ loss_out,
                  int64_t* __restrict__ n_valid) {
     __shared__ double sm_s[32];
     __shared__ long long sm_c[32];
@@ -319,7 +319,8 @@ mean_loss_kernel(const float* __restrict__ loss_rows, const int64_t* __restrict_
             c += __shfl_xor_sync(0xffffffffu, c, off);
         }
         if (lane == 0) {
-            if (loss_out) loss_out[0] = float(s / double(c));  // 0/0 = NaN when every row is ignored
+            // mean: 0/0 = NaN when every row is ignored; sum: the plain total
+            if (loss_out) loss_out[0] = reduce == VCE_REDUCE_SUM ? float(s) : float(s / double(c));
             if (n_valid) n_valid[0] = c;
         }
     }
@@ -473,7 +474,7 @@ ce_fused_rows(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
             __syncthreads();
             continue;
         }
-        const float g = reduce_loss ? grad_output[0] / float(n_valid[0]) : grad_output[row];
+        const float g = upstream_grad(reduce_loss, grad_output, n_valid, row);
         const float negl = -sm_lse * kLog2e;
         const float b = g * eps / float(vocab);
         const float c = g * (1.f - eps);
@@ -557,8 +558,8 @@ int row_grid(int64_t n_rows) {
 }  // namespace
 
 vce_status launch_mean_loss(const float* loss_rows, const int64_t* target, int64_t n_rows,
-                            int64_t ignore_idx, float* loss_out, int64_t* n_valid, cudaStream_t s) {
-    mean_loss_kernel<<<1, kMeanThreads, 0, s>>>(loss_rows, target, n_rows, ignore_idx, loss_out, n_valid);
+                            int64_t ignore_idx, int reduce, float* loss_out, int64_t* n_valid, cudaStream_t s) {
+    mean_loss_kernel<<<1, kMeanThreads, 0, s>>>(loss_rows, target, n_rows, ignore_idx, reduce, loss_out, n_valid);
     return cudaGetLastError() == cudaSuccess ? VCE_OK : VCE_ERR_CUDA;
 }
 
@@ -579,7 +580,7 @@ vce_status launch_ce_forward(const void* logits, int dtype, int64_t n_rows, int6
         if (cudaGetLastError() != cudaSuccess) return VCE_ERR_CUDA;
     }
     if (reduce_loss || n_valid)
-        return launch_mean_loss(reduce_loss ? loss_rows : nullptr, target, n_rows, ignore_idx,
+        return launch_mean_loss(reduce_loss ? loss_rows : nullptr, target, n_rows, ignore_idx, reduce_loss,
                                 reduce_loss ? loss : nullptr, n_valid, s);
     return VCE_OK;
 }
@@ -608,8 +609,8 @@ vce_status launch_ce_forward_backward(const void* logits, int dtype, int64_t n_r
     float* loss_rows = reduce_loss ? static_cast<float*>(ws) : loss;
     if (n_rows > 0) {
         // N_v first: the mean's upstream gradient g / N_v is needed inside the row pass
-        if (reduce_loss)
-            if (vce_status st = launch_mean_loss(nullptr, target, n_rows, ignore_idx, nullptr, n_valid, s))
+        if (reduce_loss == VCE_REDUCE_MEAN)
+            if (vce_status st = launch_mean_loss(nullptr, target, n_rows, ignore_idx, reduce_loss, nullptr, n_valid, s))
                 return st;
         if (dtype == VCE_BF16)
             fused_dispatch<__nv_bfloat16>(logits, n_rows, vocab, row_stride, target, eps, ignore_idx, n_valid,
@@ -621,7 +622,7 @@ vce_status launch_ce_forward_backward(const void* logits, int dtype, int64_t n_r
         if (cudaGetLastError() != cudaSuccess) return VCE_ERR_CUDA;
     }
     if (reduce_loss || n_valid)
-        return launch_mean_loss(reduce_loss ? loss_rows : nullptr, target, n_rows, ignore_idx,
+        return launch_mean_loss(reduce_loss ? loss_rows : nullptr, target, n_rows, ignore_idx, reduce_loss,
                                 reduce_loss ? loss : nullptr, n_valid, s);
     return VCE_OK;
 }

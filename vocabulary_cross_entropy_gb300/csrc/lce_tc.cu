@@ -121,6 +121,7 @@ struct FwdEpi {
     int64_t V;       // vocabulary
     float2* part_ms; // [tiles_n][M] (max, sum exp(z - max))
     float* part_sum; // [tiles_n][M] sum of z (label smoothing), may be unused
+    float* part_t;   // [tiles_n][M] sum of exp(z - max) z (entropy), NULL when not requested
     float* zy;       // [M] target logit
     int smooth;
 
@@ -130,8 +131,9 @@ struct FwdEpi {
         const bool row_ok = gm < M;
         const int64_t y = row_ok ? target[gm] : -1;
         const int64_t gn0 = int64_t(tn) * BN;
-        float m = -INFINITY, negm = 0.f, s = 0.f, sum = 0.f, zyv = 0.f;
+        float m = -INFINITY, negm = 0.f, s = 0.f, sum = 0.f, te = 0.f, zyv = 0.f;
         bool hit = false;
+        const bool want_t = part_t != nullptr;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
             uint32_t r[32];
@@ -163,18 +165,32 @@ struct FwdEpi {
 #pragma unroll
             for (int j = 1; j < 32; ++j) vm = fmaxf(vm, v[j]);
             if (vm > m) {
-                s = s * ex2f((m - vm) * kLog2e);
+                const float sc = ex2f((m - vm) * kLog2e);
+                s *= sc;
+                te *= sc;
                 m = vm;
                 negm = -vm * kLog2e;
             }
-            float t = 0.f;
+            float t = 0.f, tz = 0.f;
+            if (want_t) {
+                // columns past V have e = 0 and an (in-range, zero-filled) raw logit of 0
 #pragma unroll
-            for (int j = 0; j < 32; ++j) t += ex2f(fmaf(v[j], kLog2e, negm));
+                for (int j = 0; j < 32; ++j) {
+                    const float e = ex2f(fmaf(v[j], kLog2e, negm));
+                    t += e;
+                    tz = fmaf(e, __uint_as_float(r[j]), tz);
+                }
+                te += tz;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) t += ex2f(fmaf(v[j], kLog2e, negm));
+            }
             s += t;
         }
         if (row_ok) {
             part_ms[int64_t(tn) * M + gm] = make_float2(m, s);
             if (smooth) part_sum[int64_t(tn) * M + gm] = sum;
+            if (want_t) part_t[int64_t(tn) * M + gm] = te;
             if (hit) zy[gm] = zyv;
         }
     }
@@ -205,7 +221,7 @@ struct DzEpi {
             if (bad && tn == 0 && slab0 == 0) report(dev_status, VCE_DEVSTATUS_BAD_TARGET);
             live = !ign && !bad;
             if (live) {
-                g = reduce ? grad[0] / float(n_valid[0]) : grad[gm];
+                g = upstream_grad(reduce, grad, n_valid, gm);
                 negl = -lse[gm] * kLog2e;
             }
         }
@@ -481,40 +497,48 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 constexpr int kCombRows = 32;   // consecutive rows per CTA (coalesced partial reads)
 constexpr int kCombSplit = 8;   // partial-index splits per row, merged in a fixed order
 
-__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
+// merge (m2, s2, t2) into (m, s, t): s = sum exp(z - m), t = sum exp(z - m) z
+__device__ __forceinline__ void lse_merge(float& m, float& s, float& t, float m2, float s2, float t2) {
     const float mn = fmaxf(m, m2);
     if (mn == -INFINITY) return;
-    s = s * ex2f((m - mn) * kLog2e) + s2 * ex2f((m2 - mn) * kLog2e);
+    const float a = ex2f((m - mn) * kLog2e), b = ex2f((m2 - mn) * kLog2e);
+    s = s * a + s2 * b;
+    t = t * a + t2 * b;
     m = mn;
 }
 
 __global__ void __launch_bounds__(kCombRows * kCombSplit)
 lce_combine_kernel(const float2* __restrict__ part_ms, const float* __restrict__ part_sum,
-                   const float* __restrict__ zy, const int64_t* __restrict__ target, int64_t n, int64_t v,
-                   int nb, float eps, int64_t ignore_idx, float* __restrict__ lse_out,
-                   float* __restrict__ loss_out, int* dev_status) {
-    __shared__ float sm_m[kCombSplit][kCombRows], sm_s[kCombSplit][kCombRows], sm_u[kCombSplit][kCombRows];
+                   const float* __restrict__ part_t, const float* __restrict__ zy,
+                   const int64_t* __restrict__ target, int64_t n, int64_t v, int nb, float eps,
+                   int64_t ignore_idx, float* __restrict__ lse_out, float* __restrict__ loss_out,
+                   float* __restrict__ entropy_out, int* dev_status) {
+    __shared__ float sm_m[kCombSplit][kCombRows], sm_s[kCombSplit][kCombRows], sm_u[kCombSplit][kCombRows],
+        sm_t[kCombSplit][kCombRows];
     const int lr = threadIdx.x % kCombRows, sp = threadIdx.x / kCombRows;
     const int64_t row = int64_t(blockIdx.x) * kCombRows + lr;
-    float m = -INFINITY, s = 0.f, u = 0.f;
+    const bool want_t = entropy_out != nullptr;
+    float m = -INFINITY, s = 0.f, u = 0.f, t = 0.f;
     if (row < n) {
         for (int b = sp; b < nb; b += kCombSplit) {
             const float2 p = part_ms[int64_t(b) * n + row];
-            lse_merge(m, s, p.x, p.y);
+            lse_merge(m, s, t, p.x, p.y, want_t ? part_t[int64_t(b) * n + row] : 0.f);
             if (eps != 0.f) u += part_sum[int64_t(b) * n + row];
         }
     }
     sm_m[sp][lr] = m;
     sm_s[sp][lr] = s;
     sm_u[sp][lr] = u;
+    sm_t[sp][lr] = t;
     __syncthreads();
     if (sp != 0 || row >= n) return;
     for (int k = 1; k < kCombSplit; ++k) {
-        lse_merge(m, s, sm_m[k][lr], sm_s[k][lr]);
+        lse_merge(m, s, t, sm_m[k][lr], sm_s[k][lr], sm_t[k][lr]);
         u += sm_u[k][lr];
     }
     const float lse = m + logf(s);
     lse_out[row] = lse;
+    if (want_t) entropy_out[row] = lse - t / s;  // H = lse - sum_v p_v z_v
     const int64_t y = target[row];
     float loss;
     if (y == ignore_idx) {
@@ -637,6 +661,7 @@ __global__ void dx_finalize_kernel(const float* __restrict__ acc, int splits, in
 struct FwdWs {
     float2* part_ms;
     float* part_sum;
+    float* part_t;
     float* zy;
     float* loss_rows;
     size_t bytes;
@@ -650,6 +675,8 @@ FwdWs carve_forward(void* ws, int64_t n, int64_t v, int reduce_loss) {
     w.part_ms = reinterpret_cast<float2*>(base + off);
     off += align256(size_t(nb) * size_t(n) * 8);
     w.part_sum = reinterpret_cast<float*>(base + off);
+    off += align256(size_t(nb) * size_t(n) * 4);
+    w.part_t = reinterpret_cast<float*>(base + off);
     off += align256(size_t(nb) * size_t(n) * 4);
     w.zy = reinterpret_cast<float*>(base + off);
     off += align256(size_t(n) * 4);
@@ -716,26 +743,28 @@ int64_t lce_slab_for_ws(int64_t n, int64_t h, int64_t v, size_t ws_bytes) {
 
 vce_status launch_lce_forward(const void* X, const void* W, int64_t n, int64_t h, int64_t v,
                               const int64_t* target, float eps, int reduce_loss, int64_t ignore_idx,
-                              float* loss, float* lse, int64_t* n_valid, void* ws, int* dev_status,
-                              cudaStream_t s, const DeviceInfo& dev) {
+                              float* loss, float* lse, float* entropy, int64_t* n_valid, void* ws,
+                              int* dev_status, cudaStream_t s, const DeviceInfo& dev) {
     if (n == 0) {
         if (reduce_loss || n_valid)
-            return launch_mean_loss(nullptr, target, 0, ignore_idx, reduce_loss ? loss : nullptr, n_valid, s);
+            return launch_mean_loss(nullptr, target, 0, ignore_idx, reduce_loss, reduce_loss ? loss : nullptr,
+                                    n_valid, s);
         return VCE_OK;
     }
     const FwdWs w = carve_forward(ws, n, v, reduce_loss);
     CUtensorMap tx, tw;
     if (!map_kmajor(&tx, X, h, n, h, BM_CTA) || !map_kmajor(&tw, W, h, v, h, kVocabTile / 2)) return VCE_ERR_CUDA;
-    FwdEpi epi{target, n, v, w.part_ms, w.part_sum, w.zy, eps != 0.f ? 1 : 0};
+    FwdEpi epi{target, n, v, w.part_ms, w.part_sum, entropy ? w.part_t : nullptr, w.zy, eps != 0.f ? 1 : 0};
     if (vce_status st = launch_gemm<FwdEpi, false, false, kVocabTile>(tx, tw, n, v, h, 1, 1, epi, dev_status, s, dev))
         return st;
     const int nb = int((v + kVocabTile - 1) / kVocabTile);
     float* loss_rows = reduce_loss ? w.loss_rows : loss;
     lce_combine_kernel<<<int((n + kCombRows - 1) / kCombRows), kCombRows * kCombSplit, 0, s>>>(
-        w.part_ms, w.part_sum, w.zy, target, n, v, nb, eps, ignore_idx, lse, loss_rows, dev_status);
+        w.part_ms, w.part_sum, w.part_t, w.zy, target, n, v, nb, eps, ignore_idx, lse, loss_rows, entropy,
+        dev_status);
     if (cudaGetLastError() != cudaSuccess) return VCE_ERR_CUDA;
     if (reduce_loss || n_valid)
-        return launch_mean_loss(reduce_loss ? loss_rows : nullptr, target, n, ignore_idx,
+        return launch_mean_loss(reduce_loss ? loss_rows : nullptr, target, n, ignore_idx, reduce_loss,
                                 reduce_loss ? loss : nullptr, n_valid, s);
     return VCE_OK;
 }

@@ -44,6 +44,8 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 bool eps_ok(float eps) { return eps >= 0.f && eps <= 1.f; }  // false for NaN too
 
+bool reduce_ok(int r) { return r == VCE_REDUCE_NONE || r == VCE_REDUCE_MEAN || r == VCE_REDUCE_SUM; }
+
 size_t elem_size(int dtype) { return dtype == VCE_BF16 ? 2 : 4; }
 
 }  // namespace
@@ -77,10 +79,10 @@ vce_status ce_forward(const void* logits, int dtype, int64_t n_rows, int64_t voc
                       int64_t* n_valid, void* ws, size_t ws_bytes, int* dev_status,
                       void* stream) {
     if (dtype != VCE_BF16 && dtype != VCE_F32) return VCE_ERR_DTYPE;
-    if (n_rows < 0 || vocab < 1 || row_stride < vocab || !eps_ok(label_smoothing))
+    if (n_rows < 0 || vocab < 1 || row_stride < vocab || !eps_ok(label_smoothing) || !reduce_ok(reduce_loss))
         return VCE_ERR_INVALID_ARG;
     if (!loss || (n_rows > 0 && (!logits || !target || !stats))) return VCE_ERR_INVALID_ARG;
-    if (reduce_loss && !n_valid) return VCE_ERR_INVALID_ARG;
+    if (reduce_loss == VCE_REDUCE_MEAN && !n_valid) return VCE_ERR_INVALID_ARG;
     if (!aligned(logits, elem_size(dtype)) || !aligned(stats, 8)) return VCE_ERR_ALIGN;
     const size_t need = ce_workspace_size(n_rows, vocab, reduce_loss);
     if (need > 0 && (!ws || ws_bytes < need)) return VCE_ERR_WORKSPACE;
@@ -98,11 +100,11 @@ vce_status ce_backward(const void* logits, int dtype, int64_t n_rows, int64_t vo
                        float label_smoothing, int reduce_loss, int64_t ignore_idx,
                        void* dlogits, int* dev_status, void* stream) {
     if (dtype != VCE_BF16 && dtype != VCE_F32) return VCE_ERR_DTYPE;
-    if (n_rows < 0 || vocab < 1 || row_stride < vocab || !eps_ok(label_smoothing))
+    if (n_rows < 0 || vocab < 1 || row_stride < vocab || !eps_ok(label_smoothing) || !reduce_ok(reduce_loss))
         return VCE_ERR_INVALID_ARG;
     if (n_rows > 0 && (!logits || !target || !stats || !grad_output || !dlogits))
         return VCE_ERR_INVALID_ARG;
-    if (n_rows > 0 && reduce_loss && !n_valid) return VCE_ERR_INVALID_ARG;
+    if (n_rows > 0 && reduce_loss == VCE_REDUCE_MEAN && !n_valid) return VCE_ERR_INVALID_ARG;
     const size_t es = elem_size(dtype);
     if (!aligned(logits, es) || !aligned(dlogits, es) || !aligned(stats, 8)) return VCE_ERR_ALIGN;
     // logits and dlogits rows must share their offset within 16 bytes (vector path)
@@ -121,11 +123,11 @@ vce_status ce_forward_backward(const void* logits, int dtype, int64_t n_rows, in
                                float* loss, float* stats, int64_t* n_valid, void* dlogits, void* ws,
                                size_t ws_bytes, int* dev_status, void* stream) {
     if (dtype != VCE_BF16 && dtype != VCE_F32) return VCE_ERR_DTYPE;
-    if (n_rows < 0 || vocab < 1 || row_stride < vocab || !eps_ok(label_smoothing))
+    if (n_rows < 0 || vocab < 1 || row_stride < vocab || !eps_ok(label_smoothing) || !reduce_ok(reduce_loss))
         return VCE_ERR_INVALID_ARG;
     if (!loss || (n_rows > 0 && (!logits || !target || !stats || !grad_output || !dlogits)))
         return VCE_ERR_INVALID_ARG;
-    if (reduce_loss && !n_valid) return VCE_ERR_INVALID_ARG;
+    if (reduce_loss == VCE_REDUCE_MEAN && !n_valid) return VCE_ERR_INVALID_ARG;
     const size_t es = elem_size(dtype);
     if (!aligned(logits, es) || !aligned(dlogits, es) || !aligned(stats, 8)) return VCE_ERR_ALIGN;
     if (((reinterpret_cast<uintptr_t>(logits) ^ reinterpret_cast<uintptr_t>(dlogits)) & 15) != 0)
@@ -155,11 +157,12 @@ size_t lce_workspace_size(int64_t n, int64_t h, int64_t v, int reduce_loss,
 
 vce_status lce_forward(const void* X, const void* W, int64_t n, int64_t h, int64_t v,
                        const int64_t* target, float label_smoothing, int reduce_loss,
-                       int64_t ignore_idx, float* loss, float* lse, int64_t* n_valid,
-                       void* ws, size_t ws_bytes, int* dev_status, void* stream) {
-    if (n < 0 || h < 1 || v < 1 || !eps_ok(label_smoothing)) return VCE_ERR_INVALID_ARG;
+                       int64_t ignore_idx, float* loss, float* lse, float* entropy,
+                       int64_t* n_valid, void* ws, size_t ws_bytes, int* dev_status,
+                       void* stream) {
+    if (n < 0 || h < 1 || v < 1 || !eps_ok(label_smoothing) || !reduce_ok(reduce_loss)) return VCE_ERR_INVALID_ARG;
     if (!loss || (n > 0 && (!X || !W || !target || !lse))) return VCE_ERR_INVALID_ARG;
-    if (reduce_loss && !n_valid) return VCE_ERR_INVALID_ARG;
+    if (reduce_loss == VCE_REDUCE_MEAN && !n_valid) return VCE_ERR_INVALID_ARG;
     if (h % 8 != 0 || !aligned(X, 16) || !aligned(W, 16)) return VCE_ERR_ALIGN;
     if (n > 0) {
         const size_t need = lce_forward_ws_bytes(n, v, reduce_loss);
@@ -169,7 +172,7 @@ vce_status lce_forward(const void* X, const void* W, int64_t n, int64_t h, int64
     DeviceInfo dev;
     if (vce_status st = current_device(dev)) return st;
     return launch_lce_forward(X, W, n, h, v, target, label_smoothing, reduce_loss, ignore_idx,
-                              loss, lse, n_valid, ws, dev_status,
+                              loss, lse, entropy, n_valid, ws, dev_status,
                               static_cast<cudaStream_t>(stream), dev);
 }
 
@@ -178,10 +181,10 @@ vce_status lce_backward(const void* X, const void* W, int64_t n, int64_t h, int6
                         const float* grad_output, float label_smoothing, int reduce_loss,
                         int64_t ignore_idx, void* dX, void* dW, void* ws, size_t ws_bytes,
                         int* dev_status, void* stream) {
-    if (n < 0 || h < 1 || v < 1 || !eps_ok(label_smoothing)) return VCE_ERR_INVALID_ARG;
+    if (n < 0 || h < 1 || v < 1 || !eps_ok(label_smoothing) || !reduce_ok(reduce_loss)) return VCE_ERR_INVALID_ARG;
     if (!dW || (n > 0 && (!X || !W || !target || !lse || !grad_output || !dX)))
         return VCE_ERR_INVALID_ARG;
-    if (n > 0 && reduce_loss && !n_valid) return VCE_ERR_INVALID_ARG;
+    if (n > 0 && reduce_loss == VCE_REDUCE_MEAN && !n_valid) return VCE_ERR_INVALID_ARG;
     if (h % 8 != 0 || !aligned(X, 16) || !aligned(W, 16) || !aligned(dX, 16) || !aligned(dW, 16))
         return VCE_ERR_ALIGN;
     int64_t slab = 0;

@@ -21,6 +21,15 @@ __device__ __forceinline__ float ex2f(float x) {
     return y;
 }
 
+// Upstream gradient of row ``row``: grad_output[row] (no reduction),
+// grad_output[0] / N_v (mean) or grad_output[0] (sum).
+__device__ __forceinline__ float upstream_grad(int reduce, const float* grad_output, const int64_t* n_valid,
+                                               int64_t row) {
+    if (reduce == VCE_REDUCE_MEAN) return grad_output[0] / float(n_valid[0]);
+    if (reduce == VCE_REDUCE_SUM) return grad_output[0];
+    return grad_output[row];
+}
+
 __device__ __forceinline__ void report(int* dev_status, int bits) {
     if (dev_status) atomicOr(dev_status, bits);
 }
@@ -58,7 +67,7 @@ vce_status launch_ce_forward_backward(const void* logits, int dtype, int64_t n_r
                                       cudaStream_t s, const DeviceInfo& dev);
 // mean of per-row losses over rows whose target is not ignore_idx, and the count
 vce_status launch_mean_loss(const float* loss_rows, const int64_t* target, int64_t n_rows,
-                            int64_t ignore_idx, float* loss_out, int64_t* n_valid,
+                            int64_t ignore_idx, int reduce, float* loss_out, int64_t* n_valid,
                             cudaStream_t s);
 
 // ---- linear form (lce_tc.cu) ----
@@ -67,7 +76,7 @@ int64_t lce_slab_for_ws(int64_t n, int64_t h, int64_t v, size_t ws_bytes);
 size_t lce_backward_ws_bytes(int64_t n, int64_t h, int64_t v, int64_t slab);
 vce_status launch_lce_forward(const void* X, const void* W, int64_t n, int64_t h, int64_t v,
                               const int64_t* target, float eps, int reduce_loss,
-                              int64_t ignore_idx, float* loss, float* lse, int64_t* n_valid,
+                              int64_t ignore_idx, float* loss, float* lse, float* entropy, int64_t* n_valid,
                               void* ws, int* dev_status, cudaStream_t s, const DeviceInfo& dev);
 vce_status launch_lce_backward(const void* X, const void* W, int64_t n, int64_t h, int64_t v,
                                const int64_t* target, const float* lse, const int64_t* n_valid,
