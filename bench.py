@@ -44,6 +44,10 @@ sys.path.insert(0, ROOT)
 import workloads as wk  # noqa: E402
 
 PUBLISHED_TP1_FB_TFLOPS = 1606.5  # Liger SM100 PR, M=4096 F+B, TP1, NVIDIA B300 (context)
+# Liger SM100 PR "Model-shape campaign", TP1 forward+backward ms on NVIDIA B300 (context)
+PUBLISHED_MODEL_SHAPES_FB_MS = {"qwen3_30b_a3b_8192x2048x151936": 13.692,
+                                "llama4_8192x5120x202048": 50.180,
+                                "deepseek_v3_8192x7168x129280": 43.588}
 
 
 def FWD_GEMM_TRAFFIC_BYTES(wl):
@@ -503,6 +507,8 @@ def main():
     ap.add_argument("--workload", default="both", choices=["linear", "logits", "both"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
+    ap.add_argument("--sweep", action="store_true",
+                    help="also time the model-shape sweep (Qwen3-30B-A3B, Llama 4, DeepSeek-V3 heads at M=8192)")
     ap.add_argument("--no-large", dest="large", action="store_false",
                     help="skip the 16384x4096x128256 workload (throughput and peak extra memory)")
     ap.add_argument("--shape", default=None,
@@ -646,6 +652,23 @@ def main():
             "clocks": ckb.summary(),
         }
         del big
+    if args.sweep and lin is wk.LINEAR_HEADLINE:
+        torch.cuda.empty_cache()
+        line["sweep"] = []
+        for shp in wk.MODEL_SHAPES:
+            stp = LinearStep(shp, dev)
+            ks = max(3, args.steps // 3)
+            with Clocks(local) as cks:
+                ts, phs = time_steps(stp, ks, args.warmup, pg)
+            assert int(stp.status.item()) == 0, "device status reported an error"
+            line["sweep"].append({
+                "workload": shp.name, "n": shp.n, "h": shp.hidden, "v": shp.vocab,
+                "value": stp.units() * world * ks / (ts / 1e3), "unit": "TFLOP/s", "ms_per_step": ts / ks,
+                "fwd_ms": phs["forward"], "bwd_ms": phs["backward"], "steps": ks,
+                "pages_tp1_fb_ms_b300": PUBLISHED_MODEL_SHAPES_FB_MS.get(shp.name),
+                "workspace_bytes": stp.ws_bytes, "clocks": cks.summary()})
+            del stp
+            torch.cuda.empty_cache()
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_linear(lin)
     if rank == 0:

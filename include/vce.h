@@ -258,6 +258,22 @@ vce_status lce_backward(const void* X, const void* W, int64_t n, int64_t h, int6
                         int64_t ignore_idx, void* dX, void* dW, void* ws, size_t ws_bytes,
                         int* dev_status, void* stream);
 
+/* ------------------------------------------------------------------------ */
+/* diagnostics                                                              */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Failure-detection self-test of the bounded wait that every tensor-core
+ * pipeline wait of lce_forward / lce_backward uses.  The pages have no
+ * counterpart of this call.  One thread waits on an mbarrier that nothing
+ * arrives on; after ``timeout_ns`` (1 ns .. 2 s) the wait gives up and
+ * VCE_DEVSTATUS_TIMEOUT is ORed into *dev_status (device int).  When
+ * ``waited_ns`` (device, may be NULL) is given it receives the measured wait.
+ * The kernel returns normally and the context stays usable.
+ */
+vce_status vce_selftest_wait_timeout(uint64_t timeout_ns, int* dev_status,
+                                     unsigned long long* waited_ns, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

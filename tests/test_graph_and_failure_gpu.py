@@ -1,0 +1,87 @@
+"""CUDA-graph capture of every entry point (the API card's CUDA-graph-capturable
+mode: no host synchronisation or allocation inside a call) and the bounded-wait
+failure detection of the tensor-core pipelines, exercised without a GPU fault."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as wk
+import vocabulary_cross_entropy_gb300 as vce
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from vocabulary_cross_entropy_gb300 import build
+    build.build()
+
+
+def _bf16(a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(DEV).view(torch.bfloat16)
+
+
+def test_all_entry_points_replay_in_a_cuda_graph():
+    n, v, h, vl = 300, 5003, 256, 3001
+    z = _bf16(wk.normal_matrix(1, wk.TID_LOGITS, n, v, 3.0, True))
+    y = torch.from_numpy(wk.uniform_targets(1, n, v, 0.1)).to(DEV)
+    x = _bf16(wk.normal_matrix(1, wk.TID_X, n, h, 1.0, True))
+    w = _bf16(wk.normal_matrix(1, wk.TID_W, vl, h, h ** -0.5, True))
+    yl = torch.from_numpy(wk.uniform_targets(2, n, vl, 0.05)).to(DEV)
+    g = torch.ones(1, device=DEV)
+    # every buffer allocated up front; the graph holds only library launches
+    loss, stats, nv = torch.empty(1, device=DEV), torch.empty(n, 2, device=DEV), torch.empty(1, dtype=torch.int64, device=DEV)
+    ws = torch.empty(vce.ce_workspace_size(n, v, True), dtype=torch.uint8, device=DEV)
+    dz = torch.empty_like(z)
+    lloss, lse, lnv = torch.empty(1, device=DEV), torch.empty(n, device=DEV), torch.empty(1, dtype=torch.int64, device=DEV)
+    lws = torch.empty(vce.lce_workspace_size(n, h, vl, True), dtype=torch.uint8, device=DEV)
+    dx, dw = torch.empty_like(x), torch.empty_like(w)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+
+    def step():
+        vce.ce_forward(z, y, 0.1, True, loss=loss, stats=stats, n_valid=nv, workspace=ws, dev_status=status)
+        vce.ce_backward(z, y, stats, nv, g, 0.1, True, dlogits=dz, dev_status=status)
+        vce.lce_forward(x, w, yl, 0.0, True, loss=lloss, lse=lse, n_valid=lnv, workspace=lws, dev_status=status)
+        vce.lce_backward(x, w, yl, lse, lnv, g, 0.0, True, dX=dx, dW=dw, workspace=lws, dev_status=status)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()  # eager run first: per-kernel attributes are set outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    eager = [t.clone() for t in (loss, stats, dz, lloss, lse, dx, dw)]
+    for t in (loss, stats, dz, lloss, lse, dx, dw):
+        t.zero_()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(eager, (loss, stats, dz, lloss, lse, dx, dw)):
+        assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a,
+                           b.view(torch.int16) if b.dtype == torch.bfloat16 else b)
+    assert int(status.item()) == 0
+
+
+@pytest.mark.parametrize("timeout_ns", [1000, 2_000_000])
+def test_bounded_wait_times_out_and_reports(timeout_ns):
+    lib = vce.library()
+    f = lib.vce_selftest_wait_timeout
+    f.argtypes = [ctypes.c_uint64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    waited = torch.zeros(1, dtype=torch.int64, device=DEV)
+    st = f(timeout_ns, ctypes.c_void_p(status.data_ptr()), ctypes.c_void_p(waited.data_ptr()),
+           ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0
+    torch.cuda.synchronize()
+    assert int(status.item()) == vce.DEVSTATUS_TIMEOUT
+    assert timeout_ns <= int(waited.item()) < timeout_ns + 1_000_000_000
+    # the context is still usable afterwards
+    a = torch.arange(10, device=DEV)
+    assert int(a.sum().item()) == 45

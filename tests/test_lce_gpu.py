@@ -149,14 +149,7 @@ def test_small_linear_workload_full():
 # the oracle (dW rows need the oracle's lse of every token: one FP64 forward)
 # ---------------------------------------------------------------------------
 
-# the benchmark's launch configurations: the headline in one vocabulary slab, the
-# large workload with its dZ slab capped at 1 GiB (4 slabs, FP32 dX accumulation)
-@pytest.mark.parametrize("wl,slab_cap,entropy", [(wk.LINEAR_HEADLINE, 0, False),
-                                                 (wk.LINEAR_LARGE, 1 << 30, True)],
-                         ids=["headline", "large_slab1GiB_entropy"])
-def test_full_size_sampled(wl, slab_cap, entropy):
-    inp = wk.make_linear_inputs(wl)
-    f, b = run(inp.x, inp.w, inp.target, wl.label_smoothing, wl.reduce_loss, inp.grad, slab_cap, entropy)
+def _sampled_check(wl, inp, f, b, entropy):
     assert int(f.dev_status.item()) == 0 and int(b.dev_status.item()) == 0
     n_valid = int((inp.target != -100).sum())
     assert int(f.n_valid.item()) == n_valid
@@ -166,10 +159,10 @@ def test_full_size_sampled(wl, slab_cap, entropy):
     assert np.max(np.abs(lse_gpu - lse_all)) <= 2e-3
     if entropy:
         assert np.max(np.abs(f.entropy.double().cpu().numpy() - ent_all)) <= 2e-3
-    assert abs(f.loss.item() - oracle.mean_loss(loss_all, n_valid)) <= 2e-3
+    assert abs(f.loss.item() - oracle.reduce(loss_all, n_valid, wl.reduce_loss)) <= 2e-3
     g_all = oracle.upstream(inp.grad, wl.n, n_valid, wl.reduce_loss)
     rng = np.random.default_rng(0)
-    rows = np.unique(np.concatenate([rng.choice(wl.n, 24, replace=False), [0, wl.n - 1]]))
+    rows = np.unique(np.concatenate([rng.choice(wl.n, min(wl.n, 24), replace=False), [0, wl.n - 1]]))
     dx_ref = oracle.lce_dx_rows(inp.x[rows], inp.w, inp.target[rows], lse_all[rows], g_all[rows],
                                 wl.label_smoothing)
     gx = host_f64(b.dX[torch.from_numpy(rows).to(DEV)])
@@ -182,3 +175,26 @@ def test_full_size_sampled(wl, slab_cap, entropy):
     dw_ref = oracle.lce_dw_rows(inp.x, inp.w, vids, inp.target, lse_all, g_all, wl.label_smoothing)
     gw = host_f64(b.dW[torch.from_numpy(vids).to(DEV)])
     assert rel(gw, dw_ref) <= 1e-2, rel(gw, dw_ref)
+
+
+# production classifier shapes (H, V) of the model-shape sweep, at 512 tokens so the
+# oracle's FP64 forward over every token stays short; V = 151936 ends in a half tile
+@pytest.mark.parametrize("shape", wk.MODEL_SHAPES, ids=lambda w: w.name)
+def test_model_shapes_sampled(shape):
+    import dataclasses
+    wl = dataclasses.replace(shape, n=512, name=shape.name + "_512tok", ignore_frac=0.05,
+                             label_smoothing=0.1)
+    inp = wk.make_linear_inputs(wl)
+    f, b = run(inp.x, inp.w, inp.target, wl.label_smoothing, wl.reduce_loss, inp.grad, 0, True)
+    _sampled_check(wl, inp, f, b, True)
+
+
+# the benchmark's launch configurations: the headline in one vocabulary slab, the
+# large workload with its dZ slab capped at 1 GiB (4 slabs, FP32 dX accumulation)
+@pytest.mark.parametrize("wl,slab_cap,entropy", [(wk.LINEAR_HEADLINE, 0, False),
+                                                 (wk.LINEAR_LARGE, 1 << 30, True)],
+                         ids=["headline", "large_slab1GiB_entropy"])
+def test_full_size_sampled(wl, slab_cap, entropy):
+    inp = wk.make_linear_inputs(wl)
+    f, b = run(inp.x, inp.w, inp.target, wl.label_smoothing, wl.reduce_loss, inp.grad, slab_cap, entropy)
+    _sampled_check(wl, inp, f, b, entropy)

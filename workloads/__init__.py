@@ -203,6 +203,15 @@ def logits_rows(wl: LogitsWorkload, rows) -> np.ndarray:
     return normal_rows(wl.seed, TID_LOGITS, rows, wl.vocab, wl.std, wl.dtype == "bf16")
 
 
+# classifier shapes of production models at M = 8192 tokens (the Liger SM100 pull
+# request's "Model-shape campaign": random BF16 inputs)
+MODEL_SHAPES = [
+    LinearWorkload("qwen3_30b_a3b_8192x2048x151936", 8192, 2048, 151936),
+    LinearWorkload("llama4_8192x5120x202048", 8192, 5120, 202048),
+    LinearWorkload("deepseek_v3_8192x7168x129280", 8192, 7168, 129280),
+]
+
+
 @dataclass
 class LinearInputs:
     x: np.ndarray             # [N, H] uint16 bf16 bits
