@@ -287,6 +287,9 @@ FUSED = [
     (33, 32001, "f32", 0.0, False, True),
     (6, 262144, "bf16", 0.0, True, False),
     (64, 4099, "bf16", 0.1, 2, True),
+    (40, 49152, "bf16", 0.1, True, False),
+    (25, 98304, "f32", 0.0, 2, True),
+    (130, 128256, "bf16", 0.0, False, True),
 ]
 
 
@@ -302,7 +305,7 @@ def test_fused_matches_oracle_and_separate_path(n, vocab, dtype, eps, red, inpla
     r = run_fused(b, target, eps, red, grad, inplace=inplace)
     if inplace:
         assert r.dlogits.data_ptr() == b.data_ptr()
-    # same arithmetic as ce_forward + ce_backward: bit-identical results
+    # same arithmetic in the same order as ce_forward + ce_backward: bit-identical results
     assert torch.equal(r.stats, sep_f.stats)
     assert torch.equal(r.loss, sep_f.loss)
     assert int(r.n_valid.item()) == int(sep_f.n_valid.item())
