@@ -91,6 +91,10 @@ const char* vce_status_string(int status);
 /* Library ABI version (major * 100 + minor). */
 int vce_version(void);
 
+/* Number of kernels this library has launched in this process so far (a host-side
+ * counter; diagnostics, e.g. counting the launches of a timed region). */
+unsigned long long vce_kernel_launches(void);
+
 /* ------------------------------------------------------------------------ */
 /* logits form                                                              */
 /* ------------------------------------------------------------------------ */

@@ -21,6 +21,7 @@ from ._binding import (  # noqa: F401
     library_path,
     vce_status_string,
     vce_version,
+    vce_kernel_launches,
     ce_workspace_size,
     ce_forward,
     ce_forward_noalloc,

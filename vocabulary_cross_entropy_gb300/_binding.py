@@ -44,6 +44,8 @@ def library() -> ctypes.CDLL:
     lib.vce_status_string.restype = ctypes.c_char_p
     lib.vce_version.argtypes = []
     lib.vce_version.restype = _c_int
+    lib.vce_kernel_launches.argtypes = []
+    lib.vce_kernel_launches.restype = ctypes.c_ulonglong
     lib.ce_workspace_size.argtypes = [_c_i64, _c_i64, _c_int]
     lib.ce_workspace_size.restype = _c_size
     lib.ce_forward.argtypes = [_c_p, _c_int, _c_i64, _c_i64, _c_i64, _c_p, _c_f32, _c_int, _c_i64,
@@ -76,6 +78,11 @@ def vce_status_string(status: int) -> str:
 
 def vce_version() -> int:
     return int(library().vce_version())
+
+
+def vce_kernel_launches() -> int:
+    """Kernels the library has launched in this process (host-side count)."""
+    return int(library().vce_kernel_launches())
 
 
 def _check(func: str, status: int):

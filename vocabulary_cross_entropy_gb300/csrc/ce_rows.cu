@@ -330,6 +330,7 @@ template <typename T, int THREADS>
 void fwd_launch(const void* logits, int64_t n_rows, int64_t vocab, int64_t stride,
                 const int64_t* target, float eps, int64_t ignore_idx, float* loss_rows,
                 float* stats, int* dev_status, cudaStream_t s, int grid) {
+    count_launch();
     if (eps != 0.f)
         ce_forward_rows<THREADS, T, true><<<grid, THREADS, 0, s>>>(
             static_cast<const T*>(logits), n_rows, vocab, stride, target, eps, ignore_idx,
@@ -362,6 +363,7 @@ void bwd_dispatch(const void* logits, int64_t n_rows, int64_t vocab, int64_t str
     const T* z = static_cast<const T*>(logits);
     T* dz = static_cast<T*>(dlogits);
     const float2* st = reinterpret_cast<const float2*>(stats);
+    count_launch();
     if (nvec <= 1024)
         ce_backward_rows<128, T><<<grid, 128, 0, s>>>(z, n_rows, vocab, stride, target, st, n_valid,
                                                        grad_output, eps, reduce_loss, ignore_idx, dz, dev_status);
@@ -523,6 +525,7 @@ void fused_launch(const void* logits, int64_t n_rows, int64_t vocab, int64_t str
     float2* st = reinterpret_cast<float2*>(stats);
     const int64_t cap = int64_t(num_sms) * MINB;
     const int grid = int(n_rows < cap ? n_rows : cap);
+    count_launch();
     if (eps != 0.f)
         ce_fused_rows<THREADS, MINB, U1, T, true><<<grid, THREADS, 0, s>>>(
             z, n_rows, vocab, stride, target, eps, ignore_idx, n_valid, grad_output, reduce_loss, loss_rows, st,
@@ -559,6 +562,7 @@ int row_grid(int64_t n_rows) {
 
 vce_status launch_mean_loss(const float* loss_rows, const int64_t* target, int64_t n_rows,
                             int64_t ignore_idx, int reduce, float* loss_out, int64_t* n_valid, cudaStream_t s) {
+    count_launch();
     mean_loss_kernel<<<1, kMeanThreads, 0, s>>>(loss_rows, target, n_rows, ignore_idx, reduce, loss_out, n_valid);
     return cudaGetLastError() == cudaSuccess ? VCE_OK : VCE_ERR_CUDA;
 }

@@ -622,6 +622,7 @@ vce_status launch_gemm(const CUtensorMap& a, const CUtensorMap& b, int64_t M, in
     if (units <= 0 || args.k_blocks <= 0) return VCE_OK;
     const int64_t pairs = dev.num_sms / 2;
     const int grid = 2 * int(units < pairs ? units : pairs);
+    count_launch();
     kern<<<grid, kThreads, C::kSmemBytes, s>>>(a, b, args, epi);
     return cudaGetLastError() == cudaSuccess ? VCE_OK : VCE_ERR_CUDA;
 }
@@ -759,6 +760,7 @@ vce_status launch_lce_forward(const void* X, const void* W, int64_t n, int64_t h
         return st;
     const int nb = int((v + kVocabTile - 1) / kVocabTile);
     float* loss_rows = reduce_loss ? w.loss_rows : loss;
+    count_launch();
     lce_combine_kernel<<<int((n + kCombRows - 1) / kCombRows), kCombRows * kCombSplit, 0, s>>>(
         w.part_ms, w.part_sum, w.part_t, w.zy, target, n, v, nb, eps, ignore_idx, lse, loss_rows, entropy,
         dev_status);
@@ -811,6 +813,7 @@ vce_status launch_lce_backward(const void* X, const void* W, int64_t n, int64_t 
     if (!plan.direct) {
         const int64_t count4 = n * h / 4;  // h is a multiple of 8
         const int blocks = int((count4 + 255) / 256 < 4096 ? (count4 + 255) / 256 : 4096);
+        count_launch();
         dx_finalize_kernel<<<blocks, 256, 0, s>>>(acc, plan.splits, split_stride, count4, dXb);
         if (cudaGetLastError() != cudaSuccess) return VCE_ERR_CUDA;
     }

@@ -32,6 +32,7 @@ extern "C" vce_status vce_selftest_wait_timeout(uint64_t timeout_ns, int* dev_st
     if (!dev_status || timeout_ns == 0 || timeout_ns > 2000000000ull) return VCE_ERR_INVALID_ARG;
     DeviceInfo dev;
     if (vce_status st = current_device(dev)) return st;
+    count_launch();
     wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(timeout_ns, dev_status, waited_ns);
     return cudaGetLastError() == cudaSuccess ? VCE_OK : VCE_ERR_CUDA;
 }

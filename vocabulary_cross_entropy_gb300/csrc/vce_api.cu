@@ -4,9 +4,16 @@
 
 #include "vce_internal.cuh"
 
+#include <atomic>
 #include <mutex>
 
 namespace vce {
+
+namespace {
+std::atomic<unsigned long long> g_launches{0};
+}
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 vce_status current_device(DeviceInfo& info) {
     static std::mutex mu;
@@ -66,6 +73,8 @@ const char* vce_status_string(int status) {
 }
 
 int vce_version(void) { return 100; }
+
+unsigned long long vce_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 size_t ce_workspace_size(int64_t n_rows, int64_t vocab, int reduce_loss) {
     (void)vocab;

@@ -34,6 +34,9 @@ __device__ __forceinline__ void report(int* dev_status, int bits) {
     if (dev_status) atomicOr(dev_status, bits);
 }
 
+// Host-side count of the kernels this library has launched (diagnostics).
+void count_launch();
+
 // Round up to a multiple of 256 bytes (workspace carving).
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
