@@ -82,6 +82,7 @@ SMALL = [
     (257, 520, 2309, 0.1, True, 0.1),
     (1000, 512, 4099, 0.0, True, 0.0),
     (333, 128, 3000, 0.1, 2, 0.1),     # reduction='sum'
+    (5, 8, 40, 0.1, False, 0.0),        # the smallest hidden size (one 16-byte row)
 ]
 
 
@@ -136,6 +137,19 @@ def test_all_ignored():
     f, b = run(x, w, y, 0.1, True, np.ones(1, np.float32))
     assert int(f.n_valid.item()) == 0 and math.isnan(f.loss.item())
     assert torch.count_nonzero(b.dX).item() == 0 and torch.count_nonzero(b.dW).item() == 0
+
+
+def test_zero_tokens():
+    h, v = 64, 300
+    x = torch.empty(0, h, dtype=torch.bfloat16, device=DEV)
+    w = dev_bf16(wk.normal_matrix(3, wk.TID_W, v, h, 0.125, True))
+    y = torch.empty(0, dtype=torch.int64, device=DEV)
+    f = vce.lce_forward(x, w, y, 0.0, True)
+    dW = torch.full_like(w, 3.0)
+    b = vce.lce_backward(x, w, y, f.lse, f.n_valid, torch.ones(1, device=DEV), 0.0, True, dW=dW)
+    torch.cuda.synchronize()
+    assert int(f.n_valid.item()) == 0 and math.isnan(f.loss.item())
+    assert b.dX.shape == (0, h) and torch.count_nonzero(b.dW).item() == 0
 
 
 def test_small_linear_workload_full():
