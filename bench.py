@@ -55,7 +55,7 @@ def FWD_GEMM_TRAFFIC_BYTES(wl):
     profiles/tc_gemm_linear_4096x4096x32768.md (N = H = 4096, V = 32768), scaled to this
     workload's V: the X bytes stay, the W bytes and the per-tile partials grow with V.
     None for workloads outside that N = H = 4096 family."""
-    captured_v, read_bytes, write_bytes = 32768, 0.306430e9, 7.649792e6
+    captured_v, read_bytes, write_bytes = 32768, 0.304589e9, 7.469824e6
     if wl.n != 4096 or wl.hidden != 4096:
         return None
     x_bytes = wl.n * wl.hidden * 2
