@@ -262,6 +262,24 @@ vce_status lce_backward(const void* X, const void* W, int64_t n, int64_t h, int6
                         int64_t ignore_idx, void* dX, void* dW, void* ws, size_t ws_bytes,
                         int* dev_status, void* stream);
 
+/*
+ * Targets for causal language modelling with token shifting (Cut
+ * Cross-Entropy package card, "what_it_does": optional support for
+ * token-shifting).  With sequences of ``seq_len`` positions stored one after
+ * another (the (B, SQ) layout flattened), position t of a sequence is to be
+ * scored against the label at t + 1 of the same sequence:
+ *     shifted[i] = target[i + 1], or ignore_idx where i is the last position
+ *     of its sequence (i mod seq_len == seq_len - 1) or of the array.
+ * The result is passed as ``target`` to any entry point above; the row
+ * layout of the logits / hidden states does not change, and the last
+ * position of every sequence contributes no loss and no gradient.
+ *
+ *   target   int64 [n] (device); shifted int64 [n] (device), not overlapping target.
+ *   seq_len  >= 1.  A trailing partial sequence follows the same rule.
+ */
+vce_status shift_targets(const int64_t* target, int64_t n, int64_t seq_len, int64_t ignore_idx,
+                         int64_t* shifted, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* diagnostics                                                              */
 /* ------------------------------------------------------------------------ */

@@ -41,7 +41,12 @@ log-sum-exp over the vocabulary kept) and the Liger SM100 pull request
   row (the logits of ignored rows are computed anyway);
 * dZ by the formula above, dX = dZ @ W, dW = dZ^T @ X;
 * optional per-token entropy of the softmax (Liger pull request, "Summary":
-  optional entropy): H_n = -sum_v p_v log p_v = lse_n - sum_v p_v z[n, v].
+  optional entropy): H_n = -sum_v p_v log p_v = lse_n - sum_v p_v z[n, v];
+* token shift for causal language modelling (Cut Cross-Entropy card,
+  "what_it_does": optional token shifting): with sequences of length T laid
+  out one after another, position t of a sequence is scored against the label
+  at t + 1 of the same sequence, and the last position of each sequence is
+  ignored.
 
 Inputs are the exact stored values (bfloat16 or float32) widened to float64.
 The matrix products use NumPy's float64 matmul as a library step; every other
@@ -60,7 +65,7 @@ __all__ = [
     "widen", "row_stats", "row_loss", "grad_columns",
     "ce_forward", "ce_backward", "lce_logits", "lce_forward", "lce_backward",
     "lce_forward_rows", "lce_dx_rows", "lce_lse_all", "lce_dw_rows",
-    "mean_loss", "reduce", "row_entropy", "upstream",
+    "mean_loss", "reduce", "row_entropy", "upstream", "shift_targets",
 ]
 
 
@@ -155,6 +160,19 @@ def reduce(loss_rows: np.ndarray, n_valid: int, reduce_loss):
     if int(reduce_loss) == 2:
         return float(loss_rows.sum())
     return mean_loss(loss_rows, n_valid) if reduce_loss else loss_rows
+
+
+def shift_targets(target, seq_len: int, ignore_idx: int = -100) -> np.ndarray:
+    """shifted[b*T + t] = target[b*T + t + 1] for t < T - 1, ignore_idx for t = T - 1
+    (a final partial sequence of length n mod T follows the same rule)."""
+    target = np.asarray(target, dtype=np.int64)
+    n = len(target)
+    out = np.full(n, ignore_idx, dtype=np.int64)
+    for i in range(n):
+        last_in_sequence = (i % seq_len == seq_len - 1) or (i == n - 1)
+        if not last_in_sequence:
+            out[i] = target[i + 1]
+    return out
 
 
 def row_entropy(z: np.ndarray, lse: np.ndarray) -> np.ndarray:

@@ -212,3 +212,19 @@ def test_full_size_sampled(wl, slab_cap, entropy):
     inp = wk.make_linear_inputs(wl)
     f, b = run(inp.x, inp.w, inp.target, wl.label_smoothing, wl.reduce_loss, inp.grad, slab_cap, entropy)
     _sampled_check(wl, inp, f, b, entropy)
+
+
+def test_token_shifted_causal_lm_loss():
+    # (B, SQ) = (3, 100) sequences: shifted targets from the library, losses and
+    # gradients against the oracle's own shift of the same targets
+    b, sq, h, v = 3, 100, 128, 1000
+    n = b * sq
+    x = wk.normal_matrix(21, wk.TID_X, n, h, 1.0, True)
+    w = wk.normal_matrix(21, wk.TID_W, v, h, h ** -0.5, True)
+    y = wk.uniform_targets(21, n, v, 0.05)
+    yt = torch.from_numpy(y).to(DEV).view(b, sq)
+    shifted = vce.shift_targets(yt, sq)
+    torch.cuda.synchronize()
+    ref_shift = oracle.shift_targets(y, sq)
+    assert np.array_equal(shifted.reshape(-1).cpu().numpy(), ref_shift)
+    check_full(x, w, ref_shift, 0.1, True, np.ones(1, np.float32))

@@ -404,3 +404,29 @@ def test_linear_forward_entropy_equals_logits_entropy():
     np.testing.assert_allclose(out["entropy"], oracle.row_entropy(z, lse), rtol=1e-13)
     _, _, ent = oracle.lce_lse_all(x, w, np.zeros(5, np.int64), entropy=True, rows_per_chunk=2)
     np.testing.assert_allclose(ent, out["entropy"], rtol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# token shift (causal language modelling)
+# ---------------------------------------------------------------------------
+
+def test_shift_targets_small_example():
+    # two sequences of length 4: labels move one to the left, each sequence's last is ignored
+    t = np.array([10, 11, 12, 13, 20, 21, 22, 23])
+    assert list(oracle.shift_targets(t, 4)) == [11, 12, 13, -100, 21, 22, 23, -100]
+    # a trailing partial sequence ends with an ignored position too
+    assert list(oracle.shift_targets(np.arange(6), 4)) == [1, 2, 3, -100, 5, -100]
+    # one long sequence: the plain one-step shift
+    assert list(oracle.shift_targets(np.arange(5), 5, ignore_idx=-1)) == [1, 2, 3, 4, -1]
+
+
+def test_shifted_loss_equals_unshifted_loss_on_sliced_logits():
+    # CCE's shift: logits[:, :-1] scored against labels[:, 1:]
+    b, t, vocab = 3, 7, 19
+    z = rng.standard_normal((b, t, vocab))
+    y = rng.integers(0, vocab, (b, t))
+    shifted = oracle.shift_targets(y.reshape(-1), t)
+    full = oracle.ce_forward(z.reshape(-1, vocab), shifted, 0.1, True)
+    ref = oracle.ce_forward(z[:, :-1].reshape(-1, vocab), y[:, 1:].reshape(-1), 0.1, True)
+    assert full["n_valid"] == b * (t - 1)
+    assert abs(full["loss"] - ref["loss"]) < 1e-13

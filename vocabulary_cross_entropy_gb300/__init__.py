@@ -27,6 +27,7 @@ from ._binding import (  # noqa: F401
     ce_forward_noalloc,
     ce_backward,
     ce_forward_backward,
+    shift_targets,
     lce_workspace_size,
     lce_forward,
     lce_backward,

@@ -60,6 +60,8 @@ def library() -> ctypes.CDLL:
     lib.ce_forward_backward.argtypes = [_c_p, _c_int, _c_i64, _c_i64, _c_i64, _c_p, _c_f32, _c_int,
                                         _c_i64, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_size, _c_p, _c_p]
     lib.ce_forward_backward.restype = _c_int
+    lib.shift_targets.argtypes = [_c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_p]
+    lib.shift_targets.restype = _c_int
     lib.lce_workspace_size.argtypes = [_c_i64, _c_i64, _c_i64, _c_int, _c_size]
     lib.lce_workspace_size.restype = _c_size
     lib.lce_forward.argtypes = [_c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_f32, _c_int, _c_i64,
@@ -268,6 +270,23 @@ def ce_forward_backward(logits, target, grad_output, label_smoothing=0.0, reduce
     _check("ce_forward_backward", st)
     return CEForwardBackward(loss if _reduce(reduce_loss) else loss.view(logits.shape[:-1]), stats, n_valid,
                              dlogits, dev_status)
+
+
+def shift_targets(target, seq_len, ignore_idx=-100, *, out=None, stream=None):
+    """Targets for token-shifted causal LM loss: out[i] = target[i + 1], ignore_idx at the
+    last position of every ``seq_len``-long sequence.  ``target`` may be [B, SQ] or flat."""
+    lib = library()
+    flat = target.reshape(-1)
+    if flat.dtype != torch.int64 or not flat.is_contiguous():
+        raise ValueError("target must be a contiguous int64 tensor")
+    if out is None:
+        out = torch.empty_like(flat)
+    dev = flat.device
+    with torch.cuda.device(dev):
+        st = lib.shift_targets(_ptr(flat), flat.numel(), int(seq_len), int(ignore_idx), _ptr(out),
+                               _stream(dev, stream))
+    _check("shift_targets", st)
+    return out.view(target.shape)
 
 
 def _bf16_2d(t, name):

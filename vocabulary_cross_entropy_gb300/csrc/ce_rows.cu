@@ -326,6 +326,21 @@ mean_loss_kernel(const float* __restrict__ loss_rows, const int64_t* __restrict_
     }
 }
 
+// ---------------------------------------------------------------------------
+// token shift for causal language modelling
+// ---------------------------------------------------------------------------
+
+// shifted[i] = target[i + 1] unless i is the last position of its sequence of
+// ``seq_len`` positions (or of the whole array), where it is ignore_idx.
+__global__ void shift_targets_kernel(const int64_t* __restrict__ target, int64_t n, int64_t seq_len,
+                                     int64_t ignore_idx, int64_t* __restrict__ shifted) {
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += int64_t(gridDim.x) * blockDim.x) {
+        const bool last = (i % seq_len == seq_len - 1) || (i == n - 1);
+        shifted[i] = last ? ignore_idx : target[i + 1];
+    }
+}
+
 template <typename T, int THREADS>
 void fwd_launch(const void* logits, int64_t n_rows, int64_t vocab, int64_t stride,
                 const int64_t* target, float eps, int64_t ignore_idx, float* loss_rows,
@@ -559,6 +574,15 @@ int row_grid(int64_t n_rows) {
 }
 
 }  // namespace
+
+vce_status launch_shift_targets(const int64_t* target, int64_t n, int64_t seq_len, int64_t ignore_idx,
+                                int64_t* shifted, cudaStream_t s) {
+    if (n == 0) return VCE_OK;
+    const int64_t blocks = (n + 255) / 256;
+    count_launch();
+    shift_targets_kernel<<<int(blocks < 4096 ? blocks : 4096), 256, 0, s>>>(target, n, seq_len, ignore_idx, shifted);
+    return cudaGetLastError() == cudaSuccess ? VCE_OK : VCE_ERR_CUDA;
+}
 
 vce_status launch_mean_loss(const float* loss_rows, const int64_t* target, int64_t n_rows,
                             int64_t ignore_idx, int reduce, float* loss_out, int64_t* n_valid, cudaStream_t s) {

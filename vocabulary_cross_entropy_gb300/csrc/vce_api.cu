@@ -151,6 +151,15 @@ vce_status ce_forward_backward(const void* logits, int dtype, int64_t n_rows, in
                                       dev_status, static_cast<cudaStream_t>(stream), dev);
 }
 
+vce_status shift_targets(const int64_t* target, int64_t n, int64_t seq_len, int64_t ignore_idx,
+                         int64_t* shifted, void* stream) {
+    if (n < 0 || seq_len < 1 || (n > 0 && (!target || !shifted))) return VCE_ERR_INVALID_ARG;
+    if (n > 0 && target == shifted) return VCE_ERR_INVALID_ARG;  // the kernel reads target[i + 1]
+    DeviceInfo dev;
+    if (vce_status st = current_device(dev)) return st;
+    return launch_shift_targets(target, n, seq_len, ignore_idx, shifted, static_cast<cudaStream_t>(stream));
+}
+
 size_t lce_workspace_size(int64_t n, int64_t h, int64_t v, int reduce_loss,
                           size_t max_slab_bytes) {
     if (n <= 0 || h <= 0 || v <= 0) return 0;

@@ -68,6 +68,8 @@ vce_status launch_ce_forward_backward(const void* logits, int dtype, int64_t n_r
                                       int64_t ignore_idx, const float* grad_output, float* loss, float* stats,
                                       int64_t* n_valid, void* dlogits, void* ws, int* dev_status,
                                       cudaStream_t s, const DeviceInfo& dev);
+vce_status launch_shift_targets(const int64_t* target, int64_t n, int64_t seq_len, int64_t ignore_idx,
+                                int64_t* shifted, cudaStream_t s);
 // mean of per-row losses over rows whose target is not ignore_idx, and the count
 vce_status launch_mean_loss(const float* loss_rows, const int64_t* target, int64_t n_rows,
                             int64_t ignore_idx, int reduce, float* loss_out, int64_t* n_valid,
