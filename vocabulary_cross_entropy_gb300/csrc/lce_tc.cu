@@ -602,12 +602,20 @@ vce_status launch_gemm(const CUtensorMap& a, const CUtensorMap& b, int64_t M, in
                        int k_splits, const Epi& epi, int* dev_status, cudaStream_t s, const DeviceInfo& dev) {
     using C = PairCfg<BN>;
     auto kern = tc_gemm_kernel<Epi, kAMn, kBMn, BN>;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::kSmemBytes));
-    });
-    if (attr_err != cudaSuccess) return VCE_ERR_CUDA;
+    // the shared-memory limit is a per-device attribute of the kernel: raise it
+    // once on every device this instantiation runs on
+    static std::mutex mu;
+    static bool raised[64] = {};
+    if (dev.ordinal < 0 || dev.ordinal >= 64) return VCE_ERR_CUDA;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!raised[dev.ordinal]) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::kSmemBytes)) !=
+                cudaSuccess)
+                return VCE_ERR_CUDA;
+            raised[dev.ordinal] = true;
+        }
+    }
     GemmArgs args;
     args.tiles_m = int((M + BM - 1) / BM);
     args.tiles_n = int((N + BN - 1) / BN);
