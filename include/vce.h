@@ -143,7 +143,10 @@ vce_status ce_forward(const void* logits, int dtype, int64_t n_rows, int64_t voc
  *   dlogits     same dtype and layout (row_stride) as logits; MAY EQUAL logits,
  *               in which case the logits are overwritten by their gradient (the
  *               pull request's destructive mode: no extra buffer).  Any other
- *               overlap is undefined.  Ignored rows are written as zeros.
+ *               overlap is undefined.  Its address must have the same offset
+ *               modulo 16 bytes as logits (else VCE_ERR_ALIGN); buffers of
+ *               equal layout from one allocator always do.  Ignored rows are
+ *               written as zeros.
  */
 vce_status ce_backward(const void* logits, int dtype, int64_t n_rows, int64_t vocab,
                        int64_t row_stride, const int64_t* target, const float* stats,
@@ -164,8 +167,9 @@ vce_status ce_backward(const void* logits, int dtype, int64_t n_rows, int64_t vo
  *
  *   Arguments are those of ce_forward and ce_backward combined; the results are
  *   the same as ce_forward followed by ce_backward with the same grad_output
- *   (loss, stats, n_valid, dlogits).  dlogits MAY EQUAL logits (in place).
- *   grad_output F32 [1] when reduce_loss, else [n_rows].
+ *   (loss, stats, n_valid, dlogits).  dlogits MAY EQUAL logits (in place), with
+ *   the same 16-byte offset rule as ce_backward.
+ *   grad_output F32 [1] when reduce_loss != 0, else [n_rows].
  *   ws/ws_bytes: ce_workspace_size(n_rows, vocab, reduce_loss) bytes.
  */
 vce_status ce_forward_backward(const void* logits, int dtype, int64_t n_rows, int64_t vocab,
@@ -208,11 +212,14 @@ vce_status ce_forward_noalloc(const void* logits, int dtype, int64_t n_rows, int
  * Backward recomputes the logits one vocabulary slab at a time and keeps that
  * slab's gradient dZ [n, slab] in BF16; ``max_slab_bytes`` caps that buffer
  * (0 = no cap: one slab covers the whole vocabulary).  The slab is at least
- * 256 vocabulary rows.  With more than one slab, dX is accumulated in an FP32
- * [n, h] buffer inside the workspace.  The forward part holds per-tile
- * softmax partials (12 B per token per 256 vocabulary ids) and the per-token
- * target logit, and the per-tile entropy partials (4 B more per token per 256
- * ids).  The same size passed to lce_backward selects the same slab.
+ * 256 vocabulary rows.  dX = dZ W has few output tiles, so its vocabulary
+ * range is cut into 1-4 chunks (chosen from the tile count and the SM count
+ * of the current device); unless one slab and one chunk let dX be written
+ * directly, each chunk keeps an FP32 [n, h] partial sum inside the workspace.
+ * The forward part holds per-tile softmax partials (16 B per token per 256
+ * vocabulary ids: max, sum of exp, sum of logits, entropy term), the
+ * per-token target logit and, when reducing, the per-token losses.  The same
+ * size passed to lce_backward on the same device selects the same slab.
  */
 size_t lce_workspace_size(int64_t n, int64_t h, int64_t v, int reduce_loss,
                           size_t max_slab_bytes);
