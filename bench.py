@@ -63,6 +63,16 @@ def FWD_GEMM_TRAFFIC_BYTES(wl):
     return x_bytes + (read_bytes - x_bytes) * scale + write_bytes * scale
 
 
+def LOGITS_BWD_TRAFFIC_BYTES(wl):
+    """DRAM bytes (read + write) per launch of ce_backward_rows, from the ncu capture in
+    profiles/ce_rows_logits_2048x128256.md (2048 rows of V = 128256 BF16, 5% ignored),
+    scaled by the row count.  None for other vocabularies or dtypes."""
+    captured_rows, read_bytes, write_bytes = 2048, 502.335488e6, 467.678208e6
+    if wl.vocab != 128256 or wl.dtype != "bf16":
+        return None
+    return (read_bytes + write_bytes) * wl.n_rows / captured_rows
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -615,7 +625,8 @@ def main():
                        "l2": "inputs larger than L2 (4.2 GB logits), no flush"},
             "roofline": {"kernel": "ce_backward_rows", "bound": "hbm", "achieved": bwd_gbs,
                          "peak": pk["hbm"], "unit": "GB/s", "frac": bwd_gbs / pk["hbm"],
-                         "traffic": None, "peak_source": pk["source"] + " hbm_gbs (copy)",
+                         "traffic": LOGITS_BWD_TRAFFIC_BYTES(st.wl),
+                         "peak_source": pk["source"] + " hbm_gbs (copy)",
                          "algorithmic_bytes": st.bytes_bwd()},
             "roofline_fwd": {"kernel": "ce_forward_rows", "bound": "hbm", "achieved": fwd_gbs,
                              "peak": pk["hbm"], "unit": "GB/s", "frac": fwd_gbs / pk["hbm"],
