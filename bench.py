@@ -695,6 +695,11 @@ def main():
                      "frac": fwd_tf / pk["bf16_sustained"], "traffic": FWD_GEMM_TRAFFIC_BYTES(st.wl),
                      "peak_source": pk["source"] + " bf16_tflops_sustained (cuBLAS, seconds-long loop)",
                      "frac_of_burst_peak": fwd_tf / pk["bf16"],
+                     # against the dense BF16 rate of the SMs at the clock they ran at:
+                     # 8192 flops per SM per cycle x SM count x median SM clock
+                     "frac_of_tensor_peak_at_clock": (
+                         fwd_tf / (torch.cuda.get_device_properties(dev).multi_processor_count * 8192.0
+                                   * clocks["sm_mhz"] * 1e6 / 1e12)) if clocks.get("sm_mhz") else None,
                      "algorithmic_flops": fwd_flops},
         "e2e": e2e_obj,
         "gpu_launches": st.timed_launches,

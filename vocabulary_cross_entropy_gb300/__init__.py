@@ -32,3 +32,4 @@ from ._binding import (  # noqa: F401
     lce_forward,
     lce_backward,
 )
+from .autograd import parallel_cross_entropy, linear_cross_entropy  # noqa: F401,E402
