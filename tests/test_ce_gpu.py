@@ -290,6 +290,9 @@ FUSED = [
     (40, 49152, "bf16", 0.1, True, False),
     (25, 98304, "f32", 0.0, 2, True),
     (130, 128256, "bf16", 0.0, False, True),
+    # several rows per persistent CTA: next-row L2 prefetch on (bf16) and off (f32, rows too large)
+    (500, 65536, "bf16", 0.0, 2, True),
+    (400, 131072, "f32", 0.1, True, False),
 ]
 
 

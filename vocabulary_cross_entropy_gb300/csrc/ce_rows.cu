@@ -149,8 +149,8 @@ __device__ __forceinline__ void block_merge(OnlineLse& a, float* sm_m, float* sm
 // K1: forward row kernel
 // ---------------------------------------------------------------------------
 
-template <int THREADS, typename T, bool kSmooth>
-__global__ void __launch_bounds__(THREADS)
+template <int THREADS, int MINB, typename T, bool kSmooth>
+__global__ void __launch_bounds__(THREADS, MINB)
 ce_forward_rows(const T* __restrict__ logits, int64_t n_rows, int64_t vocab, int64_t stride,
                 const int64_t* __restrict__ target, float eps, int64_t ignore_idx,
                 float* __restrict__ loss_rows, float2* __restrict__ stats, int* dev_status) {
@@ -341,17 +341,17 @@ __global__ void shift_targets_kernel(const int64_t* __restrict__ target, int64_t
     }
 }
 
-template <typename T, int THREADS>
+template <typename T, int THREADS, int MINB>
 void fwd_launch(const void* logits, int64_t n_rows, int64_t vocab, int64_t stride,
                 const int64_t* target, float eps, int64_t ignore_idx, float* loss_rows,
                 float* stats, int* dev_status, cudaStream_t s, int grid) {
     count_launch();
     if (eps != 0.f)
-        ce_forward_rows<THREADS, T, true><<<grid, THREADS, 0, s>>>(
+        ce_forward_rows<THREADS, MINB, T, true><<<grid, THREADS, 0, s>>>(
             static_cast<const T*>(logits), n_rows, vocab, stride, target, eps, ignore_idx,
             loss_rows, reinterpret_cast<float2*>(stats), dev_status);
     else
-        ce_forward_rows<THREADS, T, false><<<grid, THREADS, 0, s>>>(
+        ce_forward_rows<THREADS, MINB, T, false><<<grid, THREADS, 0, s>>>(
             static_cast<const T*>(logits), n_rows, vocab, stride, target, eps, ignore_idx,
             loss_rows, reinterpret_cast<float2*>(stats), dev_status);
 }
@@ -360,13 +360,17 @@ template <typename T>
 void fwd_dispatch(const void* logits, int64_t n_rows, int64_t vocab, int64_t stride,
                   const int64_t* target, float eps, int64_t ignore_idx, float* loss_rows,
                   float* stats, int* dev_status, cudaStream_t s, int grid) {
+    // The thread count per row fixes the summation order, so it is the same as the
+    // fused kernel's for every row length (fused results equal forward + backward
+    // bit for bit).  Long rows: two 1024-thread CTAs per SM (32 registers).
+    // MINB 0 leaves the register budget to the compiler.
     const int64_t nvec = vocab / Elem<T>::kVec;
     if (nvec <= 1024)
-        fwd_launch<T, 128>(logits, n_rows, vocab, stride, target, eps, ignore_idx, loss_rows, stats, dev_status, s, grid);
+        fwd_launch<T, 128, 0>(logits, n_rows, vocab, stride, target, eps, ignore_idx, loss_rows, stats, dev_status, s, grid);
     else if (nvec <= 4096)
-        fwd_launch<T, 256>(logits, n_rows, vocab, stride, target, eps, ignore_idx, loss_rows, stats, dev_status, s, grid);
+        fwd_launch<T, 256, 0>(logits, n_rows, vocab, stride, target, eps, ignore_idx, loss_rows, stats, dev_status, s, grid);
     else
-        fwd_launch<T, 512>(logits, n_rows, vocab, stride, target, eps, ignore_idx, loss_rows, stats, dev_status, s, grid);
+        fwd_launch<T, 1024, 2>(logits, n_rows, vocab, stride, target, eps, ignore_idx, loss_rows, stats, dev_status, s, grid);
 }
 
 template <typename T>
@@ -393,6 +397,19 @@ void bwd_dispatch(const void* logits, int64_t n_rows, int64_t vocab, int64_t str
 // ---------------------------------------------------------------------------
 // fused forward + backward (one HBM read, one HBM write per element)
 // ---------------------------------------------------------------------------
+
+// Asks L2 to fetch the 16-byte aligned interior of a row from HBM, in 32 KiB
+// bulk requests (cp.async.bulk.prefetch.L2).  A hint only: nothing waits on it
+// and results do not depend on it; every requested byte lies inside the row.
+template <typename T>
+__device__ __forceinline__ void prefetch_row_l2(const T* row, int64_t vocab) {
+    const uintptr_t b = reinterpret_cast<uintptr_t>(row);
+    const uintptr_t a1 = (b + uintptr_t(vocab) * sizeof(T)) & ~uintptr_t(15);
+    for (uintptr_t a = (b + 15) & ~uintptr_t(15); a < a1; a += 32768) {
+        const uint32_t bytes = uint32_t(a1 - a < 32768 ? a1 - a : 32768);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a), "r"(bytes) : "memory");
+    }
+}
 
 // Streams one row through the online (max, sum exp) accumulator.
 template <int THREADS, int U, typename T, bool kSmooth>
@@ -438,10 +455,13 @@ __device__ __forceinline__ void row_zero(T* q, const RowSplit<T>& sp, int64_t vo
 
 // Row kernel doing the forward and, with the row still in L2, the backward:
 // loss, (max, lse) and dlogits = g (softmax - (1-eps) onehot - eps/V) from one
-// pass over HBM in each direction.  A persistent grid of two CTAs per SM keeps
-// about 2 x 152 rows in flight, small enough for their second read to hit L2.
+// pass over HBM in each direction.  A persistent grid keeps MINB rows per SM in
+// flight, few enough for their second read to hit L2.  With kPrefetch, the CTA
+// asks L2 for its next row as its second pass starts, so HBM reads continue
+// while the CTA reads L2 and writes gradients (the caller enables it only when
+// two rows per CTA fit in L2 with room to spare).
 // dlogits may equal logits (the row is overwritten by its gradient).
-template <int THREADS, int MINB, int U1, typename T, bool kSmooth>
+template <int THREADS, int MINB, int U1, int U2, typename T, bool kSmooth, bool kPrefetch>
 __global__ void __launch_bounds__(THREADS, MINB)
 ce_fused_rows(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, const int64_t* __restrict__ target,
               float eps, int64_t ignore_idx, const int64_t* __restrict__ n_valid,
@@ -449,7 +469,7 @@ ce_fused_rows(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
               float2* __restrict__ stats, T* dlogits, int* dev_status) {
     using E = Elem<T>;
     constexpr int V = E::kVec;
-    constexpr int U = 2;
+    constexpr int U = U2;
     __shared__ float sm_m[32], sm_s[32], sm_sum[32];
     __shared__ float sm_lse;
 
@@ -484,6 +504,10 @@ ce_fused_rows(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
             loss_rows[row] = loss;
             stats[row] = make_float2(acc.m, lse);
             sm_lse = lse;
+        }
+        if (kPrefetch && threadIdx.x == 32) {
+            const int64_t next = row + gridDim.x;
+            if (next < n_rows && target[next] != ignore_idx) prefetch_row_l2(logits + next * stride, vocab);
         }
         __syncthreads();
         if (bad) {
@@ -530,42 +554,62 @@ ce_fused_rows(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
     }
 }
 
-template <typename T, int THREADS, int MINB, int U1>
+template <typename T, int THREADS, int MINB, int U1, int U2, bool kPrefetch>
 void fused_launch(const void* logits, int64_t n_rows, int64_t vocab, int64_t stride, const int64_t* target,
                   float eps, int64_t ignore_idx, const int64_t* n_valid, const float* grad_output,
                   int reduce_loss, float* loss_rows, float* stats, void* dlogits, int* dev_status,
-                  cudaStream_t s, int num_sms) {
+                  cudaStream_t s, int grid) {
     const T* z = static_cast<const T*>(logits);
     T* dz = static_cast<T*>(dlogits);
     float2* st = reinterpret_cast<float2*>(stats);
-    const int64_t cap = int64_t(num_sms) * MINB;
-    const int grid = int(n_rows < cap ? n_rows : cap);
     count_launch();
     if (eps != 0.f)
-        ce_fused_rows<THREADS, MINB, U1, T, true><<<grid, THREADS, 0, s>>>(
+        ce_fused_rows<THREADS, MINB, U1, U2, T, true, kPrefetch><<<grid, THREADS, 0, s>>>(
             z, n_rows, vocab, stride, target, eps, ignore_idx, n_valid, grad_output, reduce_loss, loss_rows, st,
             dz, dev_status);
     else
-        ce_fused_rows<THREADS, MINB, U1, T, false><<<grid, THREADS, 0, s>>>(
+        ce_fused_rows<THREADS, MINB, U1, U2, T, false, kPrefetch><<<grid, THREADS, 0, s>>>(
             z, n_rows, vocab, stride, target, eps, ignore_idx, n_valid, grad_output, reduce_loss, loss_rows, st,
             dz, dev_status);
+}
+
+// Persistent grid of ``per_sm`` CTAs per SM, or one CTA per row if fewer.
+inline int fused_grid(int64_t n_rows, int num_sms, int per_sm) {
+    const int64_t cap = int64_t(num_sms) * per_sm;
+    return int(n_rows < cap ? n_rows : cap);
 }
 
 template <typename T>
 void fused_dispatch(const void* logits, int64_t n_rows, int64_t vocab, int64_t stride, const int64_t* target,
                     float eps, int64_t ignore_idx, const int64_t* n_valid, const float* grad_output,
                     int reduce_loss, float* loss_rows, float* stats, void* dlogits, int* dev_status,
-                    cudaStream_t s, int num_sms) {
+                    cudaStream_t s, const DeviceInfo& dev) {
+    // Same threads per row as the forward kernel (identical summation order).
     const int64_t nvec = vocab / Elem<T>::kVec;
-    if (nvec <= 1024)
-        fused_launch<T, 128, 8, 4>(logits, n_rows, vocab, stride, target, eps, ignore_idx, n_valid, grad_output,
-                                      reduce_loss, loss_rows, stats, dlogits, dev_status, s, num_sms);
-    else if (nvec <= 4096)
-        fused_launch<T, 256, 4, 4>(logits, n_rows, vocab, stride, target, eps, ignore_idx, n_valid, grad_output,
-                                      reduce_loss, loss_rows, stats, dlogits, dev_status, s, num_sms);
+    if (nvec <= 1024) {
+        fused_launch<T, 128, 8, 4, 2, false>(logits, n_rows, vocab, stride, target, eps, ignore_idx, n_valid,
+                                             grad_output, reduce_loss, loss_rows, stats, dlogits, dev_status, s,
+                                             fused_grid(n_rows, dev.num_sms, 8));
+        return;
+    }
+    if (nvec <= 4096) {
+        fused_launch<T, 256, 4, 4, 2, false>(logits, n_rows, vocab, stride, target, eps, ignore_idx, n_valid,
+                                             grad_output, reduce_loss, loss_rows, stats, dlogits, dev_status, s,
+                                             fused_grid(n_rows, dev.num_sms, 4));
+        return;
+    }
+    // Long rows: one 1024-thread CTA per SM.  The next-row prefetch doubles the
+    // rows resident in L2; it pays while both rows of every CTA take at most
+    // two thirds of L2, and thrashes it beyond (measured: 256 KiB rows gain 10%,
+    // 400-500 KiB rows lose 5-25%).
+    const int grid = fused_grid(n_rows, dev.num_sms, 1);
+    const double resident = 2.0 * double(grid) * double(vocab) * double(sizeof(T));
+    if (resident <= double(dev.l2_bytes) * 2.0 / 3.0)
+        fused_launch<T, 1024, 1, 4, 4, true>(logits, n_rows, vocab, stride, target, eps, ignore_idx, n_valid,
+                                             grad_output, reduce_loss, loss_rows, stats, dlogits, dev_status, s, grid);
     else
-        fused_launch<T, 512, 2, 4>(logits, n_rows, vocab, stride, target, eps, ignore_idx, n_valid, grad_output,
-                                      reduce_loss, loss_rows, stats, dlogits, dev_status, s, num_sms);
+        fused_launch<T, 1024, 1, 4, 4, false>(logits, n_rows, vocab, stride, target, eps, ignore_idx, n_valid,
+                                              grad_output, reduce_loss, loss_rows, stats, dlogits, dev_status, s, grid);
 }
 
 int row_grid(int64_t n_rows) {
@@ -642,11 +686,10 @@ vce_status launch_ce_forward_backward(const void* logits, int dtype, int64_t n_r
                 return st;
         if (dtype == VCE_BF16)
             fused_dispatch<__nv_bfloat16>(logits, n_rows, vocab, row_stride, target, eps, ignore_idx, n_valid,
-                                          grad_output, reduce_loss, loss_rows, stats, dlogits, dev_status, s,
-                                          dev.num_sms);
+                                          grad_output, reduce_loss, loss_rows, stats, dlogits, dev_status, s, dev);
         else
             fused_dispatch<float>(logits, n_rows, vocab, row_stride, target, eps, ignore_idx, n_valid,
-                                  grad_output, reduce_loss, loss_rows, stats, dlogits, dev_status, s, dev.num_sms);
+                                  grad_output, reduce_loss, loss_rows, stats, dlogits, dev_status, s, dev);
         if (cudaGetLastError() != cudaSuccess) return VCE_ERR_CUDA;
     }
     if (reduce_loss || n_valid)

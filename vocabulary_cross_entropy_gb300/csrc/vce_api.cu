@@ -26,13 +26,15 @@ vce_status current_device(DeviceInfo& info) {
         if (cache[dev].ordinal != dev) {
             DeviceInfo d;
             d.ordinal = dev;
-            int v = 0;
+            int v = 0, l2 = 0;
             if (cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
                 cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
                 cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-                cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+                cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
                 return VCE_ERR_CUDA;
             d.max_smem_optin = size_t(v);
+            d.l2_bytes = size_t(l2);
             cache[dev] = d;
         }
         info = cache[dev];

@@ -46,6 +46,7 @@ struct DeviceInfo {
     int cc_major = 0, cc_minor = 0;
     int num_sms = 0;
     size_t max_smem_optin = 0;
+    size_t l2_bytes = 0;
 };
 
 // Returns VCE_OK and fills ``info`` for the current device, VCE_ERR_CUDA if the
