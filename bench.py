@@ -124,15 +124,22 @@ def max_over_ranks(pg, x: float) -> float:
 # ---------------------------------------------------------------------------
 
 class Clocks:
-    """nvidia-smi sampling (200 ms) around a timed region; waits for the first sample."""
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi sampling (every 50 ms) around a timed region.
+
+    Each sample carries nvidia-smi's own timestamp, and the summary keeps only the
+    samples taken between entering and leaving the ``with`` block, so that idle
+    readings just before or after the region never enter the median.
+    """
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    INTERVAL_MS = 50
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
         self.lines = []
+        self.t0 = self.t1 = None
 
     def _reader(self):
         for line in self.proc.stdout:
@@ -144,49 +151,64 @@ class Clocks:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", str(self.INTERVAL_MS)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (FileNotFoundError, OSError):
             self.proc = None
             return self
         self.thread = threading.Thread(target=self._reader, daemon=True)
         self.thread.start()
-        t0 = time.time()
-        while not self.lines and time.time() - t0 < 5.0:
+        t = time.time()
+        while not self.lines and time.time() - t < 5.0:
             time.sleep(0.02)
-        self.skip = len(self.lines)  # samples taken before the timed region
+        self.t0 = time.time()
         return self
 
     def __exit__(self, *exc):
+        self.t1 = time.time()
         if self.proc is not None:
-            time.sleep(0.25)
+            time.sleep(0.25)  # let samples taken inside the region arrive
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
             self.thread.join(timeout=2)
-            self.lines = self.lines[getattr(self, "skip", 0):]
         return False
+
+    @staticmethod
+    def _when(stamp):
+        import datetime
+        try:
+            return datetime.datetime.strptime(stamp, "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
 
     def summary(self):
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in self.lines:
-            f = [x.strip() for x in l.split(",")]
-            if len(f) < 9:
+        rows = [[x.strip() for x in l.split(",")] for l in self.lines]
+        rows = [f for f in rows if len(f) >= 10]
+        # if nvidia-smi's timestamps cannot be read, every sample counts (window unknown)
+        stamped = any(self._when(f[0]) is not None for f in rows)
+        for f in rows:
+            when = self._when(f[0])
+            if stamped and (when is None or self.t0 is None or not (self.t0 <= when <= self.t1)):
                 continue
             try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
+                sm.append(float(f[2]))
+                mx.append(float(f[3]))
             except ValueError:
                 continue
-            for name, val in zip(names, f[5:9]):
+            for name, val in zip(names, f[6:10]):
                 if val.lower() == "active":
                     reasons.add(name)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+               "samples": len(sm)}
+        if not stamped:
+            out["window"] = "unfiltered"
+        return out
 
 
 # ---------------------------------------------------------------------------
