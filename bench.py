@@ -63,14 +63,23 @@ def FWD_GEMM_TRAFFIC_BYTES(wl):
     return x_bytes + (read_bytes - x_bytes) * scale + write_bytes * scale
 
 
-def LOGITS_BWD_TRAFFIC_BYTES(wl):
-    """DRAM bytes (read + write) per launch of ce_backward_rows, from the ncu capture in
-    profiles/ce_rows_logits_2048x128256.md (2048 rows of V = 128256 BF16, 5% ignored),
-    scaled by the row count.  None for other vocabularies or dtypes."""
-    captured_rows, read_bytes, write_bytes = 2048, 502.335488e6, 467.678208e6
+# DRAM bytes (read, write) per launch of the logits-form row kernels, from the ncu
+# captures in profiles/ce_rows_logits_2048x128256.md and
+# profiles/ce_fused_rows_logits_2048x128256.md (2048 rows of V = 128256 BF16, 5% ignored)
+LOGITS_CAPTURED_TRAFFIC = {
+    "forward": (502.304768e6, 2.953984e6),
+    "backward": (502.335488e6, 467.678208e6),
+    "fused": (525.410304e6, 467.438848e6),
+}
+
+
+def LOGITS_TRAFFIC_BYTES(wl, kernel):
+    """Read + write DRAM bytes per launch of one row kernel, scaled from the 2048-row
+    capture by the row count.  None for other vocabularies or dtypes."""
     if wl.vocab != 128256 or wl.dtype != "bf16":
         return None
-    return (read_bytes + write_bytes) * wl.n_rows / captured_rows
+    read_bytes, write_bytes = LOGITS_CAPTURED_TRAFFIC[kernel]
+    return (read_bytes + write_bytes) * wl.n_rows / 2048
 
 
 def peaks():
@@ -647,11 +656,12 @@ def main():
                        "l2": "inputs larger than L2 (4.2 GB logits), no flush"},
             "roofline": {"kernel": "ce_backward_rows", "bound": "hbm", "achieved": bwd_gbs,
                          "peak": pk["hbm"], "unit": "GB/s", "frac": bwd_gbs / pk["hbm"],
-                         "traffic": LOGITS_BWD_TRAFFIC_BYTES(st.wl),
+                         "traffic": LOGITS_TRAFFIC_BYTES(st.wl, "backward"),
                          "peak_source": pk["source"] + " hbm_gbs (copy)",
                          "algorithmic_bytes": st.bytes_bwd()},
             "roofline_fwd": {"kernel": "ce_forward_rows", "bound": "hbm", "achieved": fwd_gbs,
                              "peak": pk["hbm"], "unit": "GB/s", "frac": fwd_gbs / pk["hbm"],
+                             "traffic": LOGITS_TRAFFIC_BYTES(st.wl, "forward"),
                              "algorithmic_bytes": st.bytes_fwd()},
             "gpu_launches": st.timed_launches,
             "clocks": clocks_l,
@@ -659,6 +669,7 @@ def main():
             # one HBM read and one write per logit (timed separately, same workload)
             "fused": {"ms_per_step": fused_ms, "value": fused_gbs, "unit": "GB/s",
                       "algorithmic_bytes": st.bytes_bwd(), "frac": fused_gbs / pk["hbm"],
+                      "traffic": LOGITS_TRAFFIC_BYTES(st.wl, "fused"),
                       "speedup_vs_separate": (total / args.steps) / fused_ms},
         }
         if rank == 0 and not args.no_cpu_baseline:
