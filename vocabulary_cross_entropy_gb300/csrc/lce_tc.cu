@@ -68,22 +68,28 @@ struct GemmArgs {
     int k_splits;      // the K range is cut into this many consecutive chunks (separate work units)
     int kb_per_split;  // K blocks per chunk (the last chunk may be shorter)
     int m_fastest;     // unit order: 1 = M index varies fastest, else N; the K chunk varies slowest
+    int group;         // tiles of the fast index per group of the unit order (see unit_coords)
     int* dev_status;
 };
 
 // Work unit u -> output tile (tm, tn), K chunk ks and its K-block range [kb0, kb1).
+// Units are ordered in groups of ``group`` tiles of the fast index: inside a group
+// the fast index cycles over its ``group`` tiles for each value of the slow index.
+// With group = all tiles of the fast index this is plain fast-index-first order.
 __device__ __forceinline__ void unit_coords(const GemmArgs& a, int u, int& tm, int& tn, int& ks, int& kb0,
                                             int& kb1) {
     const int per = a.tiles_m * a.tiles_n;
     ks = u / per;
     const int t = u - ks * per;
-    if (a.m_fastest) {
-        tm = t % a.tiles_m;
-        tn = t / a.tiles_m;
-    } else {
-        tn = t % a.tiles_n;
-        tm = t / a.tiles_n;
-    }
+    const int fast = a.m_fastest ? a.tiles_m : a.tiles_n;
+    const int slow = a.m_fastest ? a.tiles_n : a.tiles_m;
+    const int g = t / (a.group * slow);          // every group but the last has group * slow units
+    const int r = t - g * (a.group * slow);
+    const int f0 = g * a.group;
+    const int gw = fast - f0 < a.group ? fast - f0 : a.group;
+    const int f = f0 + r % gw, sl = r / gw;
+    tm = a.m_fastest ? f : sl;
+    tn = a.m_fastest ? sl : f;
     kb0 = ks * a.kb_per_split;
     kb1 = kb0 + a.kb_per_split;
     if (kb1 > a.k_blocks) kb1 = a.k_blocks;
@@ -597,6 +603,26 @@ bool map_mnmajor(CUtensorMap* m, const void* base, int64_t mn, int64_t k, int64_
     return make_map(m, base, uint64_t(mn), uint64_t(k), uint64_t(ld) * 2, 64, BK);
 }
 
+// Tiles of the fast index per group of the unit order.  The group's strips of the
+// fast-index operand (A when M is fast, B when N is: 256 rows x the unit's K range)
+// are read by every unit of the group, and each strip of the other operand by
+// ``group`` consecutive units, so the fast operand is read from HBM once and the
+// other once per group.  The group is as wide as a third of L2 holds, and never
+// narrower than about sqrt(CTA pairs) tiles: when strips are too long for L2
+// (K = a vocabulary slab), the pairs working at one time then still cover a
+// near-square block of output tiles and share their strips while they stream.
+int raster_group(int tiles_fast, int64_t strip_bytes, const DeviceInfo& dev) {
+    const int pairs = dev.num_sms / 2;
+    int g_win = 1;
+    while (g_win * g_win < pairs) ++g_win;
+    const int64_t budget = int64_t(dev.l2_bytes / 3);
+    const int64_t g_l2 = strip_bytes > 0 ? budget / strip_bytes : tiles_fast;
+    int64_t g = g_l2 > g_win ? g_l2 : g_win;
+    if (g >= tiles_fast) return tiles_fast < 1 ? 1 : tiles_fast;
+    const int64_t groups = (tiles_fast + g - 1) / g;  // equal groups, as few as that width allows
+    return int((tiles_fast + groups - 1) / groups);
+}
+
 template <class Epi, bool kAMn, bool kBMn, int BN>
 vce_status launch_gemm(const CUtensorMap& a, const CUtensorMap& b, int64_t M, int64_t N, int64_t K, int m_fastest,
                        int k_splits, const Epi& epi, int* dev_status, cudaStream_t s, const DeviceInfo& dev) {
@@ -625,6 +651,10 @@ vce_status launch_gemm(const CUtensorMap& a, const CUtensorMap& b, int64_t M, in
     args.kb_per_split = (args.k_blocks + k_splits - 1) / k_splits;
     args.k_splits = (args.k_blocks + args.kb_per_split - 1) / args.kb_per_split;  // every chunk non-empty
     args.m_fastest = m_fastest;
+    {
+        const int64_t strip = int64_t(m_fastest ? BM : BN) * args.kb_per_split * BK * 2;
+        args.group = raster_group(m_fastest ? args.tiles_m : args.tiles_n, strip, dev);
+    }
     args.dev_status = dev_status;
     const int64_t units = int64_t(args.tiles_m) * args.tiles_n * args.k_splits;
     if (units <= 0 || args.k_blocks <= 0) return VCE_OK;
