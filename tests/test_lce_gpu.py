@@ -116,6 +116,24 @@ def test_token_wave_boundaries():
         check_full(x, w, y, 0.0, True, np.ones(1, np.float32))
 
 
+def test_many_short_units_repeatable():
+    # H = 64: every forward work unit is a single K block, so each CTA pair takes
+    # about 27 units from the in-order ticket counter in quick succession, and
+    # the per-launch counter reset is exercised by three calls in a row; the
+    # results must not depend on which pair computed which tile.
+    n, h, v = 4096, 64, 32768
+    x = wk.normal_matrix(21, wk.TID_X, n, h, 1.0, True)
+    w = wk.normal_matrix(21, wk.TID_W, v, h, h ** -0.5, True)
+    y = wk.uniform_targets(21, n, v, 0.05)
+    g = np.ones(1, np.float32)
+    runs = [run(x, w, y, 0.1, True, g) for _ in range(3)]
+    for f, b in runs[1:]:
+        assert torch.equal(f.lse, runs[0][0].lse) and torch.equal(f.loss, runs[0][0].loss)
+        assert torch.equal(b.dX.view(torch.int16), runs[0][1].dX.view(torch.int16))
+        assert torch.equal(b.dW.view(torch.int16), runs[0][1].dW.view(torch.int16))
+    check_full(x, w, y, 0.1, True, g)
+
+
 def test_bad_target_status():
     n, h, v = 64, 64, 300
     x = wk.normal_matrix(1, wk.TID_X, n, h, 1.0, True)
