@@ -51,11 +51,11 @@ PUBLISHED_MODEL_SHAPES_FB_MS = {"qwen3_30b_a3b_8192x2048x151936": 13.692,
 
 
 def FWD_GEMM_TRAFFIC_BYTES(wl):
-    """DRAM bytes (read + write) per launch of the forward GEMM, from the ncu capture in
-    profiles/tc_gemm_linear_4096x4096x32768.md (N = H = 4096, V = 32768), scaled to this
-    workload's V: the X bytes stay, the W bytes and the per-tile partials grow with V.
-    None for workloads outside that N = H = 4096 family."""
-    captured_v, read_bytes, write_bytes = 32768, 0.304589e9, 7.469824e6
+    """DRAM bytes (read + write) per launch of the forward GEMM, from the full-size ncu
+    capture in profiles/tc_gemm_traffic_headline_and_16384_tokens.md (N = H = 4096,
+    V = 131072), scaled to this workload's V: the X bytes stay, the W bytes and the
+    per-tile partials grow with V.  None for workloads outside that N = H = 4096 family."""
+    captured_v, read_bytes, write_bytes = 131072, 1.107715840e9, 19.7056e6
     if wl.n != 4096 or wl.hidden != 4096:
         return None
     x_bytes = wl.n * wl.hidden * 2
