@@ -399,6 +399,41 @@ def time_fused_logits(step, steps, warmup, pg):
     return max_over_ranks(pg, s.elapsed_time(e)) / steps
 
 
+def time_forward_entropy(step, steps, warmup, pg):
+    """Mean ms of lce_forward without and with the per-token entropy output, each over
+    ``steps`` back-to-back calls (the entropy adds one multiply-add per logit and a
+    third partial per vocabulary tile)."""
+    import torch
+    wl = step.wl
+    stream = torch.cuda.current_stream()
+    ent = torch.empty(wl.n, dtype=torch.float32, device=step.lse.device)
+
+    def one(with_entropy):
+        step.vce.lce_forward(step.d["X"], step.d["W"], step.d["target"], wl.label_smoothing, wl.reduce_loss,
+                             loss=step.loss, lse=step.lse, n_valid=step.n_valid, workspace=step.ws,
+                             dev_status=step.status, entropy=ent if with_entropy else None)
+
+    out = {}
+    for with_entropy in (False, True, False, True):
+        for _ in range(warmup):
+            one(with_entropy)
+        torch.cuda.synchronize()
+        barrier(pg)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(steps):
+            one(with_entropy)
+        e.record(stream)
+        torch.cuda.synchronize()
+        barrier(pg)
+        ms = max_over_ranks(pg, s.elapsed_time(e)) / steps
+        key = "forward_with_entropy_ms" if with_entropy else "forward_ms"
+        out[key] = min(out.get(key, ms), ms)
+    out["overhead"] = out["forward_with_entropy_ms"] / out["forward_ms"] - 1.0
+    out["note"] = "best of two alternating loops of each, same workload"
+    return out
+
+
 def time_e2e_linear(step, steps, warmup, pg):
     """The same step through the public calls, inputs copied from pinned host memory each step."""
     import torch
@@ -738,6 +773,7 @@ def main():
         "gpu_launches": st.timed_launches,
         "clocks": clocks,
     }
+    line["entropy_cost"] = time_forward_entropy(st, max(3, args.steps // 3), 3, pg)
     line["config"]["peak_extra_memory_bytes"] = peak_extra_memory(st)
     if logits_obj is not None:
         line["logits_ce"] = logits_obj

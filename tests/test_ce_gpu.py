@@ -319,6 +319,35 @@ def test_fused_matches_oracle_and_separate_path(n, vocab, dtype, eps, red, inpla
     check_rows(r, r.dlogits, ref, ref_dz, np.arange(n), dtype, red, target)
 
 
+@pytest.mark.parametrize("n,vocab,pad,dtype,eps,red", [
+    (200, 50001, 3, "bf16", 0.1, True),   # 1024 threads per row, next-row prefetch, rows off 16-byte alignment
+    (150, 3001, 5, "f32", 0.0, False),    # 256 threads per row
+    (300, 129, 1, "bf16", 0.1, 2),        # 128 threads per row
+])
+def test_fused_padded_rows(n, vocab, pad, dtype, eps, red):
+    seed = 5 * n + vocab
+    stride = vocab + pad
+    full = wk.normal_matrix(seed, wk.TID_LOGITS, n, stride, 3.0, dtype == "bf16")
+    target = wk.uniform_targets(seed, n, vocab, 0.1)
+    grad = np.full(1, 0.5, np.float32) if red else wk.grad_rows(seed, n)
+    dev_full = to_dev(full, dtype)
+    sep_f, sep_dz = run_gpu(dev_full[:, :vocab], target, eps, red, grad,
+                            dlogits=torch.empty_like(dev_full)[:, :vocab])
+    dz_full = torch.full_like(dev_full, 7.0)
+    tgt = torch.from_numpy(target).to(DEV)
+    g = torch.from_numpy(np.asarray(grad, np.float32)).to(DEV)
+    r = vce.ce_forward_backward(dev_full[:, :vocab], tgt, g, eps, red, dlogits=dz_full[:, :vocab])
+    torch.cuda.synchronize()
+    assert torch.equal(r.stats, sep_f.stats) and torch.equal(r.loss, sep_f.loss)
+    view = (lambda t: t.view(torch.int16)) if dtype == "bf16" else (lambda t: t)
+    assert torch.equal(view(r.dlogits.contiguous()), view(sep_dz.contiguous()))
+    assert torch.all(dz_full[:, vocab:] == 7.0).item()
+    z = full[:, :vocab]
+    ref = oracle.ce_forward(z, target, eps, red, dtype=dtype)
+    ref_dz = oracle.ce_backward(z, target, ref["lse"], ref["n_valid"], grad, eps, red, dtype=dtype)
+    check_rows(r, r.dlogits, ref, ref_dz, np.arange(n), dtype, red, target)
+
+
 def test_fused_membound_full_size_inplace():
     wl = wk.LOGITS_MEMBOUND
     inp = wk.make_logits_inputs(wl)
