@@ -62,6 +62,22 @@ template <> struct Elem<__nv_bfloat16> {
     __device__ static void store1(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
 };
 
+// v[k] = g * exp2(v[k] * log2(e) + negl) - b for a vector of K (even) elements,
+// two lanes per FFMA2: each lane is the same IEEE fused multiply-add as fmaf.
+template <int K>
+__device__ __forceinline__ void grad_lanes(float (&v)[K], float g, float negl, float b) {
+    static_assert(K % 2 == 0, "pairs of lanes");
+    const float2 l2 = make_float2(kLog2e, kLog2e), nl = make_float2(negl, negl);
+    const float2 g2 = make_float2(g, g), nb = make_float2(-b, -b);
+#pragma unroll
+    for (int k = 0; k < K; k += 2) {
+        const float2 a = __ffma2_rn(make_float2(v[k], v[k + 1]), l2, nl);
+        const float2 d = __ffma2_rn(g2, make_float2(ex2f(a.x), ex2f(a.y)), nb);
+        v[k] = d.x;
+        v[k + 1] = d.y;
+    }
+}
+
 // Split of a row into a scalar head (up to the first 16-byte boundary), whole
 // 16-byte vectors and a scalar tail.
 template <typename T>
@@ -96,15 +112,34 @@ struct OnlineLse {
             m = vm;
             negm = -vm * kLog2e;
         }
-        float t = 0.f;
+        if constexpr (K % 2 == 0) {
+            // two lanes per instruction (FFMA2 / FADD2): exponent arguments and the
+            // running sums of even and odd elements
+            const float2 l2 = make_float2(kLog2e, kLog2e), nm = make_float2(negm, negm);
+            float2 t2 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < K; ++i) t += ex2f(fmaf(v[i], kLog2e, negm));
-        s += t;
-        if (kSum) {
-            float u = 0.f;
+            for (int i = 0; i < K; i += 2) {
+                const float2 a = __ffma2_rn(make_float2(v[i], v[i + 1]), l2, nm);
+                t2 = __fadd2_rn(t2, make_float2(ex2f(a.x), ex2f(a.y)));
+            }
+            s += t2.x + t2.y;
+            if (kSum) {
+                float2 u2 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int i = 0; i < K; ++i) u += v[i];
-            sum += u;
+                for (int i = 0; i < K; i += 2) u2 = __fadd2_rn(u2, make_float2(v[i], v[i + 1]));
+                sum += u2.x + u2.y;
+            }
+        } else {
+            float t = 0.f;
+#pragma unroll
+            for (int i = 0; i < K; ++i) t += ex2f(fmaf(v[i], kLog2e, negm));
+            s += t;
+            if (kSum) {
+                float u = 0.f;
+#pragma unroll
+                for (int i = 0; i < K; ++i) u += v[i];
+                sum += u;
+            }
         }
     }
 
@@ -262,8 +297,7 @@ ce_backward_rows(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride,
         auto gradv = [&](const uint4& raw, int64_t i) {
             float v[V];
             E::unpack(raw, v);
-#pragma unroll
-            for (int k = 0; k < V; ++k) v[k] = fmaf(g, ex2f(fmaf(v[k], kLog2e, negl)), -b);
+            grad_lanes<V>(v, g, negl, b);
             const int64_t base = sp.head + i * V;
             if (uint64_t(y - base) < uint64_t(V)) {
 #pragma unroll
@@ -531,6 +565,8 @@ ce_fused_rows(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
         auto gradv = [&](const uint4& raw, int64_t i) {
             float v[V];
             E::unpack(raw, v);
+            // scalar FMAs here (the same per-lane arithmetic as grad_lanes, so the same
+            // bits as ce_backward_rows): the pair form costs this 64-register kernel a spill
 #pragma unroll
             for (int k = 0; k < V; ++k) v[k] = fmaf(g, ex2f(fmaf(v[k], kLog2e, negl)), -b);
             const int64_t base = sp.head + i * V;
