@@ -67,9 +67,9 @@ def FWD_GEMM_TRAFFIC_BYTES(wl):
 # captures in profiles/ce_rows_logits_2048x128256.md and
 # profiles/ce_fused_rows_logits_2048x128256.md (2048 rows of V = 128256 BF16, 5% ignored)
 LOGITS_CAPTURED_TRAFFIC = {
-    "forward": (502.304768e6, 2.953984e6),
-    "backward": (502.335488e6, 467.678208e6),
-    "fused": (525.410304e6, 467.438848e6),
+    "forward": (502.361088e6, 3.546112e6),
+    "backward": (502.321664e6, 467.872e6),
+    "fused": (526.883072e6, 466.792192e6),
 }
 
 
