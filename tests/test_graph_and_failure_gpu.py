@@ -68,6 +68,42 @@ def test_all_entry_points_replay_in_a_cuda_graph():
     assert int(status.item()) == 0
 
 
+def test_concurrent_streams_match_sequential():
+    # Two linear-form forward + backward calls with separate workspaces on two
+    # streams at once: each GEMM takes its work units from the counter in its own
+    # workspace, so the results equal those of running the calls one after another.
+    n, h, v = 2048, 512, 9000
+    cases = []
+    for seed in (5, 6):
+        x = _bf16(wk.normal_matrix(seed, wk.TID_X, n, h, 1.0, True))
+        w = _bf16(wk.normal_matrix(seed, wk.TID_W, v, h, h ** -0.5, True))
+        y = torch.from_numpy(wk.uniform_targets(seed, n, v, 0.05)).to(DEV)
+        cases.append((x, w, y))
+    g = torch.ones(1, device=DEV)
+
+    def run(stream, x, w, y):
+        with torch.cuda.stream(stream):
+            ws = torch.empty(vce.lce_workspace_size(n, h, v, True, 8 << 20), dtype=torch.uint8, device=DEV)
+            f = vce.lce_forward(x, w, y, 0.1, True, workspace=ws)
+            b = vce.lce_backward(x, w, y, f.lse, f.n_valid, g, 0.1, True, workspace=ws)
+        return f, b
+
+    main = torch.cuda.current_stream()
+    seq = [run(main, *c) for c in cases]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for st in streams:
+        st.wait_stream(main)
+    for _ in range(3):
+        par = [run(st, *c) for st, c in zip(streams, cases)]
+        torch.cuda.synchronize()
+        for (fs, bs), (fp, bp) in zip(seq, par):
+            assert torch.equal(fs.loss, fp.loss) and torch.equal(fs.lse, fp.lse)
+            assert torch.equal(bs.dX.view(torch.int16), bp.dX.view(torch.int16))
+            assert torch.equal(bs.dW.view(torch.int16), bp.dW.view(torch.int16))
+            assert int(fp.dev_status.item()) == 0 and int(bp.dev_status.item()) == 0
+
+
 @pytest.mark.parametrize("timeout_ns", [1000, 2_000_000])
 def test_bounded_wait_times_out_and_reports(timeout_ns):
     lib = vce.library()
