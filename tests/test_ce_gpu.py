@@ -293,6 +293,9 @@ FUSED = [
     # several rows per persistent CTA: next-row L2 prefetch on (bf16) and off (f32, rows too large)
     (500, 65536, "bf16", 0.0, 2, True),
     (400, 131072, "f32", 0.1, True, False),
+    # several rows per CTA with the prefetch on the 256- and 128-thread paths
+    (1000, 20000, "bf16", 0.1, True, False),
+    (3000, 1000, "bf16", 0.0, 2, True),
 ]
 
 
@@ -321,7 +324,7 @@ def test_fused_matches_oracle_and_separate_path(n, vocab, dtype, eps, red, inpla
 
 @pytest.mark.parametrize("n,vocab,pad,dtype,eps,red", [
     (200, 50001, 3, "bf16", 0.1, True),   # 1024 threads per row, next-row prefetch, rows off 16-byte alignment
-    (150, 3001, 5, "f32", 0.0, False),    # 256 threads per row
+    (150, 9001, 5, "f32", 0.0, False),    # 256 threads per row
     (300, 129, 1, "bf16", 0.1, 2),        # 128 threads per row
 ])
 def test_fused_padded_rows(n, vocab, pad, dtype, eps, red):

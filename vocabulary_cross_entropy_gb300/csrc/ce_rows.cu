@@ -621,31 +621,30 @@ void fused_dispatch(const void* logits, int64_t n_rows, int64_t vocab, int64_t s
                     int reduce_loss, float* loss_rows, float* stats, void* dlogits, int* dev_status,
                     cudaStream_t s, const DeviceInfo& dev) {
     // Same threads per row as the forward kernel (identical summation order).
+    // The next-row prefetch doubles the rows resident in L2; it pays while both
+    // rows of every CTA take at most two thirds of L2, and thrashes it beyond
+    // (measured: 16-256 KiB rows gain 2-13%, 400-500 KiB rows lose 5-25%).
     const int64_t nvec = vocab / Elem<T>::kVec;
+    auto fits = [&](int grid) {
+        return 2.0 * double(grid) * double(vocab) * double(sizeof(T)) <= double(dev.l2_bytes) * 2.0 / 3.0;
+    };
+#define VCE_FUSED_ARGS logits, n_rows, vocab, stride, target, eps, ignore_idx, n_valid, grad_output, reduce_loss, \
+                       loss_rows, stats, dlogits, dev_status, s
     if (nvec <= 1024) {
-        fused_launch<T, 128, 8, 4, 2, false>(logits, n_rows, vocab, stride, target, eps, ignore_idx, n_valid,
-                                             grad_output, reduce_loss, loss_rows, stats, dlogits, dev_status, s,
-                                             fused_grid(n_rows, dev.num_sms, 8));
-        return;
+        const int grid = fused_grid(n_rows, dev.num_sms, 8);
+        if (fits(grid)) fused_launch<T, 128, 8, 4, 2, true>(VCE_FUSED_ARGS, grid);
+        else fused_launch<T, 128, 8, 4, 2, false>(VCE_FUSED_ARGS, grid);
+    } else if (nvec <= 4096) {
+        const int grid = fused_grid(n_rows, dev.num_sms, 2);
+        if (fits(grid)) fused_launch<T, 256, 2, 4, 2, true>(VCE_FUSED_ARGS, grid);
+        else fused_launch<T, 256, 4, 4, 2, false>(VCE_FUSED_ARGS, fused_grid(n_rows, dev.num_sms, 4));
+    } else {
+        // long rows: one 1024-thread CTA per SM
+        const int grid = fused_grid(n_rows, dev.num_sms, 1);
+        if (fits(grid)) fused_launch<T, 1024, 1, 4, 4, true>(VCE_FUSED_ARGS, grid);
+        else fused_launch<T, 1024, 1, 4, 4, false>(VCE_FUSED_ARGS, grid);
     }
-    if (nvec <= 4096) {
-        fused_launch<T, 256, 4, 4, 2, false>(logits, n_rows, vocab, stride, target, eps, ignore_idx, n_valid,
-                                             grad_output, reduce_loss, loss_rows, stats, dlogits, dev_status, s,
-                                             fused_grid(n_rows, dev.num_sms, 4));
-        return;
-    }
-    // Long rows: one 1024-thread CTA per SM.  The next-row prefetch doubles the
-    // rows resident in L2; it pays while both rows of every CTA take at most
-    // two thirds of L2, and thrashes it beyond (measured: 256 KiB rows gain 10%,
-    // 400-500 KiB rows lose 5-25%).
-    const int grid = fused_grid(n_rows, dev.num_sms, 1);
-    const double resident = 2.0 * double(grid) * double(vocab) * double(sizeof(T));
-    if (resident <= double(dev.l2_bytes) * 2.0 / 3.0)
-        fused_launch<T, 1024, 1, 4, 4, true>(logits, n_rows, vocab, stride, target, eps, ignore_idx, n_valid,
-                                             grad_output, reduce_loss, loss_rows, stats, dlogits, dev_status, s, grid);
-    else
-        fused_launch<T, 1024, 1, 4, 4, false>(logits, n_rows, vocab, stride, target, eps, ignore_idx, n_valid,
-                                              grad_output, reduce_loss, loss_rows, stats, dlogits, dev_status, s, grid);
+#undef VCE_FUSED_ARGS
 }
 
 int row_grid(int64_t n_rows) {
