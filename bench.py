@@ -285,8 +285,9 @@ class LogitsStep:
         self.vce = vce
         self.wl = wl
         inp = wk.make_logits_inputs(wl)
-        self.host = dict(logits=torch.from_numpy(inp.logits.view(np.int16)).view(torch.bfloat16),
-                         target=torch.from_numpy(inp.target), grad=torch.from_numpy(inp.grad))
+        logits = (torch.from_numpy(inp.logits.view(np.int16)).view(torch.bfloat16) if wl.dtype == "bf16"
+                  else torch.from_numpy(inp.logits))
+        self.host = dict(logits=logits, target=torch.from_numpy(inp.target), grad=torch.from_numpy(inp.grad))
         del inp
         self.d = {k: v.to(dev) for k, v in self.host.items()}
         n, v = wl.n_rows, wl.vocab
@@ -312,10 +313,11 @@ class LogitsStep:
                              dev_status=self.status)
 
     def bytes_fwd(self):
-        return float(self.n_valid_count) * self.wl.vocab * 2
+        return float(self.n_valid_count) * self.wl.vocab * self.d["logits"].element_size()
 
     def bytes_bwd(self):
-        return float(self.n_valid_count) * self.wl.vocab * 2 + float(self.wl.n_rows) * self.wl.vocab * 2
+        es = self.d["logits"].element_size()
+        return float(self.n_valid_count) * self.wl.vocab * es + float(self.wl.n_rows) * self.wl.vocab * es
 
     def units(self):
         return (self.bytes_fwd() + self.bytes_bwd()) / 1e9  # GB per step
@@ -798,6 +800,29 @@ def main():
             "clocks": ckb.summary(),
         }
         del big
+    if args.large and lin is wk.LINEAR_HEADLINE:
+        # the two small configurations: the tiny FP32 logits case (launch latency)
+        # and the 4096 x 2048 x 32000 linear case (per-token loss, 2% ignored)
+        torch.cuda.empty_cache()
+        tiny = LogitsStep(wk.LOGITS_TINY[3], dev)
+        kt = 100
+        tt, pht = time_steps(tiny, kt, args.warmup, pg)
+        assert int(tiny.status.item()) == 0, "device status reported an error"
+        sm = LinearStep(wk.LINEAR_SMALL, dev)
+        ks = max(3, args.steps // 3)
+        with Clocks(local) as ckm:
+            tsm, phm = time_steps(sm, ks, args.warmup, pg)
+        assert int(sm.status.item()) == 0, "device status reported an error"
+        line["small_configs"] = {
+            "logits_tiny": {"workload": tiny.wl.name, "n_rows": tiny.wl.n_rows, "vocab": tiny.wl.vocab,
+                            "dtype": "f32", "us_per_step": 1e3 * tt / kt, "fwd_us": 1e3 * pht["forward"],
+                            "bwd_us": 1e3 * pht["backward"], "steps": kt,
+                            "note": "ce_forward (+ mean) + ce_backward; launch-latency bound"},
+            "linear_small": {"workload": sm.wl.name, "value": sm.units() * world * ks / (tsm / 1e3),
+                             "unit": "TFLOP/s", "ms_per_step": tsm / ks, "fwd_ms": phm["forward"],
+                             "bwd_ms": phm["backward"], "steps": ks, "clocks": ckm.summary()},
+        }
+        del tiny, sm
     if args.sweep and lin is wk.LINEAR_HEADLINE:
         torch.cuda.empty_cache()
         line["sweep"] = []
