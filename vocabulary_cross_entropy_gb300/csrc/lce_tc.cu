@@ -16,12 +16,12 @@
 //             FP32 running sum of dX across vocabulary slabs.
 //
 // Kernel shape: CTA pairs (clusters of 2) on tcgen05's cta_group::2 path.  A
-// pair computes a 256 x BN output tile (BN = 256, or 128 for the dX GEMM whose
-// output is small): each CTA stages its 128 rows of A and its BN/2 rows of B
-// per 64-wide K step, the even CTA issues UMMA M=256, N=BN, K=16 over both
-// CTAs' shared memory, and each CTA's tensor memory receives its 128 output
-// rows.  The pair halves the B bytes every SM stages and reads, which buys a
-// deeper ring (6 stages of 32 KiB, 8 of 24 KiB) in the same shared memory.
+// pair computes a 256 x BN output tile (BN = 256 for every product here; the
+// template also builds BN = 128): each CTA stages its 128 rows of A and its
+// BN/2 rows of B per 64-wide K step, the even CTA issues UMMA M=256, N=BN,
+// K=16 over both CTAs' shared memory, and each CTA's tensor memory receives its
+// 128 output rows.  The pair halves the B bytes every SM stages and reads,
+// which buys a deeper ring (6 stages of 32 KiB) in the same shared memory.
 // Persistent: one pair per two SMs; two FP32 accumulators in tensor memory so
 // the epilogue of one tile overlaps the main loop of the next.  Tiles are handed
 // out in order from a global ticket counter, so the tiles in progress at any
