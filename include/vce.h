@@ -166,9 +166,12 @@ vce_status ce_backward(const void* logits, int dtype, int64_t n_rows, int64_t vo
  * two reads and one write.
  *
  *   Arguments are those of ce_forward and ce_backward combined; the results are
- *   the same as ce_forward followed by ce_backward with the same grad_output
- *   (loss, stats, n_valid, dlogits).  dlogits MAY EQUAL logits (in place), with
- *   the same 16-byte offset rule as ce_backward.
+ *   those of ce_forward followed by ce_backward with the same grad_output (loss,
+ *   stats, n_valid, dlogits): bit for bit for rows of up to about 100 KiB, which
+ *   both calls sum with the same threads per row; for longer rows this call
+ *   splits a row's sum differently, so lse and the loss agree to FP32 rounding
+ *   (row maxima, n_valid and ignored rows exactly).  dlogits MAY EQUAL logits
+ *   (in place), with the same 16-byte offset rule as ce_backward.
  *   grad_output F32 [1] when reduce_loss != 0, else [n_rows].
  *   ws/ws_bytes: ce_workspace_size(n_rows, vocab, reduce_loss) bytes.
  */

@@ -278,6 +278,27 @@ def run_fused(logits, target, eps, red, grad, ignore_idx=-100, inplace=False):
     return r
 
 
+def assert_fused_matches_separate(r, sep_f, sep_dz, target, dtype):
+    """The fused call against ce_forward + ce_backward on the same data.  Where
+    both use the same threads per row the results are bit-identical; for long
+    rows the fused kernel may split a row's sum differently, so lse and the loss
+    may differ by FP32 rounding, and the gradient by what that does to
+    exp(z - lse) - eps/V (tensor-wise; single elements near p = eps/V cancel).
+    Counts, row maxima and ignored rows are exact either way."""
+    assert int(r.n_valid.item()) == int(sep_f.n_valid.item())
+    st, ss = r.stats.double().cpu().numpy(), sep_f.stats.double().cpu().numpy()
+    np.testing.assert_array_equal(st[:, 0], ss[:, 0])
+    np.testing.assert_allclose(st[:, 1], ss[:, 1], rtol=2e-6, atol=1e-6)
+    lf, ls = r.loss.double().cpu().numpy().reshape(-1), sep_f.loss.double().cpu().numpy().reshape(-1)
+    np.testing.assert_allclose(lf, ls, rtol=2e-6, atol=2e-6)
+    a = r.dlogits.float().cpu().numpy()
+    b = sep_dz.float().cpu().numpy()
+    ign = target == -100
+    assert np.all(a[ign] == 0.0) and np.all(b[ign] == 0.0)
+    tol = 1e-3 if dtype == "bf16" else 1e-5
+    assert np.linalg.norm(a - b) <= tol * np.linalg.norm(b) + 1e-30
+
+
 FUSED = [
     # n, vocab, dtype, eps, reduce, inplace
     (128, 1024, "f32", 0.0, False, False),
@@ -311,12 +332,7 @@ def test_fused_matches_oracle_and_separate_path(n, vocab, dtype, eps, red, inpla
     r = run_fused(b, target, eps, red, grad, inplace=inplace)
     if inplace:
         assert r.dlogits.data_ptr() == b.data_ptr()
-    # same arithmetic in the same order as ce_forward + ce_backward: bit-identical results
-    assert torch.equal(r.stats, sep_f.stats)
-    assert torch.equal(r.loss, sep_f.loss)
-    assert int(r.n_valid.item()) == int(sep_f.n_valid.item())
-    assert torch.equal(r.dlogits.view(torch.int16) if dtype == "bf16" else r.dlogits,
-                       sep_dz.view(torch.int16) if dtype == "bf16" else sep_dz)
+    assert_fused_matches_separate(r, sep_f, sep_dz, target, dtype)
     ref = oracle.ce_forward(z, target, eps, red, dtype=dtype)
     ref_dz = oracle.ce_backward(z, target, ref["lse"], ref["n_valid"], grad, eps, red, dtype=dtype)
     check_rows(r, r.dlogits, ref, ref_dz, np.arange(n), dtype, red, target)
@@ -341,9 +357,7 @@ def test_fused_padded_rows(n, vocab, pad, dtype, eps, red):
     g = torch.from_numpy(np.asarray(grad, np.float32)).to(DEV)
     r = vce.ce_forward_backward(dev_full[:, :vocab], tgt, g, eps, red, dlogits=dz_full[:, :vocab])
     torch.cuda.synchronize()
-    assert torch.equal(r.stats, sep_f.stats) and torch.equal(r.loss, sep_f.loss)
-    view = (lambda t: t.view(torch.int16)) if dtype == "bf16" else (lambda t: t)
-    assert torch.equal(view(r.dlogits.contiguous()), view(sep_dz.contiguous()))
+    assert_fused_matches_separate(r, sep_f, sep_dz, target, dtype)
     assert torch.all(dz_full[:, vocab:] == 7.0).item()
     z = full[:, :vocab]
     ref = oracle.ce_forward(z, target, eps, red, dtype=dtype)

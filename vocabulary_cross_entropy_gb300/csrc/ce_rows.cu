@@ -394,17 +394,17 @@ template <typename T>
 void fwd_dispatch(const void* logits, int64_t n_rows, int64_t vocab, int64_t stride,
                   const int64_t* target, float eps, int64_t ignore_idx, float* loss_rows,
                   float* stats, int* dev_status, cudaStream_t s, int grid) {
-    // The thread count per row fixes the summation order, so it is the same as the
-    // fused kernel's for every row length (fused results equal forward + backward
-    // bit for bit).  Long rows: two 1024-thread CTAs per SM (32 registers).
-    // MINB 0 leaves the register budget to the compiler.
+    // One CTA per row, threads by row length (MINB 0 leaves the register budget
+    // to the compiler).  512 threads were measured faster than 1024 for every
+    // row above 4096 vectors (0.24 against 0.31 ms at 16384 x 50257 BF16, 0.56
+    // against 0.58 ms at 16384 x 128256).
     const int64_t nvec = vocab / Elem<T>::kVec;
     if (nvec <= 1024)
         fwd_launch<T, 128, 0>(logits, n_rows, vocab, stride, target, eps, ignore_idx, loss_rows, stats, dev_status, s, grid);
     else if (nvec <= 4096)
         fwd_launch<T, 256, 0>(logits, n_rows, vocab, stride, target, eps, ignore_idx, loss_rows, stats, dev_status, s, grid);
     else
-        fwd_launch<T, 1024, 2>(logits, n_rows, vocab, stride, target, eps, ignore_idx, loss_rows, stats, dev_status, s, grid);
+        fwd_launch<T, 512, 0>(logits, n_rows, vocab, stride, target, eps, ignore_idx, loss_rows, stats, dev_status, s, grid);
 }
 
 template <typename T>
@@ -620,29 +620,36 @@ void fused_dispatch(const void* logits, int64_t n_rows, int64_t vocab, int64_t s
                     float eps, int64_t ignore_idx, const int64_t* n_valid, const float* grad_output,
                     int reduce_loss, float* loss_rows, float* stats, void* dlogits, int* dev_status,
                     cudaStream_t s, const DeviceInfo& dev) {
-    // Same threads per row as the forward kernel (identical summation order).
     // The next-row prefetch doubles the rows resident in L2; it pays while both
-    // rows of every CTA take at most two thirds of L2, and thrashes it beyond
-    // (measured: 16-256 KiB rows gain 2-13%, 400-500 KiB rows lose 5-25%).
+    // rows of every CTA leave most of L2 free and thrashes it beyond.  Rows up to
+    // 4096 vectors and rows up to ~100 KiB use the forward kernel's threads per
+    // row, so there the results equal ce_forward + ce_backward bit for bit;
+    // longer rows run fastest with one 1024-thread CTA per SM (measured at
+    // 16384 rows: 50257 BF16 0.57 ms with 2 x 512 + prefetch against 0.76 ms with
+    // 1024; 128256 BF16 1.42 ms with 1024 + prefetch against 1.57 ms with 2 x 512).
     const int64_t nvec = vocab / Elem<T>::kVec;
-    auto fits = [&](int grid) {
-        return 2.0 * double(grid) * double(vocab) * double(sizeof(T)) <= double(dev.l2_bytes) * 2.0 / 3.0;
-    };
+    const double l2 = double(dev.l2_bytes), row = double(vocab) * double(sizeof(T));
+    auto resident = [&](int grid, int rows_per_cta) { return double(grid) * rows_per_cta * row; };
 #define VCE_FUSED_ARGS logits, n_rows, vocab, stride, target, eps, ignore_idx, n_valid, grad_output, reduce_loss, \
                        loss_rows, stats, dlogits, dev_status, s
     if (nvec <= 1024) {
         const int grid = fused_grid(n_rows, dev.num_sms, 8);
-        if (fits(grid)) fused_launch<T, 128, 8, 4, 2, true>(VCE_FUSED_ARGS, grid);
+        if (resident(grid, 2) <= l2 * 2.0 / 3.0) fused_launch<T, 128, 8, 4, 2, true>(VCE_FUSED_ARGS, grid);
         else fused_launch<T, 128, 8, 4, 2, false>(VCE_FUSED_ARGS, grid);
     } else if (nvec <= 4096) {
         const int grid = fused_grid(n_rows, dev.num_sms, 2);
-        if (fits(grid)) fused_launch<T, 256, 2, 4, 2, true>(VCE_FUSED_ARGS, grid);
+        if (resident(grid, 2) <= l2 * 2.0 / 3.0) fused_launch<T, 256, 2, 4, 2, true>(VCE_FUSED_ARGS, grid);
         else fused_launch<T, 256, 4, 4, 2, false>(VCE_FUSED_ARGS, fused_grid(n_rows, dev.num_sms, 4));
     } else {
-        // long rows: one 1024-thread CTA per SM
-        const int grid = fused_grid(n_rows, dev.num_sms, 1);
-        if (fits(grid)) fused_launch<T, 1024, 1, 4, 4, true>(VCE_FUSED_ARGS, grid);
-        else fused_launch<T, 1024, 1, 4, 4, false>(VCE_FUSED_ARGS, grid);
+        const int g512 = fused_grid(n_rows, dev.num_sms, 2), g1024 = fused_grid(n_rows, dev.num_sms, 1);
+        if (resident(g512, 2) <= l2 * 0.47)        // up to ~100 KiB rows: 2 x 512 threads, prefetch
+            fused_launch<T, 512, 2, 4, 2, true>(VCE_FUSED_ARGS, g512);
+        else if (resident(g512, 1) <= l2 * 0.35)   // up to ~150 KiB rows: 2 x 512 threads
+            fused_launch<T, 512, 2, 4, 2, false>(VCE_FUSED_ARGS, g512);
+        else if (resident(g1024, 2) <= l2 * 2.0 / 3.0)  // up to ~300 KiB rows: 1024 threads, prefetch
+            fused_launch<T, 1024, 1, 4, 4, true>(VCE_FUSED_ARGS, g1024);
+        else
+            fused_launch<T, 1024, 1, 4, 4, false>(VCE_FUSED_ARGS, g1024);
     }
 #undef VCE_FUSED_ARGS
 }
