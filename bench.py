@@ -67,8 +67,8 @@ def FWD_GEMM_TRAFFIC_BYTES(wl):
 # captures in profiles/ce_rows_logits_2048x128256.md and
 # profiles/ce_fused_rows_logits_2048x128256.md (2048 rows of V = 128256 BF16, 5% ignored)
 LOGITS_CAPTURED_TRAFFIC = {
-    "forward": (502.361088e6, 3.546112e6),
-    "backward": (502.321664e6, 467.872e6),
+    "forward": (502.399488e6, 3.231744e6),
+    "backward": (502.3232e6, 467.8656e6),
     "fused": (526.883072e6, 466.792192e6),
 }
 
