@@ -401,6 +401,65 @@ def time_fused_logits(step, steps, warmup, pg):
     return max_over_ranks(pg, s.elapsed_time(e)) / steps
 
 
+# vocabularies of common models (BF16 logits, 16384 rows; 8192 rows above 150K)
+VOCAB_SWEEP = (32000, 32768, 50257, 65536, 100352, 128256, 151936, 202048, 256000)
+
+
+def vocab_sweep(dev, args, pg, pk):
+    """ce_forward, ce_backward and ce_forward_backward over common vocabulary sizes:
+    BF16 logits ~ N(0, 9) drawn on the device from a seeded generator, 5% ignored
+    rows, eps = 0.1, mean reduction.  GB/s counts the algorithmic bytes."""
+    import torch
+    import vocabulary_cross_entropy_gb300 as vce
+    out = []
+    for v in VOCAB_SWEEP:
+        n = 16384 if v <= 150000 else 8192
+        g = torch.Generator(device=dev).manual_seed(v)
+        z = (torch.randn(n, v, device=dev, generator=g) * 3).to(torch.bfloat16)
+        t = torch.randint(0, v, (n,), device=dev, generator=g)
+        t[torch.rand(n, device=dev, generator=g) < 0.05] = wk.IGNORE_IDX
+        dz = torch.empty_like(z)
+        grad = torch.ones(1, device=dev)
+        loss, stats = torch.empty(1, device=dev), torch.empty(n, 2, device=dev)
+        nv = torch.empty(1, dtype=torch.int64, device=dev)
+        ws = torch.empty(vce.ce_workspace_size(n, v, True), dtype=torch.uint8, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        calls = {
+            "forward": lambda: vce.ce_forward(z, t, 0.1, True, loss=loss, stats=stats, n_valid=nv, workspace=ws,
+                                              dev_status=status),
+            "backward": lambda: vce.ce_backward(z, t, stats, nv, grad, 0.1, True, dlogits=dz, dev_status=status),
+            "fused": lambda: vce.ce_forward_backward(z, t, grad, 0.1, True, dlogits=dz, loss=loss, stats=stats,
+                                                     n_valid=nv, workspace=ws, dev_status=status),
+        }
+        calls["forward"]()
+        torch.cuda.synchronize()
+        n_valid = int(nv.item())
+        read, write = float(n_valid) * v * 2, float(n) * v * 2
+        nbytes = {"forward": read, "backward": read + write, "fused": read + write}
+        row = {"vocab": v, "n_rows": n}
+        stream = torch.cuda.current_stream()
+        for name, fn in calls.items():
+            for _ in range(args.warmup):
+                fn()
+            torch.cuda.synchronize()
+            barrier(pg)
+            s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            k = 20
+            s_.record(stream)
+            for _ in range(k):
+                fn()
+            e_.record(stream)
+            torch.cuda.synchronize()
+            ms = max_over_ranks(pg, s_.elapsed_time(e_)) / k
+            row[name + "_ms"] = ms
+            row[name + "_frac_hbm"] = nbytes[name] / (ms / 1e3) / 1e9 / pk["hbm"]
+        assert int(status.item()) == 0, "device status reported an error"
+        out.append(row)
+        del z, dz, t
+        torch.cuda.empty_cache()
+    return out
+
+
 def time_forward_entropy(step, steps, warmup, pg):
     """Mean ms of lce_forward without and with the per-token entropy output, each over
     ``steps`` back-to-back calls (the entropy adds one multiply-add per logit and a
@@ -641,6 +700,8 @@ def main():
     ap.add_argument("--workload", default="both", choices=["linear", "logits", "both"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
+    ap.add_argument("--vocab-sweep", action="store_true",
+                    help="also time the logits form (forward, backward, fused) over common vocabulary sizes")
     ap.add_argument("--sweep", action="store_true",
                     help="also time the model-shape sweep (Qwen3-30B-A3B, Llama 4, DeepSeek-V3 heads at M=8192)")
     ap.add_argument("--no-large", dest="large", action="store_false",
@@ -840,6 +901,9 @@ def main():
                 "workspace_bytes": stp.ws_bytes, "clocks": cks.summary()})
             del stp
             torch.cuda.empty_cache()
+    if args.vocab_sweep and lin is wk.LINEAR_HEADLINE:
+        torch.cuda.empty_cache()
+        line["vocab_sweep"] = vocab_sweep(dev, args, pg, pk)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_linear(lin)
     if rank == 0:

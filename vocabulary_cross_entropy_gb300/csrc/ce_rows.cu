@@ -330,12 +330,33 @@ mean_loss_kernel(const float* __restrict__ loss_rows, const int64_t* __restrict_
                  int64_t* __restrict__ n_valid) {
     __shared__ double sm_s[32];
     __shared__ long long sm_c[32];
-    double s = 0.0;
-    long long c = 0;
-    for (int64_t i = threadIdx.x; i < n; i += kMeanThreads) {
-        if (loss_rows) s += double(loss_rows[i]);
-        c += (target[i] != ignore_idx) ? 1 : 0;
+    // Each thread adds its rows eight at a time (a small FP32 tree per batch of
+    // loads) into a running FP32 sum with Neumaier compensation (the rounding
+    // error each addition dropped is kept and added back), which keeps it within
+    // FP32 rounding of the exact total; only the 1024 per-thread results are
+    // widened to FP64 for the block reduction.  FP64 arithmetic runs at a small
+    // fraction of the FP32 rate on this GPU: converting and adding every row in
+    // FP64 took 14 us for 16384 rows and 585 us for 1M rows.
+    float fs = 0.f, fc = 0.f;
+    int ci = 0;  // this thread's count (at most n / 1024 + 8)
+    constexpr int U = 8;  // loads in flight per thread, summed as a small tree
+    for (int64_t i0 = threadIdx.x; i0 < n; i0 += int64_t(kMeanThreads) * U) {
+        float l[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t i = i0 + int64_t(u) * kMeanThreads;
+            const bool in = i < n;
+            ci += (in && target[i] != ignore_idx) ? 1 : 0;
+            l[u] = (in && loss_rows) ? loss_rows[i] : 0.f;
+        }
+        const float b = ((l[0] + l[1]) + (l[2] + l[3])) + ((l[4] + l[5]) + (l[6] + l[7]));
+        const float t = fs + b;
+        if (isfinite(t))  // an infinite or NaN loss propagates through fs alone
+            fc += fabsf(fs) >= fabsf(b) ? (fs - t) + b : (b - t) + fs;
+        fs = t;
     }
+    double s = double(fs) + double(fc);
+    long long c = ci;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
         s += __shfl_xor_sync(0xffffffffu, s, off);
