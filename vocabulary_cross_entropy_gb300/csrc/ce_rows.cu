@@ -667,7 +667,7 @@ void fused_dispatch(const void* logits, int64_t n_rows, int64_t vocab, int64_t s
             fused_launch<T, 512, 2, 4, 2, true>(VCE_FUSED_ARGS, g512);
         else if (resident(g512, 1) <= l2 * 0.35)   // up to ~150 KiB rows: 2 x 512 threads
             fused_launch<T, 512, 2, 4, 2, false>(VCE_FUSED_ARGS, g512);
-        else if (resident(g1024, 2) <= l2 * 2.0 / 3.0)  // up to ~300 KiB rows: 1024 threads, prefetch
+        else if (resident(g1024, 2) <= l2 * 0.70)  // up to ~310 KiB rows: 1024 threads, prefetch
             fused_launch<T, 1024, 1, 4, 4, true>(VCE_FUSED_ARGS, g1024);
         else
             fused_launch<T, 1024, 1, 4, 4, false>(VCE_FUSED_ARGS, g1024);
