@@ -528,18 +528,23 @@ def time_e2e_linear(step, steps, warmup, pg):
 def time_e2e_linear_pipelined(step, steps, warmup, pg):
     """End to end with the host copies overlapped: while step i computes, step i+1's
     inputs are copied from pinned host memory on a second stream into the other of two
-    device input buffers (the usual prefetch of a training loop).  Every step still
-    copies all of its inputs and reads its loss back; the timed region runs from before
-    the first copy to after the last loss read."""
+    device input buffers (the usual prefetch of a training loop), and step i's loss is
+    read back on a third stream, so that the 4-byte read never waits on the compute
+    stream behind a copy engine that is busy with the next step's inputs (two loss
+    buffers by step parity keep a step from overwriting a loss still being read).
+    Every step still copies all of its inputs and reads its loss back; the timed region
+    runs from before the first copy to after the last loss read."""
     import torch
     vce, wl = step.vce, step.wl
     comp = torch.cuda.current_stream()
-    copy_stream = torch.cuda.Stream()
+    copy_stream, read_stream = torch.cuda.Stream(), torch.cuda.Stream()
     pinned = {k: v.pin_memory() for k, v in step.host.items()}
     bufs = [step.d, {k: torch.empty_like(v) for k, v in step.d.items()}]
+    losses = [step.loss, torch.empty_like(step.loss)]
     ready = [torch.cuda.Event(), torch.cuda.Event()]
     done = [torch.cuda.Event(), torch.cuda.Event()]
-    loss_host = torch.empty_like(step.loss, device="cpu").pin_memory()
+    read = [torch.cuda.Event(), torch.cuda.Event()]
+    loss_host = [torch.empty_like(step.loss, device="cpu").pin_memory() for _ in range(2)]
 
     def copy_into(b):
         with torch.cuda.stream(copy_stream):
@@ -551,12 +556,16 @@ def time_e2e_linear_pipelined(step, steps, warmup, pg):
     def compute(b):
         d = bufs[b]
         comp.wait_event(ready[b])
-        vce.lce_forward(d["X"], d["W"], d["target"], wl.label_smoothing, wl.reduce_loss, loss=step.loss,
+        comp.wait_event(read[b])  # the loss buffer's previous read has finished
+        vce.lce_forward(d["X"], d["W"], d["target"], wl.label_smoothing, wl.reduce_loss, loss=losses[b],
                         lse=step.lse, n_valid=step.n_valid, workspace=step.ws, dev_status=step.status)
         vce.lce_backward(d["X"], d["W"], d["target"], step.lse, step.n_valid, d["grad"], wl.label_smoothing,
                          wl.reduce_loss, dX=step.dX, dW=step.dW, workspace=step.ws, dev_status=step.status)
-        loss_host.copy_(step.loss, non_blocking=True)
         done[b].record(comp)
+        with torch.cuda.stream(read_stream):
+            read_stream.wait_event(done[b])
+            loss_host[b].copy_(losses[b], non_blocking=True)
+            read[b].record(read_stream)
 
     def run(n):
         copy_into(0)
@@ -564,6 +573,7 @@ def time_e2e_linear_pipelined(step, steps, warmup, pg):
             if i + 1 < n:
                 copy_into((i + 1) % 2)
             compute(i % 2)
+        comp.wait_stream(read_stream)  # every loss read is inside the region
 
     run(warmup)
     torch.cuda.synchronize()
@@ -571,6 +581,7 @@ def time_e2e_linear_pipelined(step, steps, warmup, pg):
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s.record(comp)
     copy_stream.wait_event(s)
+    read_stream.wait_event(s)
     run(steps)
     e.record(comp)
     torch.cuda.synchronize()
@@ -803,7 +814,8 @@ def main():
         e2e_obj = {"value": st.units() * world * e2e_steps / (pip_ms / 1e3), "unit": "TFLOP/s",
                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": pip_ms / e2e_steps,
                    "pipeline": "step i+1's inputs copied from pinned host memory on a second stream "
-                               "while step i computes (two device input buffers)",
+                               "while step i computes (two device input buffers); each loss read on a third "
+                               "stream",
                    "serial": {"value": st.units() * world * e2e_steps / (ser_ms / 1e3),
                               "ms_per_step": ser_ms / e2e_steps,
                               "pipeline": "copy, forward, backward, loss read, one after another"}}
