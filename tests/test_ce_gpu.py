@@ -150,6 +150,36 @@ def test_edge_shapes(n, vocab, pad, dtype, eps, red):
         assert torch.all(dz_full[:, vocab:] == 7.0).item()
 
 
+@pytest.mark.parametrize("dtype,offset", [("f32", 200.0), ("f32", 1000.0), ("bf16", 1000.0)])
+def test_large_logit_offset(dtype, offset):
+    # Logits far from zero.  The softmax works relative to the row maximum, and the
+    # rounding of -lse * log2(e) in the exponent is put back per row, so what is
+    # left is lse itself being an FP32 value: its rounding, |lse| * 2^-24, moves
+    # every probability of the row by that relative amount.  At +200 that stays
+    # inside the usual FP32 tolerance; at +1000 the FP32 gradient is checked
+    # against that bound instead.
+    n, vocab = 64, 5000
+    z = wk.normal_matrix(77, wk.TID_LOGITS, n, vocab, 3.0, False) + np.float32(offset)
+    if dtype == "bf16":
+        z = wk.f32_to_bf16_bits(z)  # BF16 spacing is 4 near 1000: few distinct values per row
+    target = wk.uniform_targets(77, n, vocab, 0.1)
+    grad = wk.grad_rows(77, n)
+    ref = oracle.ce_forward(z, target, 0.1, False, dtype=dtype)
+    with np.errstate(over="ignore", invalid="ignore"):  # ignored rows: lse 0 in the oracle, zeroed after
+        ref_dz = oracle.ce_backward(z, target, ref["lse"], ref["n_valid"], grad, 0.1, False, dtype=dtype)
+    for f, dz in (run_gpu(to_dev(z, dtype), target, 0.1, False, grad),
+                  (lambda r: (r, r.dlogits))(run_fused(to_dev(z, dtype), target, 0.1, False, grad))):
+        assert int(f.dev_status.item()) == 0
+        if dtype == "f32" and offset > 500:
+            lse_max = float(np.max(np.abs(ref["lse"])))
+            got = dz_np(dz, dtype)
+            assert np.linalg.norm(got - ref_dz) <= 2.0 ** -23 * lse_max * np.linalg.norm(ref_dz)
+            loss = f.loss.double().cpu().numpy()
+            assert np.all(np.abs(loss - ref["loss_rows"]) <= 2.0 ** -22 * lse_max + 1e-5)
+        else:
+            check_rows(f, dz, ref, ref_dz, np.arange(n), dtype, False, target)
+
+
 def test_inplace_backward_matches_out_of_place():
     n, vocab = 300, 50257
     z = wk.normal_matrix(5, wk.TID_LOGITS, n, vocab, 3.0, True)

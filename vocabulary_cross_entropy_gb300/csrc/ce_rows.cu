@@ -281,13 +281,15 @@ ce_backward_rows(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride,
             continue;
         }
         const float g = upstream_grad(reduce_loss, grad_output, n_valid, row);
-        const float negl = -stats[row].y * kLog2e;
+        const Exp2Offset eo = exp2_offset(stats[row].y);
+        const float negl = eo.neg;
+        const float gp = g * eo.fix;              // scale of the softmax term
         const float b = g * eps / float(vocab);   // eps / V share of every class
         const float c = g * (1.f - eps);          // target class
 
         auto grad1 = [&](int64_t j) {
             const float z = E::load1(p + j);
-            float d = fmaf(g, ex2f(fmaf(z, kLog2e, negl)), -b);
+            float d = fmaf(gp, ex2f(fmaf(z, kLog2e, negl)), -b);
             if (j == y) d -= c;
             E::store1(q + j, d);
         };
@@ -297,7 +299,7 @@ ce_backward_rows(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride,
         auto gradv = [&](const uint4& raw, int64_t i) {
             float v[V];
             E::unpack(raw, v);
-            grad_lanes<V>(v, g, negl, b);
+            grad_lanes<V>(v, gp, negl, b);
             const int64_t base = sp.head + i * V;
             if (uint64_t(y - base) < uint64_t(V)) {
 #pragma unroll
@@ -571,12 +573,14 @@ ce_fused_rows(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
             continue;
         }
         const float g = upstream_grad(reduce_loss, grad_output, n_valid, row);
-        const float negl = -sm_lse * kLog2e;
+        const Exp2Offset eo = exp2_offset(sm_lse);
+        const float negl = eo.neg;
+        const float gp = g * eo.fix;
         const float b = g * eps / float(vocab);
         const float c = g * (1.f - eps);
         auto grad1 = [&](int64_t j) {
             const float z = E::load1(p + j);
-            float d = fmaf(g, ex2f(fmaf(z, kLog2e, negl)), -b);
+            float d = fmaf(gp, ex2f(fmaf(z, kLog2e, negl)), -b);
             if (j == y) d -= c;
             E::store1(q + j, d);
         };
@@ -589,7 +593,7 @@ ce_fused_rows(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
             // scalar FMAs here (the same per-lane arithmetic as grad_lanes, so the same
             // bits as ce_backward_rows): the pair form costs this 64-register kernel a spill
 #pragma unroll
-            for (int k = 0; k < V; ++k) v[k] = fmaf(g, ex2f(fmaf(v[k], kLog2e, negl)), -b);
+            for (int k = 0; k < V; ++k) v[k] = fmaf(gp, ex2f(fmaf(v[k], kLog2e, negl)), -b);
             const int64_t base = sp.head + i * V;
             if (uint64_t(y - base) < uint64_t(V)) {
 #pragma unroll

@@ -226,7 +226,7 @@ struct DzEpi {
         const bool row_ok = gm < M;
         bool live = false;
         int64_t y = -1;
-        float g = 0.f, negl = 0.f;
+        float g = 0.f, gp = 0.f, negl = 0.f;
         if (row_ok) {
             y = target[gm];
             const bool ign = (y == ignore_idx);
@@ -235,7 +235,9 @@ struct DzEpi {
             live = !ign && !bad;
             if (live) {
                 g = upstream_grad(reduce, grad, n_valid, gm);
-                negl = -lse[gm] * kLog2e;
+                const Exp2Offset eo = exp2_offset(lse[gm]);
+                negl = eo.neg;
+                gp = g * eo.fix;
             }
         }
         const float b = g * eps / float(V);
@@ -253,7 +255,7 @@ struct DzEpi {
             float d[32];
             if (live) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) d[j] = fmaf(g, ex2f(fmaf(__uint_as_float(r[j]), kLog2e, negl)), -b);
+                for (int j = 0; j < 32; ++j) d[j] = fmaf(gp, ex2f(fmaf(__uint_as_float(r[j]), kLog2e, negl)), -b);
                 const int64_t yy = y - slab0 - col0;
                 if ((uint64_t)yy < 32ull) {
 #pragma unroll

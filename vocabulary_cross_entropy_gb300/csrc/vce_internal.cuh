@@ -21,6 +21,21 @@ __device__ __forceinline__ float ex2f(float x) {
     return y;
 }
 
+// The exp2 offset -lse * log2(e) of a row rounded to FP32, and the factor
+// 1 + r ln 2 that puts back its rounding residual r (computed exactly with an
+// FMA).  Every exponent of the row shares the residual, so the factor scales the
+// row's softmax term once instead of changing each element's arithmetic; without
+// it the rounding reaches |lse| * 2^-24 relative (4e-5 for logits near 1000).
+struct Exp2Offset {
+    float neg;  // -lse * log2(e), rounded
+    float fix;  // multiply exp2(z * log2(e) + neg) by this
+};
+__device__ __forceinline__ Exp2Offset exp2_offset(float lse) {
+    const float neg = -lse * kLog2e;
+    const float r = fmaf(-lse, kLog2e, -neg);
+    return {neg, fmaf(r, kLn2, 1.f)};
+}
+
 // Upstream gradient of row ``row``: grad_output[row] (no reduction),
 // grad_output[0] / N_v (mean) or grad_output[0] (sum).
 __device__ __forceinline__ float upstream_grad(int reduce, const float* grad_output, const int64_t* n_valid,
