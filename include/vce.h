@@ -223,8 +223,9 @@ vce_status ce_forward_noalloc(const void* logits, int dtype, int64_t n_rows, int
  * vocabulary ids: max, sum of exp, sum of logits, entropy term), the
  * per-token target logit and, when reducing, the per-token losses.  Both
  * parts end with 256 bytes for the GEMMs' work-unit counter, which the
- * library zeroes with a one-thread kernel on the call's stream before each GEMM.  The
- * same size passed to lce_backward on the same device selects the same slab.
+ * library zeroes with a one-thread kernel on the call's stream before each
+ * GEMM.  The same size passed to lce_backward on the same device selects the
+ * same slab.
  */
 size_t lce_workspace_size(int64_t n, int64_t h, int64_t v, int reduce_loss,
                           size_t max_slab_bytes);
