@@ -805,7 +805,7 @@ def main():
     fwd_flops = 2.0 * st.wl.n * st.wl.hidden * st.wl.vocab
     fwd_tf = fwd_flops / (ph["forward"] / 1e3) / 1e12
     bwd_tf = 3 * fwd_flops / (ph["backward"] / 1e3) / 1e12
-    e2e_steps = max(3, args.steps // 2)
+    e2e_steps = max(3, args.steps)  # as many steps as the device loop: the first copy (pipeline fill) counts once
     if args.no_e2e:
         e2e_obj = None
     else:
