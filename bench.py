@@ -495,18 +495,48 @@ def time_forward_entropy(step, steps, warmup, pg):
     return out
 
 
-def time_e2e_linear(step, steps, warmup, pg):
-    """The same step through the public calls, inputs copied from pinned host memory each step."""
+H2D_STREAMS = 1  # copy streams that share one step's host-to-device copy (--h2d-streams)
+
+
+def copy_inputs(dst, pinned, streams, after):
+    """Issues the copy of every pinned host tensor into ``dst``: with several streams,
+    tensors of 64 MiB or more are cut into equal row ranges, one per stream, so that
+    several copy engines can share them; each stream first waits for ``after``.
+    Returns one event per stream.  (Measured on shared boxes, 1, 2 and 4 streams gave
+    the same spread of end-to-end times: the host's copy bandwidth varies between runs.)"""
+    import torch
+    events = []
+    for i, st in enumerate(streams):
+        with torch.cuda.stream(st):
+            st.wait_event(after)
+            for k, t in pinned.items():
+                if t.dim() >= 1 and t.numel() * t.element_size() >= (64 << 20):
+                    lo, hi = t.shape[0] * i // len(streams), t.shape[0] * (i + 1) // len(streams)
+                    dst[k][lo:hi].copy_(t[lo:hi], non_blocking=True)
+                elif i == 0:
+                    dst[k].copy_(t, non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(st)
+            events.append(ev)
+    return events
+
+
+def time_e2e_linear(step, steps, warmup, pg, h2d_streams=H2D_STREAMS):
+    """The same step through the public calls, inputs copied from pinned host memory
+    each step, then forward, backward and the loss read, one after another."""
     import torch
     stream = torch.cuda.current_stream()
+    copy_streams = [torch.cuda.Stream() for _ in range(max(1, h2d_streams))]
     pinned = {k: v.pin_memory() for k, v in step.host.items()}
     loss_host = torch.empty_like(step.loss, device="cpu").pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in pinned.values())
     d2h = loss_host.numel() * loss_host.element_size()
 
     def one():
-        for k, t in pinned.items():
-            step.d[k].copy_(t, non_blocking=True)
+        prev = torch.cuda.Event()
+        prev.record(stream)  # the previous step no longer reads the inputs
+        for ev in copy_inputs(step.d, pinned, copy_streams, prev):
+            stream.wait_event(ev)
         step.forward()
         step.backward()
         loss_host.copy_(step.loss, non_blocking=True)
@@ -525,37 +555,35 @@ def time_e2e_linear(step, steps, warmup, pg):
     return max_over_ranks(pg, s.elapsed_time(e)), h2d, d2h
 
 
-def time_e2e_linear_pipelined(step, steps, warmup, pg):
+def time_e2e_linear_pipelined(step, steps, warmup, pg, h2d_streams=H2D_STREAMS):
     """End to end with the host copies overlapped: while step i computes, step i+1's
-    inputs are copied from pinned host memory on a second stream into the other of two
-    device input buffers (the usual prefetch of a training loop), and step i's loss is
-    read back on a third stream, so that the 4-byte read never waits on the compute
-    stream behind a copy engine that is busy with the next step's inputs (two loss
-    buffers by step parity keep a step from overwriting a loss still being read).
-    Every step still copies all of its inputs and reads its loss back; the timed region
-    runs from before the first copy to after the last loss read."""
+    inputs are copied from pinned host memory into the other of two device input
+    buffers (the usual prefetch of a training loop), and
+    step i's loss is read back on its own stream, so that the 4-byte read never waits
+    on the compute stream behind a copy engine that is busy with the next step's
+    inputs (two loss buffers by step parity keep a step from overwriting a loss still
+    being read).  Every step still copies all of its inputs and reads its loss back;
+    the timed region runs from before the first copy to after the last loss read."""
     import torch
     vce, wl = step.vce, step.wl
     comp = torch.cuda.current_stream()
-    copy_stream, read_stream = torch.cuda.Stream(), torch.cuda.Stream()
+    copy_streams = [torch.cuda.Stream() for _ in range(max(1, h2d_streams))]
+    read_stream = torch.cuda.Stream()
     pinned = {k: v.pin_memory() for k, v in step.host.items()}
     bufs = [step.d, {k: torch.empty_like(v) for k, v in step.d.items()}]
     losses = [step.loss, torch.empty_like(step.loss)]
-    ready = [torch.cuda.Event(), torch.cuda.Event()]
+    ready = [[], []]
     done = [torch.cuda.Event(), torch.cuda.Event()]
     read = [torch.cuda.Event(), torch.cuda.Event()]
     loss_host = [torch.empty_like(step.loss, device="cpu").pin_memory() for _ in range(2)]
 
     def copy_into(b):
-        with torch.cuda.stream(copy_stream):
-            copy_stream.wait_event(done[b])
-            for k, t in pinned.items():
-                bufs[b][k].copy_(t, non_blocking=True)
-            ready[b].record(copy_stream)
+        ready[b] = copy_inputs(bufs[b], pinned, copy_streams, done[b])
 
     def compute(b):
         d = bufs[b]
-        comp.wait_event(ready[b])
+        for ev in ready[b]:
+            comp.wait_event(ev)
         comp.wait_event(read[b])  # the loss buffer's previous read has finished
         vce.lce_forward(d["X"], d["W"], d["target"], wl.label_smoothing, wl.reduce_loss, loss=losses[b],
                         lse=step.lse, n_valid=step.n_valid, workspace=step.ws, dev_status=step.status)
@@ -580,7 +608,8 @@ def time_e2e_linear_pipelined(step, steps, warmup, pg):
     barrier(pg)
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s.record(comp)
-    copy_stream.wait_event(s)
+    for st in copy_streams:
+        st.wait_event(s)
     read_stream.wait_event(s)
     run(steps)
     e.record(comp)
@@ -711,6 +740,8 @@ def main():
     ap.add_argument("--workload", default="both", choices=["linear", "logits", "both"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
+    ap.add_argument("--h2d-streams", type=int, default=H2D_STREAMS,
+                    help="copy streams that share each step's host-to-device copy in the e2e timing")
     ap.add_argument("--vocab-sweep", action="store_true",
                     help="also time the logits form (forward, backward, fused) over common vocabulary sizes")
     ap.add_argument("--sweep", action="store_true",
@@ -809,16 +840,19 @@ def main():
     if args.no_e2e:
         e2e_obj = None
     else:
-        ser_ms, h2d, d2h = time_e2e_linear(st, e2e_steps, 3, pg)
-        pip_ms = time_e2e_linear_pipelined(st, e2e_steps, 3, pg)
+        ser_ms, h2d, d2h = time_e2e_linear(st, e2e_steps, 3, pg, args.h2d_streams)
+        with Clocks(local) as cke:
+            pip_ms = time_e2e_linear_pipelined(st, e2e_steps, 3, pg, args.h2d_streams)
         e2e_obj = {"value": st.units() * world * e2e_steps / (pip_ms / 1e3), "unit": "TFLOP/s",
                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": pip_ms / e2e_steps,
-                   "pipeline": "step i+1's inputs copied from pinned host memory on a second stream "
-                               "while step i computes (two device input buffers); each loss read on a third "
-                               "stream",
+                   "pipeline": f"step i+1's inputs copied from pinned host memory (W cut over "
+                               f"{args.h2d_streams} copy streams) while step i computes (two device input "
+                               "buffers); each loss read on its own stream",
+                   "clocks": cke.summary(),
                    "serial": {"value": st.units() * world * e2e_steps / (ser_ms / 1e3),
                               "ms_per_step": ser_ms / e2e_steps,
-                              "pipeline": "copy, forward, backward, loss read, one after another"}}
+                              "pipeline": f"copy (W cut over {args.h2d_streams} copy streams), forward, "
+                                          "backward, loss read, one after another"}}
     line = {
         "metric": "linear-CE fwd+bwd TFLOP/s (4 classifier GEMMs)",
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
