@@ -460,6 +460,55 @@ def vocab_sweep(dev, args, pg, pk):
     return out
 
 
+TOKEN_SWEEP = (512, 1024, 2048, 4096, 8192, 16384)
+
+
+def token_sweep(dev, args, pg, pk):
+    """lce_forward + lce_backward at H = 4096, V = 131072 over token counts: X ~ N(0, 1)
+    and W ~ N(0, 1/H) in BF16 drawn on the device from a seeded generator, uniform
+    targets, mean reduction.  TFLOP/s counts the four classifier GEMMs, 8 N H V."""
+    import torch
+    import vocabulary_cross_entropy_gb300 as vce
+    h, v = 4096, 131072
+    g = torch.Generator(device=dev).manual_seed(1)
+    w = (torch.randn(v, h, device=dev, generator=g) * h ** -0.5).to(torch.bfloat16)
+    dw = torch.empty_like(w)
+    out = []
+    for n in TOKEN_SWEEP:
+        x = torch.randn(n, h, device=dev, generator=g).to(torch.bfloat16)
+        y = torch.randint(0, v, (n,), device=dev, generator=g)
+        dx = torch.empty_like(x)
+        grad = torch.ones(1, device=dev)
+        loss, lse = torch.empty(1, device=dev), torch.empty(n, device=dev)
+        nv = torch.empty(1, dtype=torch.int64, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        ws = torch.empty(vce.lce_workspace_size(n, h, v, True), dtype=torch.uint8, device=dev)
+
+        def step():
+            vce.lce_forward(x, w, y, 0.0, True, loss=loss, lse=lse, n_valid=nv, workspace=ws, dev_status=status)
+            vce.lce_backward(x, w, y, lse, nv, grad, 0.0, True, dX=dx, dW=dw, workspace=ws, dev_status=status)
+
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        barrier(pg)
+        k = max(3, args.steps // 3)
+        stream = torch.cuda.current_stream()
+        s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s_.record(stream)
+        for _ in range(k):
+            step()
+        e_.record(stream)
+        torch.cuda.synchronize()
+        ms = max_over_ranks(pg, s_.elapsed_time(e_)) / k
+        assert int(status.item()) == 0, "device status reported an error"
+        tf = 8.0 * n * h * v / (ms / 1e3) / 1e12
+        out.append({"n": n, "ms_per_step": ms, "value": tf, "unit": "TFLOP/s", "frac_of_burst": tf / pk["bf16"]})
+        del x, dx, ws
+        torch.cuda.empty_cache()
+    return out
+
+
 def time_forward_entropy(step, steps, warmup, pg):
     """Mean ms of lce_forward without and with the per-token entropy output, each over
     ``steps`` back-to-back calls (the entropy adds one multiply-add per logit and a
@@ -742,6 +791,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
     ap.add_argument("--h2d-streams", type=int, default=H2D_STREAMS,
                     help="copy streams that share each step's host-to-device copy in the e2e timing")
+    ap.add_argument("--token-sweep", action="store_true",
+                    help="also time the linear form at H=4096, V=131072 over token counts 512..16384")
     ap.add_argument("--vocab-sweep", action="store_true",
                     help="also time the logits form (forward, backward, fused) over common vocabulary sizes")
     ap.add_argument("--sweep", action="store_true",
@@ -947,6 +998,9 @@ def main():
                 "workspace_bytes": stp.ws_bytes, "clocks": cks.summary()})
             del stp
             torch.cuda.empty_cache()
+    if args.token_sweep and lin is wk.LINEAR_HEADLINE:
+        torch.cuda.empty_cache()
+        line["token_sweep"] = token_sweep(dev, args, pg, pk)
     if args.vocab_sweep and lin is wk.LINEAR_HEADLINE:
         torch.cuda.empty_cache()
         line["vocab_sweep"] = vocab_sweep(dev, args, pg, pk)
