@@ -510,9 +510,11 @@ def token_sweep(dev, args, pg, pk):
 
 
 def time_forward_entropy(step, steps, warmup, pg):
-    """Mean ms of lce_forward without and with the per-token entropy output, each over
-    ``steps`` back-to-back calls (the entropy adds one multiply-add per logit and a
-    third partial per vocabulary tile)."""
+    """lce_forward without and with the per-token entropy output (one more multiply-add
+    per logit and a third partial per vocabulary tile).  The two kinds of call alternate
+    one by one, each timed by its own pair of events, and the medians are compared: the
+    power-capped SM clock drifts over tens of milliseconds, so two separate loops of each
+    kind can see different clocks, while neighbouring calls see the same one."""
     import torch
     wl = step.wl
     stream = torch.cuda.current_stream()
@@ -523,25 +525,24 @@ def time_forward_entropy(step, steps, warmup, pg):
                              loss=step.loss, lse=step.lse, n_valid=step.n_valid, workspace=step.ws,
                              dev_status=step.status, entropy=ent if with_entropy else None)
 
-    out = {}
-    for with_entropy in (False, True, False, True):
-        for _ in range(warmup):
-            one(with_entropy)
-        torch.cuda.synchronize()
-        barrier(pg)
-        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s.record(stream)
-        for _ in range(steps):
-            one(with_entropy)
-        e.record(stream)
-        torch.cuda.synchronize()
-        barrier(pg)
-        ms = max_over_ranks(pg, s.elapsed_time(e)) / steps
-        key = "forward_with_entropy_ms" if with_entropy else "forward_ms"
-        out[key] = min(out.get(key, ms), ms)
-    out["overhead"] = out["forward_with_entropy_ms"] / out["forward_ms"] - 1.0
-    out["note"] = "best of two alternating loops of each, same workload"
-    return out
+    for _ in range(warmup):
+        one(False)
+        one(True)
+    torch.cuda.synchronize()
+    barrier(pg)
+    ev = {k: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+          for k in (False, True)}
+    for i in range(steps):
+        for k in ((False, True) if i % 2 == 0 else (True, False)):
+            ev[k][i][0].record(stream)
+            one(k)
+            ev[k][i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(pg)
+    med = {k: max_over_ranks(pg, statistics.median(a.elapsed_time(b) for a, b in ev[k])) for k in ev}
+    return {"forward_ms": med[False], "forward_with_entropy_ms": med[True],
+            "overhead": med[True] / med[False] - 1.0,
+            "note": "medians over %d calls of each kind, the two kinds alternating call by call" % steps}
 
 
 H2D_STREAMS = 1  # copy streams that share one step's host-to-device copy (--h2d-streams)
@@ -933,7 +934,7 @@ def main():
         "gpu_launches": st.timed_launches,
         "clocks": clocks,
     }
-    line["entropy_cost"] = time_forward_entropy(st, max(3, args.steps // 3), 3, pg)
+    line["entropy_cost"] = time_forward_entropy(st, max(3, args.steps), 3, pg)
     line["config"]["peak_extra_memory_bytes"] = peak_extra_memory(st)
     if logits_obj is not None:
         line["logits_ce"] = logits_obj
