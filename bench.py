@@ -55,7 +55,7 @@ def FWD_GEMM_TRAFFIC_BYTES(wl):
     capture in profiles/tc_gemm_traffic_headline_and_16384_tokens.md (N = H = 4096,
     V = 131072), scaled to this workload's V: the X bytes stay, the W bytes and the
     per-tile partials grow with V.  None for workloads outside that N = H = 4096 family."""
-    captured_v, read_bytes, write_bytes = 131072, 1.107715840e9, 19.7056e6
+    captured_v, read_bytes, write_bytes = 131072, 1.108554752e9, 19.760128e6
     if wl.n != 4096 or wl.hidden != 4096:
         return None
     x_bytes = wl.n * wl.hidden * 2
@@ -67,9 +67,9 @@ def FWD_GEMM_TRAFFIC_BYTES(wl):
 # captures in profiles/ce_rows_logits_2048x128256.md and
 # profiles/ce_fused_rows_logits_2048x128256.md (2048 rows of V = 128256 BF16, 5% ignored)
 LOGITS_CAPTURED_TRAFFIC = {
-    "forward": (502.399488e6, 3.231744e6),
-    "backward": (502.3232e6, 467.8656e6),
-    "fused": (526.883072e6, 466.792192e6),
+    "forward": (502.397952e6, 3.326976e6),
+    "backward": (502.323968e6, 467.554560e6),
+    "fused": (525.266432e6, 467.363584e6),
 }
 
 
