@@ -65,11 +65,11 @@ def FWD_GEMM_TRAFFIC_BYTES(wl):
 
 # DRAM bytes (read, write) per launch of the logits-form row kernels, from the ncu
 # captures in profiles/ce_rows_logits_2048x128256.md and
-# profiles/ce_fused_rows_logits_2048x128256.md (2048 rows of V = 128256 BF16, 5% ignored)
+# profiles/ce_fused_ring_logits_2048x128256.md (2048 rows of V = 128256 BF16, 5% ignored)
 LOGITS_CAPTURED_TRAFFIC = {
     "forward": (502.397952e6, 3.326976e6),
     "backward": (502.323968e6, 467.554560e6),
-    "fused": (525.266432e6, 467.363584e6),
+    "fused": (505.122304e6, 464.573952e6),
 }
 
 
@@ -874,6 +874,9 @@ def main():
         line.update({"n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                      "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                      "dtype": "bf16", "data": "synthetic"})
+        if args.vocab_sweep:
+            torch.cuda.empty_cache()
+            line["vocab_sweep"] = vocab_sweep(dev, args, pg, pk)
         if rank == 0:
             print(json.dumps(line), flush=True)
         return 0

@@ -47,8 +47,8 @@
  *     device int the caller zeroes and reads after its own synchronisation;
  *     may be NULL): VCE_DEVSTATUS_BAD_TARGET for a target outside [0, V) that
  *     is not ignore_idx (that row's loss is NaN and its gradient row 0),
- *     VCE_DEVSTATUS_TIMEOUT when a tensor-core pipeline wait gave up (the
- *     outputs are then incomplete).
+ *     VCE_DEVSTATUS_TIMEOUT when a wait of a tensor-core or copy pipeline gave
+ *     up (the outputs are then incomplete).
  *   - The library runs on compute capability 10.3 (GB300) only; on any other
  *     device every compute call returns VCE_ERR_ARCH.
  */
@@ -167,10 +167,15 @@ vce_status ce_backward(const void* logits, int dtype, int64_t n_rows, int64_t vo
  *
  *   Arguments are those of ce_forward and ce_backward combined; the results are
  *   those of ce_forward followed by ce_backward with the same grad_output (loss,
- *   stats, n_valid, dlogits): bit for bit for rows of up to about 100 KiB, which
- *   both calls sum with the same threads per row; for longer rows this call
- *   splits a row's sum differently, so lse and the loss agree to FP32 rounding
- *   (row maxima, n_valid and ignored rows exactly).  dlogits MAY EQUAL logits
+ *   stats, n_valid, dlogits): bit for bit for rows of at most 4096 16-byte
+ *   vectors (64 KiB) and for rows of more than 112 KiB, where both calls give
+ *   every thread the same elements in the same order; for rows in between this
+ *   call splits a row's sum differently, so lse and the loss agree to FP32
+ *   rounding (row maxima, n_valid and ignored rows exactly).  The call uses up
+ *   to about 193 KiB of shared memory per CTA and raises the kernel's dynamic
+ *   shared-memory limit on the first call on each device.  A timeout of its
+ *   internal copy pipeline (not expected) sets VCE_DEVSTATUS_TIMEOUT and leaves
+ *   the outputs undefined.  dlogits MAY EQUAL logits
  *   (in place), with the same 16-byte offset rule as ce_backward.
  *   grad_output F32 [1] when reduce_loss != 0, else [n_rows].
  *   ws/ws_bytes: ce_workspace_size(n_rows, vocab, reduce_loss) bytes.

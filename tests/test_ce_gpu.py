@@ -341,9 +341,13 @@ FUSED = [
     (40, 49152, "bf16", 0.1, True, False),
     (25, 98304, "f32", 0.0, 2, True),
     (130, 128256, "bf16", 0.0, False, True),
-    # several rows per persistent CTA: next-row L2 prefetch on (bf16) and off (f32, rows too large)
+    # several rows per persistent CTA on the TMA-fed ring kernel (rows of more than
+    # 4096 vectors): one CTA per SM with a 192 KiB ring (bf16 128 KiB rows, f32
+    # 512 KiB rows) and two CTAs per SM with 96 KiB rings (bf16 78 KiB rows)
     (500, 65536, "bf16", 0.0, 2, True),
     (400, 131072, "f32", 0.1, True, False),
+    (700, 40000, "bf16", 0.1, True, True),
+    (333, 20001, "f32", 0.0, False, False),
     # several rows per CTA with the prefetch on the 256- and 128-thread paths
     (1000, 20000, "bf16", 0.1, True, False),
     (3000, 1000, "bf16", 0.0, 2, True),
@@ -369,7 +373,8 @@ def test_fused_matches_oracle_and_separate_path(n, vocab, dtype, eps, red, inpla
 
 
 @pytest.mark.parametrize("n,vocab,pad,dtype,eps,red", [
-    (200, 50001, 3, "bf16", 0.1, True),   # 1024 threads per row, next-row prefetch, rows off 16-byte alignment
+    (200, 50001, 3, "bf16", 0.1, True),   # ring kernel, two CTAs per SM, rows off 16-byte alignment
+    (400, 70001, 7, "bf16", 0.0, 2),      # ring kernel, one CTA per SM, rows off 16-byte alignment
     (150, 9001, 5, "f32", 0.0, False),    # 256 threads per row
     (300, 129, 1, "bf16", 0.1, 2),        # 128 threads per row
 ])
@@ -393,6 +398,42 @@ def test_fused_padded_rows(n, vocab, pad, dtype, eps, red):
     ref = oracle.ce_forward(z, target, eps, red, dtype=dtype)
     ref_dz = oracle.ce_backward(z, target, ref["lse"], ref["n_valid"], grad, eps, red, dtype=dtype)
     check_rows(r, r.dlogits, ref, ref_dz, np.arange(n), dtype, red, target)
+
+
+@pytest.mark.parametrize("vocab,dtype", [(40000, "bf16"), (70001, "bf16"), (33000, "f32")])
+def test_fused_ring_bad_and_ignored_rows(vocab, dtype):
+    """Rows whose target is out of range get one pass through the ring kernel (their
+    statistics) and a zero gradient, ignored rows none; the producer and the compute
+    warps must agree on that sequence for every later row to be right."""
+    n = 1000
+    seed = 11 + vocab
+    z = wk.normal_matrix(seed, wk.TID_LOGITS, n, vocab, 3.0, dtype == "bf16")
+    target = wk.uniform_targets(seed, n, vocab, 0.1)
+    target[5::97] = vocab          # out of range above
+    target[50::131] = -7           # out of range below
+    grad = wk.grad_rows(seed, n)
+    r = run_fused(to_dev(z, dtype), target, 0.1, False, grad)
+    bad = (target == vocab) | (target == -7)
+    assert int(r.dev_status.item()) & vce.DEVSTATUS_BAD_TARGET
+    loss = r.loss.double().cpu().numpy()
+    assert np.all(np.isnan(loss[bad])) and np.all(np.isfinite(loss[~bad]))
+    dz = r.dlogits.float().cpu().numpy()
+    assert np.all(dz[bad] == 0.0)
+    good = ~bad
+    ref = oracle.ce_forward(z[good], target[good], 0.1, False, dtype=dtype)
+    ref_dz = oracle.ce_backward(z[good], target[good], ref["lse"], ref["n_valid"], grad[good], 0.1, False,
+                                dtype=dtype)
+    rows = np.nonzero(good)[0]
+    sub = r._replace(loss=r.loss[torch.from_numpy(rows).to(DEV)], stats=r.stats[torch.from_numpy(rows).to(DEV)])
+    check_rows(sub, r.dlogits[torch.from_numpy(rows).to(DEV)], ref, ref_dz, np.arange(len(rows)), dtype, False,
+               target[good])
+    # the statistics of a bad row are still those of its logits
+    bad_rows = np.nonzero(bad)[0]
+    ref_bad = oracle.ce_forward(z[bad_rows], np.zeros(len(bad_rows), np.int64), 0.1, False, dtype=dtype)
+    st = r.stats.double().cpu().numpy()[bad_rows]
+    np.testing.assert_array_equal(st[:, 0], ref_bad["m"])
+    np.testing.assert_allclose(st[:, 1], ref_bad["lse"], rtol=1e-5 if dtype == "f32" else 0.0,
+                               atol=0.0 if dtype == "f32" else 2e-3)
 
 
 def test_fused_membound_full_size_inplace():

@@ -12,10 +12,18 @@
 //   dz = g (exp(z - lse) - (1 - eps) onehot(y) - eps / V), zeros for ignored rows.
 // Mean reduction: one CTA sums the per-row losses in a fixed order (run to run
 // identical) and counts the rows whose target is not ignore_idx.
+// Fused forward + backward (for a caller that knows grad_output up front): each
+// row is read from HBM once and its gradient written once; the second read of
+// the row is served by L2.  Short rows: several CTAs per SM, each asking L2 for
+// its next row ahead of time.  Rows of more than 4096 16-byte vectors: a
+// persistent CTA per SM (or two) whose producer thread streams the row through
+// a shared-memory ring with TMA bulk copies.
 
 #include "vce_internal.cuh"
+#include "sm100_ptx.cuh"
 
 #include <math.h>
+#include <mutex>
 
 namespace vce {
 namespace {
@@ -615,6 +623,358 @@ ce_fused_rows(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
     }
 }
 
+// ---------------------------------------------------------------------------
+// fused forward + backward for long rows: rows streamed through a shared-memory
+// ring by TMA bulk copies
+// ---------------------------------------------------------------------------
+
+// Global -> shared bulk copy (16-byte aligned addresses, size a multiple of 16)
+// whose completion is counted on an mbarrier of this CTA.
+__device__ __forceinline__ void bulk_load_shared(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(mbar)
+                 : "memory");
+}
+
+// The same copy with an L2 eviction-priority hint for the bytes it reads.
+__device__ __forceinline__ void bulk_load_shared_hint(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar,
+                                                      uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(mbar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// Barrier among the NT compute threads only (the producer warp does not take part).
+template <int NT>
+__device__ __forceinline__ void compute_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+}
+
+// block_merge over the compute threads of the ring kernel
+template <int NT, bool kSum>
+__device__ __forceinline__ void compute_merge(OnlineLse& a, float* sm_m, float* sm_s, float* sm_sum) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, a.m, off);
+        const float s2 = __shfl_xor_sync(0xffffffffu, a.s, off);
+        const float u2 = kSum ? __shfl_xor_sync(0xffffffffu, a.sum, off) : 0.f;
+        a.merge(m2, s2, u2);
+    }
+    if (lane == 0) { sm_m[warp] = a.m; sm_s[warp] = a.s; sm_sum[warp] = a.sum; }
+    compute_sync<NT>();
+    if (warp == 0) {
+        constexpr int W = NT / 32;
+        OnlineLse b;
+        if (lane < W) { b.m = sm_m[lane]; b.s = sm_s[lane]; b.sum = sm_sum[lane]; }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float m2 = __shfl_xor_sync(0xffffffffu, b.m, off);
+            const float s2 = __shfl_xor_sync(0xffffffffu, b.s, off);
+            const float u2 = kSum ? __shfl_xor_sync(0xffffffffu, b.sum, off) : 0.f;
+            b.merge(m2, s2, u2);
+        }
+        a = b;
+    }
+}
+
+constexpr uint64_t kRingTimeoutNs = 2000000000ull;  // 2 s per wait
+
+// NW compute warps, each thread taking PER 16-byte vectors of every full
+// chunk; RING_KB KiB of shared memory in equal chunks.
+template <int NW, int PER, int RING_KB>
+struct RingCfg {
+    static constexpr int kThreads = NW * 32;                        // compute threads
+    static constexpr uint32_t kChunk = uint32_t(kThreads) * PER * 16;  // bytes per ring slot
+    static constexpr int kSlots = int(uint32_t(RING_KB) * 1024 / kChunk);
+    static constexpr size_t kSmemBytes = size_t(kSlots) * kChunk + 2 * kSlots * 8 + (3 * 32 + 2) * 4;
+    static_assert(kSlots >= 2 && kSlots <= 16, "ring depth");
+};
+
+// Bounded wait that ignores the abort flag (draining copies still in flight).
+__device__ __forceinline__ bool ring_drain_wait(uint64_t* bar, uint32_t parity) {
+    const uint64_t t0 = sm100::globaltimer();
+    while (!sm100::mbar_try_wait(bar, parity))
+        if (sm100::globaltimer() - t0 > kRingTimeoutNs) return false;
+    return true;
+}
+
+// MINB persistent CTAs per SM; warps 0..NW-1 compute, warp NW is the producer.
+// The producer's first thread walks the same sequence of rows as the compute
+// warps and, for every row that is not ignored, copies the row's 16-byte
+// aligned interior into the ring chunk by chunk, once for the first pass and,
+// unless the target is out of range, once more for the second pass (the second
+// read is served by L2).  It runs ahead of the compute warps by up to the ring
+// depth, across the block-wide merge between the passes and across rows, so
+// HBM and L2 reads continue while the compute warps merge, and the copies in
+// flight (up to the whole ring) take no registers.  The compute warps take
+// every chunk in order: pass 1 folds it into the online (max, sum exp), pass 2
+// turns it into dlogits written to global memory; the few elements before the
+// first 16-byte boundary and after the last are read directly.  With kHint the
+// first pass's copies ask L2 to keep the row's lines (evict_last) and the second
+// pass's to drop them first (evict_first), so the next row's first-pass reads do
+// not push out lines the second pass still needs.
+// Every wait is bounded: on timeout the CTA sets its abort flag, every role
+// stops waiting, the producer waits for the copies it issued, and
+// VCE_DEVSTATUS_TIMEOUT is reported (the outputs are then undefined).
+template <int NW, int PER, int RING_KB, int MINB, bool kHint, typename T, bool kSmooth>
+__global__ void __launch_bounds__(NW * 32 + 32, MINB)
+ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, const int64_t* __restrict__ target,
+              float eps, int64_t ignore_idx, const int64_t* __restrict__ n_valid,
+              const float* __restrict__ grad_output, int reduce_loss, float* __restrict__ loss_rows,
+              float2* __restrict__ stats, T* dlogits, int* dev_status) {
+    using E = Elem<T>;
+    using C = RingCfg<NW, PER, RING_KB>;
+    using namespace sm100;
+    constexpr int V = E::kVec;
+    constexpr int NT = C::kThreads;
+    constexpr uint32_t CH = C::kChunk;
+    constexpr int S = C::kSlots;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t* ring = smem;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(S) * CH);
+    uint64_t* empty = full + S;
+    float* sm_m = reinterpret_cast<float*>(empty + S);
+    float* sm_s = sm_m + 32;
+    float* sm_sum = sm_s + 32;
+    float* sm_lse = sm_sum + 32;
+    int* abort_flag = reinterpret_cast<int*>(sm_lse + 1);
+    const int tid = threadIdx.x;
+
+    if (tid == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], NW);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (tid >= NT) {
+        // ---------------- producer ----------------
+        if (tid != NT) return;
+        uint32_t slot = 0, ph = 0, issued = 0;
+        bool ok = true;
+        const uint64_t keep = kHint ? l2_policy_evict_last() : 0, drop = kHint ? l2_policy_evict_first() : 0;
+        for (int64_t row = blockIdx.x; row < n_rows && ok; row += gridDim.x) {
+            const int64_t y = target[row];
+            if (y == ignore_idx) continue;
+            const bool bad = y < 0 || y >= vocab;
+            const T* p = logits + row * stride;
+            const RowSplit<T> sp(p, vocab);
+            const uint64_t total = uint64_t(sp.nvec) * 16;
+            const uint8_t* src = reinterpret_cast<const uint8_t*>(p + sp.head);
+            for (int pass = 0; pass < (bad ? 1 : 2) && ok; ++pass) {
+                for (uint64_t off = 0; off < total; off += CH) {
+                    if (!mbar_wait(&empty[slot], ph ^ 1, abort_flag, kRingTimeoutNs)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t bytes = uint32_t(total - off < CH ? total - off : CH);
+                    mbar_arrive_expect_tx(&full[slot], bytes);
+                    if (kHint)
+                        bulk_load_shared_hint(smem_u32(ring + size_t(slot) * CH), src + off, bytes,
+                                              smem_u32(&full[slot]), pass == 0 ? keep : drop);
+                    else
+                        bulk_load_shared(smem_u32(ring + size_t(slot) * CH), src + off, bytes,
+                                         smem_u32(&full[slot]));
+                    ++issued;
+                    if (++slot == uint32_t(S)) {
+                        slot = 0;
+                        ph ^= 1;
+                    }
+                }
+            }
+        }
+        // wait for the last copy into every slot that received one (all of them
+        // have completed already unless the CTA gave up)
+        for (uint32_t i = 0; i < uint32_t(S) && i < issued; ++i) {
+            const uint32_t last = i + ((issued - 1 - i) / S) * S;
+            ring_drain_wait(&full[i], (last / S) & 1);
+        }
+        if (!ok) report(dev_status, VCE_DEVSTATUS_TIMEOUT);
+        return;
+    }
+
+    // ---------------- compute warps ----------------
+    const int lane = tid & 31;
+    uint32_t slot = 0, ph = 0;
+    bool ok = true;
+    // wait for the next chunk; false once this CTA has given up
+    auto take = [&]() -> bool {
+        if (ok && !mbar_wait(&full[slot], ph, abort_flag, kRingTimeoutNs)) ok = false;
+        return ok;
+    };
+    auto release = [&]() {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+        if (++slot == uint32_t(S)) {
+            slot = 0;
+            ph ^= 1;
+        }
+    };
+    for (int64_t row = blockIdx.x; row < n_rows; row += gridDim.x) {
+        const int64_t y = target[row];
+        const T* p = logits + row * stride;
+        T* q = dlogits + row * stride;
+        const RowSplit<T> sp(p, vocab);
+        if (y == ignore_idx) {
+            if (tid == 0) {
+                loss_rows[row] = 0.f;
+                stats[row] = make_float2(0.f, 0.f);
+            }
+            row_zero<NT, T>(q, sp, vocab);
+            continue;
+        }
+        const bool bad = y < 0 || y >= vocab;
+        const uint64_t total = uint64_t(sp.nvec) * 16;
+
+        // pass 1: online (max, sum exp) and sum of logits
+        OnlineLse acc;
+        if (tid < sp.head) {
+            float v[1] = {E::load1(p + tid)};
+            acc.push<1, kSmooth>(v);
+        }
+        for (uint64_t off = 0; off < total; off += CH) {
+            if (take()) {
+                const uint4* src = reinterpret_cast<const uint4*>(ring + size_t(slot) * CH);
+                if (total - off >= CH) {
+                    uint4 raw[PER];
+#pragma unroll
+                    for (int u = 0; u < PER; ++u) raw[u] = src[tid + u * NT];
+#pragma unroll
+                    for (int u = 0; u < PER; ++u) {
+                        float v[V];
+                        E::unpack(raw[u], v);
+                        acc.push<V, kSmooth>(v);
+                    }
+                } else {
+                    const uint32_t nv = uint32_t(total - off) / 16;
+                    for (uint32_t j = tid; j < nv; j += NT) {
+                        float v[V];
+                        E::unpack(src[j], v);
+                        acc.push<V, kSmooth>(v);
+                    }
+                }
+            }
+            release();
+        }
+        for (int64_t j = sp.tail0 + tid; j < vocab; j += NT) {
+            float v[1] = {E::load1(p + j)};
+            acc.push<1, kSmooth>(v);
+        }
+        compute_merge<NT, kSmooth>(acc, sm_m, sm_s, sm_sum);
+        if (tid == 0) {
+            const float lse = acc.m + logf(acc.s);
+            float loss;
+            if (!bad) {
+                const float zy = E::load1(p + y);
+                loss = lse - zy;
+                if (kSmooth) loss = (1.f - eps) * loss + eps * (lse - acc.sum / float(vocab));
+            } else {
+                loss = __int_as_float(0x7fc00000);
+                report(dev_status, VCE_DEVSTATUS_BAD_TARGET);
+            }
+            loss_rows[row] = loss;
+            stats[row] = make_float2(acc.m, lse);
+            *sm_lse = lse;
+        }
+        compute_sync<NT>();
+        if (bad) {
+            row_zero<NT, T>(q, sp, vocab);
+            continue;
+        }
+
+        // pass 2: dlogits = g (softmax - (1 - eps) onehot - eps / V)
+        const float g = upstream_grad(reduce_loss, grad_output, n_valid, row);
+        const Exp2Offset eo = exp2_offset(*sm_lse);
+        const float negl = eo.neg;
+        const float gp = g * eo.fix;
+        const float b = g * eps / float(vocab);
+        const float c = g * (1.f - eps);
+        auto grad1 = [&](int64_t j) {
+            const float z = E::load1(p + j);
+            float d = fmaf(gp, ex2f(fmaf(z, kLog2e, negl)), -b);
+            if (j == y) d -= c;
+            E::store1(q + j, d);
+        };
+        if (tid < sp.head) grad1(tid);
+        uint4* qv = reinterpret_cast<uint4*>(q + sp.head);
+        auto gradv = [&](const uint4& raw, int64_t i) {
+            float v[V];
+            E::unpack(raw, v);
+            grad_lanes<V>(v, gp, negl, b);
+            const int64_t base = sp.head + i * V;
+            if (uint64_t(y - base) < uint64_t(V)) {
+#pragma unroll
+                for (int k = 0; k < V; ++k) v[k] -= (base + k == y) ? c : 0.f;
+            }
+            __stcs(qv + i, E::pack(v));
+        };
+        for (uint64_t off = 0; off < total; off += CH) {
+            if (take()) {
+                const uint4* src = reinterpret_cast<const uint4*>(ring + size_t(slot) * CH);
+                const int64_t i0 = int64_t(off / 16);
+                if (total - off >= CH) {
+                    uint4 raw[PER];
+#pragma unroll
+                    for (int u = 0; u < PER; ++u) raw[u] = src[tid + u * NT];
+#pragma unroll
+                    for (int u = 0; u < PER; ++u) gradv(raw[u], i0 + tid + u * NT);
+                } else {
+                    const uint32_t nv = uint32_t(total - off) / 16;
+                    for (uint32_t j = tid; j < nv; j += NT) gradv(src[j], i0 + j);
+                }
+            }
+            release();
+        }
+        for (int64_t j = sp.tail0 + tid; j < vocab; j += NT) grad1(j);
+    }
+}
+
+template <typename T, int NW, int PER, int RING_KB, int MINB, bool kHint>
+void ring_launch(const void* logits, int64_t n_rows, int64_t vocab, int64_t stride, const int64_t* target,
+                 float eps, int64_t ignore_idx, const int64_t* n_valid, const float* grad_output, int reduce_loss,
+                 float* loss_rows, float* stats, void* dlogits, int* dev_status, cudaStream_t s,
+                 const DeviceInfo& dev) {
+    using C = RingCfg<NW, PER, RING_KB>;
+    auto kern = eps != 0.f ? ce_fused_ring<NW, PER, RING_KB, MINB, kHint, T, true>
+                           : ce_fused_ring<NW, PER, RING_KB, MINB, kHint, T, false>;
+    // the dynamic shared-memory limit is a per-device attribute of each kernel
+    static std::mutex mu;
+    static bool raised[2][64] = {};
+    const int k = eps != 0.f ? 1 : 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!raised[k][dev.ordinal]) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::kSmemBytes)) !=
+                cudaSuccess)
+                return;  // not launched: the caller's cudaGetLastError() reports the failure
+            raised[k][dev.ordinal] = true;
+        }
+    }
+    const int64_t cap = int64_t(dev.num_sms) * MINB;
+    const int grid = int(n_rows < cap ? n_rows : cap);
+    count_launch();
+    kern<<<grid, C::kThreads + 32, C::kSmemBytes, s>>>(
+        static_cast<const T*>(logits), n_rows, vocab, stride, target, eps, ignore_idx, n_valid, grad_output,
+        reduce_loss, loss_rows, reinterpret_cast<float2*>(stats), static_cast<T*>(dlogits), dev_status);
+}
+
 template <typename T, int THREADS, int MINB, int U1, int U2, bool kPrefetch>
 void fused_launch(const void* logits, int64_t n_rows, int64_t vocab, int64_t stride, const int64_t* target,
                   float eps, int64_t ignore_idx, const int64_t* n_valid, const float* grad_output,
@@ -645,13 +1005,19 @@ void fused_dispatch(const void* logits, int64_t n_rows, int64_t vocab, int64_t s
                     float eps, int64_t ignore_idx, const int64_t* n_valid, const float* grad_output,
                     int reduce_loss, float* loss_rows, float* stats, void* dlogits, int* dev_status,
                     cudaStream_t s, const DeviceInfo& dev) {
-    // The next-row prefetch doubles the rows resident in L2; it pays while both
-    // rows of every CTA leave most of L2 free and thrashes it beyond.  Rows up to
-    // 4096 vectors and rows up to ~100 KiB use the forward kernel's threads per
-    // row, so there the results equal ce_forward + ce_backward bit for bit;
-    // longer rows run fastest with one 1024-thread CTA per SM (measured at
-    // 16384 rows: 50257 BF16 0.57 ms with 2 x 512 + prefetch against 0.76 ms with
-    // 1024; 128256 BF16 1.42 ms with 1024 + prefetch against 1.57 ms with 2 x 512).
+    // Rows up to 4096 vectors: the forward kernel's threads per row, several CTAs
+    // per SM, next-row L2 prefetch while two rows per CTA leave a third of L2 free
+    // (the results equal ce_forward + ce_backward bit for bit).  Longer rows: the
+    // TMA-fed ring kernel.  Measured at 16384 rows of BF16 (fraction of the copy
+    // peak, against the previous 512/1024-thread row kernels with prefetch):
+    // rows up to 112 KiB run best with two CTAs of 8 compute warps and 96 KiB
+    // rings per SM (V = 40000: 0.89 against 0.85; 50257: 0.87 against 0.80);
+    // longer rows with one CTA of 16 compute warps, a 192 KiB ring and L2 hints
+    // that keep the first pass's bytes for the second (V = 65536: 0.88 against
+    // 0.86; 128256: 0.97 against 0.86; 151936: 0.93 against 0.79; FP32 50257:
+    // 0.93 against 0.80).  The 16-warp ring gives every thread the vectors the
+    // 512-thread forward gives it, in the same order, so those rows also equal
+    // ce_forward + ce_backward bit for bit.
     const int64_t nvec = vocab / Elem<T>::kVec;
     const double l2 = double(dev.l2_bytes), row = double(vocab) * double(sizeof(T));
     auto resident = [&](int grid, int rows_per_cta) { return double(grid) * rows_per_cta * row; };
@@ -665,16 +1031,10 @@ void fused_dispatch(const void* logits, int64_t n_rows, int64_t vocab, int64_t s
         const int grid = fused_grid(n_rows, dev.num_sms, 2);
         if (resident(grid, 2) <= l2 * 2.0 / 3.0) fused_launch<T, 256, 2, 4, 2, true>(VCE_FUSED_ARGS, grid);
         else fused_launch<T, 256, 4, 4, 2, false>(VCE_FUSED_ARGS, fused_grid(n_rows, dev.num_sms, 4));
+    } else if (nvec * 16 <= 112 * 1024) {
+        ring_launch<T, 8, 4, 96, 2, false>(VCE_FUSED_ARGS, dev);
     } else {
-        const int g512 = fused_grid(n_rows, dev.num_sms, 2), g1024 = fused_grid(n_rows, dev.num_sms, 1);
-        if (resident(g512, 2) <= l2 * 0.47)        // up to ~100 KiB rows: 2 x 512 threads, prefetch
-            fused_launch<T, 512, 2, 4, 2, true>(VCE_FUSED_ARGS, g512);
-        else if (resident(g512, 1) <= l2 * 0.35)   // up to ~150 KiB rows: 2 x 512 threads
-            fused_launch<T, 512, 2, 4, 2, false>(VCE_FUSED_ARGS, g512);
-        else if (resident(g1024, 2) <= l2 * 0.70)  // up to ~310 KiB rows: 1024 threads, prefetch
-            fused_launch<T, 1024, 1, 4, 4, true>(VCE_FUSED_ARGS, g1024);
-        else
-            fused_launch<T, 1024, 1, 4, 4, false>(VCE_FUSED_ARGS, g1024);
+        ring_launch<T, 16, 4, 192, 1, true>(VCE_FUSED_ARGS, dev);
     }
 #undef VCE_FUSED_ARGS
 }
