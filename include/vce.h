@@ -167,12 +167,12 @@ vce_status ce_backward(const void* logits, int dtype, int64_t n_rows, int64_t vo
  *
  *   Arguments are those of ce_forward and ce_backward combined; the results are
  *   those of ce_forward followed by ce_backward with the same grad_output (loss,
- *   stats, n_valid, dlogits): bit for bit for rows of at most 4096 16-byte
- *   vectors (64 KiB) and for rows of more than 112 KiB, where both calls give
- *   every thread the same elements in the same order; for rows in between this
- *   call splits a row's sum differently, so lse and the loss agree to FP32
- *   rounding (row maxima, n_valid and ignored rows exactly).  The call uses up
- *   to about 193 KiB of shared memory per CTA and raises the kernel's dynamic
+ *   stats, n_valid, dlogits): bit for bit for rows of at most 16 KiB, of 48 to
+ *   64 KiB and of more than 112 KiB, where both calls give every thread the
+ *   same elements in the same order; for other rows this call splits a row's
+ *   sum differently, so lse and the loss agree to FP32 rounding (row maxima,
+ *   n_valid and ignored rows exactly).  For rows above 16 KiB the call uses up
+ *   to about 193 KiB of shared memory per SM and raises its kernels' dynamic
  *   shared-memory limit on the first call on each device.  A timeout of its
  *   internal copy pipeline (not expected) sets VCE_DEVSTATUS_TIMEOUT and leaves
  *   the outputs undefined.  dlogits MAY EQUAL logits

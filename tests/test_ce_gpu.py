@@ -341,15 +341,18 @@ FUSED = [
     (40, 49152, "bf16", 0.1, True, False),
     (25, 98304, "f32", 0.0, 2, True),
     (130, 128256, "bf16", 0.0, False, True),
-    # several rows per persistent CTA on the TMA-fed ring kernel (rows of more than
-    # 4096 vectors): one CTA per SM with a 192 KiB ring (bf16 128 KiB rows, f32
-    # 512 KiB rows) and two CTAs per SM with 96 KiB rings (bf16 78 KiB rows)
+    # several rows per persistent CTA on the TMA-fed ring kernel (rows above 16 KiB):
+    # one CTA per SM with a 192 KiB ring (bf16 128 KiB rows, f32 512 KiB rows), two
+    # CTAs per SM with 96 KiB rings (bf16 78 and 59 KiB rows, f32 78 KiB rows) and
+    # four CTAs per SM with 48 KiB rings (bf16 39 and 23 KiB rows)
     (500, 65536, "bf16", 0.0, 2, True),
     (400, 131072, "f32", 0.1, True, False),
     (700, 40000, "bf16", 0.1, True, True),
+    (400, 30000, "bf16", 0.1, True, False),
     (333, 20001, "f32", 0.0, False, False),
-    # several rows per CTA with the prefetch on the 256- and 128-thread paths
     (1000, 20000, "bf16", 0.1, True, False),
+    (1500, 12000, "bf16", 0.0, 2, True),
+    # several rows per CTA with the next-row prefetch on the 128-thread path
     (3000, 1000, "bf16", 0.0, 2, True),
 ]
 
@@ -375,7 +378,7 @@ def test_fused_matches_oracle_and_separate_path(n, vocab, dtype, eps, red, inpla
 @pytest.mark.parametrize("n,vocab,pad,dtype,eps,red", [
     (200, 50001, 3, "bf16", 0.1, True),   # ring kernel, two CTAs per SM, rows off 16-byte alignment
     (400, 70001, 7, "bf16", 0.0, 2),      # ring kernel, one CTA per SM, rows off 16-byte alignment
-    (150, 9001, 5, "f32", 0.0, False),    # 256 threads per row
+    (150, 9001, 5, "f32", 0.0, False),    # ring kernel, four CTAs per SM
     (300, 129, 1, "bf16", 0.1, 2),        # 128 threads per row
 ])
 def test_fused_padded_rows(n, vocab, pad, dtype, eps, red):
@@ -400,7 +403,7 @@ def test_fused_padded_rows(n, vocab, pad, dtype, eps, red):
     check_rows(r, r.dlogits, ref, ref_dz, np.arange(n), dtype, red, target)
 
 
-@pytest.mark.parametrize("vocab,dtype", [(40000, "bf16"), (70001, "bf16"), (33000, "f32")])
+@pytest.mark.parametrize("vocab,dtype", [(40000, "bf16"), (70001, "bf16"), (33000, "f32"), (20003, "bf16")])
 def test_fused_ring_bad_and_ignored_rows(vocab, dtype):
     """Rows whose target is out of range get one pass through the ring kernel (their
     statistics) and a zero gradient, ignored rows none; the producer and the compute

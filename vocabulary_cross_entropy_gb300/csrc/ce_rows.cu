@@ -14,10 +14,10 @@
 // identical) and counts the rows whose target is not ignore_idx.
 // Fused forward + backward (for a caller that knows grad_output up front): each
 // row is read from HBM once and its gradient written once; the second read of
-// the row is served by L2.  Short rows: several CTAs per SM, each asking L2 for
-// its next row ahead of time.  Rows of more than 4096 16-byte vectors: a
-// persistent CTA per SM (or two) whose producer thread streams the row through
-// a shared-memory ring with TMA bulk copies.
+// the row is served by L2.  Rows up to 16 KiB: several CTAs per SM, each asking
+// L2 for its next row ahead of time.  Longer rows: one to four persistent CTAs
+// per SM whose producer thread streams the rows through a shared-memory ring
+// with TMA bulk copies.
 
 #include "vce_internal.cuh"
 #include "sm100_ptx.cuh"
@@ -1005,32 +1005,33 @@ void fused_dispatch(const void* logits, int64_t n_rows, int64_t vocab, int64_t s
                     float eps, int64_t ignore_idx, const int64_t* n_valid, const float* grad_output,
                     int reduce_loss, float* loss_rows, float* stats, void* dlogits, int* dev_status,
                     cudaStream_t s, const DeviceInfo& dev) {
-    // Rows up to 4096 vectors: the forward kernel's threads per row, several CTAs
-    // per SM, next-row L2 prefetch while two rows per CTA leave a third of L2 free
-    // (the results equal ce_forward + ce_backward bit for bit).  Longer rows: the
-    // TMA-fed ring kernel.  Measured at 16384 rows of BF16 (fraction of the copy
-    // peak, against the previous 512/1024-thread row kernels with prefetch):
-    // rows up to 112 KiB run best with two CTAs of 8 compute warps and 96 KiB
-    // rings per SM (V = 40000: 0.89 against 0.85; 50257: 0.87 against 0.80);
-    // longer rows with one CTA of 16 compute warps, a 192 KiB ring and L2 hints
-    // that keep the first pass's bytes for the second (V = 65536: 0.88 against
-    // 0.86; 128256: 0.97 against 0.86; 151936: 0.93 against 0.79; FP32 50257:
-    // 0.93 against 0.80).  The 16-warp ring gives every thread the vectors the
-    // 512-thread forward gives it, in the same order, so those rows also equal
-    // ce_forward + ce_backward bit for bit.
+    // Rows up to 1024 vectors (16 KiB): 128 threads per row, 8 CTAs per SM, and
+    // the next-row L2 prefetch while two rows per CTA take at most two thirds of
+    // L2.  Longer rows: the TMA-fed ring kernel, shaped by row length.  Measured
+    // at 16384 rows (fraction of the copy peak; in brackets the previous 256-,
+    // 512- and 1024-thread row kernels with next-row prefetch):
+    //   up to 48 KiB: four CTAs per SM, 4 compute warps, 48 KiB rings
+    //     (BF16 V = 12000: 0.69 [0.51]; 20000: 0.82 [0.65]; FP32 6000: 0.76 [0.59]);
+    //   up to 112 KiB: two CTAs per SM, 8 compute warps, 96 KiB rings
+    //     (BF16 32000: 0.84 [0.80]; 50257: 0.87 [0.80]; FP32 16000: 0.88 [0.85]);
+    //   longer: one CTA per SM, 16 compute warps, a 192 KiB ring and L2 hints
+    //     that keep the first pass's bytes for the second (BF16 65536: 0.88
+    //     [0.86]; 128256: 0.97 [0.86]; 151936: 0.93 [0.79]; FP32 50257: 0.93 [0.80]).
+    // Where a ring has as many compute threads as the forward kernel has threads
+    // per row, every thread takes the same vectors in the same order, so those
+    // rows equal ce_forward + ce_backward bit for bit: rows of 48-64 KiB (8 warps,
+    // the forward's 256 threads) and rows above 112 KiB (16 warps, its 512), as
+    // the rows up to 16 KiB do.
     const int64_t nvec = vocab / Elem<T>::kVec;
     const double l2 = double(dev.l2_bytes), row = double(vocab) * double(sizeof(T));
-    auto resident = [&](int grid, int rows_per_cta) { return double(grid) * rows_per_cta * row; };
 #define VCE_FUSED_ARGS logits, n_rows, vocab, stride, target, eps, ignore_idx, n_valid, grad_output, reduce_loss, \
                        loss_rows, stats, dlogits, dev_status, s
     if (nvec <= 1024) {
         const int grid = fused_grid(n_rows, dev.num_sms, 8);
-        if (resident(grid, 2) <= l2 * 2.0 / 3.0) fused_launch<T, 128, 8, 4, 2, true>(VCE_FUSED_ARGS, grid);
+        if (double(grid) * 2 * row <= l2 * 2.0 / 3.0) fused_launch<T, 128, 8, 4, 2, true>(VCE_FUSED_ARGS, grid);
         else fused_launch<T, 128, 8, 4, 2, false>(VCE_FUSED_ARGS, grid);
-    } else if (nvec <= 4096) {
-        const int grid = fused_grid(n_rows, dev.num_sms, 2);
-        if (resident(grid, 2) <= l2 * 2.0 / 3.0) fused_launch<T, 256, 2, 4, 2, true>(VCE_FUSED_ARGS, grid);
-        else fused_launch<T, 256, 4, 4, 2, false>(VCE_FUSED_ARGS, fused_grid(n_rows, dev.num_sms, 4));
+    } else if (nvec * 16 <= 48 * 1024) {
+        ring_launch<T, 4, 4, 48, 4, false>(VCE_FUSED_ARGS, dev);
     } else if (nvec * 16 <= 112 * 1024) {
         ring_launch<T, 8, 4, 96, 2, false>(VCE_FUSED_ARGS, dev);
     } else {
