@@ -40,12 +40,24 @@ def test_all_entry_points_replay_in_a_cuda_graph():
     lws = torch.empty(vce.lce_workspace_size(n, h, vl, True), dtype=torch.uint8, device=DEV)
     dx, dw = torch.empty_like(x), torch.empty_like(w)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    # ce_forward_backward on the short-row kernel (v = 5003) and on two ring shapes
+    fused = []
+    for vf in (5003, 40000, 70001):
+        zf = _bf16(wk.normal_matrix(7, wk.TID_LOGITS, n, vf, 3.0, True))
+        yf = torch.from_numpy(wk.uniform_targets(7, n, vf, 0.1)).to(DEV)
+        fused.append((zf, yf, torch.empty(1, device=DEV), torch.empty(n, 2, device=DEV),
+                      torch.empty(1, dtype=torch.int64, device=DEV),
+                      torch.empty(vce.ce_workspace_size(n, vf, True), dtype=torch.uint8, device=DEV),
+                      torch.empty_like(zf)))
 
     def step():
         vce.ce_forward(z, y, 0.1, True, loss=loss, stats=stats, n_valid=nv, workspace=ws, dev_status=status)
         vce.ce_backward(z, y, stats, nv, g, 0.1, True, dlogits=dz, dev_status=status)
         vce.lce_forward(x, w, yl, 0.0, True, loss=lloss, lse=lse, n_valid=lnv, workspace=lws, dev_status=status)
         vce.lce_backward(x, w, yl, lse, lnv, g, 0.0, True, dX=dx, dW=dw, workspace=lws, dev_status=status)
+        for zf, yf, fl, fs, fn, fw, fd in fused:
+            vce.ce_forward_backward(zf, yf, g, 0.1, True, dlogits=fd, loss=fl, stats=fs, n_valid=fn,
+                                    workspace=fw, dev_status=status)
 
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
@@ -53,8 +65,9 @@ def test_all_entry_points_replay_in_a_cuda_graph():
         step()  # eager run first: per-kernel attributes are set outside the capture
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
-    eager = [t.clone() for t in (loss, stats, dz, lloss, lse, dx, dw)]
-    for t in (loss, stats, dz, lloss, lse, dx, dw):
+    outs = [loss, stats, dz, lloss, lse, dx, dw] + [t for f in fused for t in (f[2], f[3], f[6])]
+    eager = [t.clone() for t in outs]
+    for t in outs:
         t.zero_()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
@@ -62,7 +75,7 @@ def test_all_entry_points_replay_in_a_cuda_graph():
     for _ in range(2):
         graph.replay()
     torch.cuda.synchronize()
-    for a, b in zip(eager, (loss, stats, dz, lloss, lse, dx, dw)):
+    for a, b in zip(eager, outs):
         assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a,
                            b.view(torch.int16) if b.dtype == torch.bfloat16 else b)
     assert int(status.item()) == 0
