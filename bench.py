@@ -357,6 +357,37 @@ def time_steps(step, steps, warmup, pg, events_for=("forward", "backward")):
     return total, phases
 
 
+def time_graph_replay(step, k, warmup):
+    """Mean us of one forward + backward step captured once in a CUDA graph and
+    replayed ``k`` times (every library call is capturable: no allocation, no host
+    synchronisation); the replays show the device time without the per-call host
+    overhead of the Python binding."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(warmup):
+            step.forward()
+            step.backward()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step.forward()
+        step.backward()
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(k):
+        graph.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return 1e3 * a.elapsed_time(b) / k
+
+
 def peak_extra_memory(step):
     """Peak device memory one forward + backward call adds beyond inputs, weights and final
     outputs (loss, dX, dW): workspace, lse and the small state, allocated on demand through
@@ -969,6 +1000,7 @@ def main():
         tiny = LogitsStep(wk.LOGITS_TINY[3], dev)
         kt = 100
         tt, pht = time_steps(tiny, kt, args.warmup, pg)
+        graph_us = time_graph_replay(tiny, kt, args.warmup)
         assert int(tiny.status.item()) == 0, "device status reported an error"
         sm = LinearStep(wk.LINEAR_SMALL, dev)
         ks = max(3, args.steps // 3)
@@ -978,8 +1010,10 @@ def main():
         line["small_configs"] = {
             "logits_tiny": {"workload": tiny.wl.name, "n_rows": tiny.wl.n_rows, "vocab": tiny.wl.vocab,
                             "dtype": "f32", "us_per_step": 1e3 * tt / kt, "fwd_us": 1e3 * pht["forward"],
-                            "bwd_us": 1e3 * pht["backward"], "steps": kt,
-                            "note": "ce_forward (+ mean) + ce_backward; launch-latency bound"},
+                            "bwd_us": 1e3 * pht["backward"], "steps": kt, "graph_us_per_step": graph_us,
+                            "note": "ce_forward (+ mean) + ce_backward; launch-latency bound when called "
+                                    "from Python one by one; graph_us_per_step replays the step captured "
+                                    "in a CUDA graph"},
             "linear_small": {"workload": sm.wl.name, "value": sm.units() * world * ks / (tsm / 1e3),
                              "unit": "TFLOP/s", "ms_per_step": tsm / ks, "fwd_ms": phm["forward"],
                              "bwd_ms": phm["backward"], "steps": ks, "clocks": ckm.summary()},
