@@ -579,7 +579,28 @@ lce_combine_kernel(const float2* __restrict__ part_ms, const float* __restrict__
     const bool want_t = entropy_out != nullptr;
     float m = -INFINITY, s = 0.f, u = 0.f, t = 0.f;
     if (row < n) {
-        for (int b = sp; b < nb; b += kCombSplit) {
+        // eight partials per batch with every load issued before the merges (the
+        // merge order is unchanged): a load per dependent merge left each load's
+        // latency exposed, 35.5 against 16.0 us at 4096 rows x 512 tiles
+        constexpr int U = 8;
+        int b = sp;
+        for (; b + (U - 1) * kCombSplit < nb; b += U * kCombSplit) {
+            float2 p[U];
+            float pt[U], pu[U];
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                const int64_t idx = int64_t(b + k * kCombSplit) * n + row;
+                p[k] = part_ms[idx];
+                pt[k] = want_t ? part_t[idx] : 0.f;
+                pu[k] = eps != 0.f ? part_sum[idx] : 0.f;
+            }
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                lse_merge(m, s, t, p[k].x, p[k].y, pt[k]);
+                if (eps != 0.f) u += pu[k];
+            }
+        }
+        for (; b < nb; b += kCombSplit) {
             const float2 p = part_ms[int64_t(b) * n + row];
             lse_merge(m, s, t, p.x, p.y, want_t ? part_t[int64_t(b) * n + row] : 0.f);
             if (eps != 0.f) u += part_sum[int64_t(b) * n + row];
