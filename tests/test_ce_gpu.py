@@ -378,6 +378,7 @@ def test_fused_matches_oracle_and_separate_path(n, vocab, dtype, eps, red, inpla
 @pytest.mark.parametrize("n,vocab,pad,dtype,eps,red", [
     (200, 50001, 3, "bf16", 0.1, True),   # ring kernel, two CTAs per SM, rows off 16-byte alignment
     (400, 70001, 7, "bf16", 0.0, 2),      # ring kernel, one CTA per SM, rows off 16-byte alignment
+    (160, 205003, 3, "bf16", 0.1, True),  # ring kernel with the row's first 64 KiB pinned, rows off alignment
     (150, 9001, 5, "f32", 0.0, False),    # ring kernel, four CTAs per SM
     (300, 129, 1, "bf16", 0.1, 2),        # 128 threads per row
 ])
@@ -403,12 +404,13 @@ def test_fused_padded_rows(n, vocab, pad, dtype, eps, red):
     check_rows(r, r.dlogits, ref, ref_dz, np.arange(n), dtype, red, target)
 
 
-@pytest.mark.parametrize("vocab,dtype", [(40000, "bf16"), (70001, "bf16"), (33000, "f32"), (20003, "bf16")])
-def test_fused_ring_bad_and_ignored_rows(vocab, dtype):
+@pytest.mark.parametrize("vocab,dtype,n", [(40000, "bf16", 1000), (70001, "bf16", 1000), (33000, "f32", 1000),
+                                           (20003, "bf16", 1000), (210001, "bf16", 400)])
+def test_fused_ring_bad_and_ignored_rows(vocab, dtype, n):
     """Rows whose target is out of range get one pass through the ring kernel (their
     statistics) and a zero gradient, ignored rows none; the producer and the compute
-    warps must agree on that sequence for every later row to be right."""
-    n = 1000
+    warps must agree on that sequence for every later row to be right (for the
+    longest rows also on the pinned area, released after a bad row's one pass)."""
     seed = 11 + vocab
     z = wk.normal_matrix(seed, wk.TID_LOGITS, n, vocab, 3.0, dtype == "bf16")
     target = wk.uniform_targets(seed, n, vocab, 0.1)

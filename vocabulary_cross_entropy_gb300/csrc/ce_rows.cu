@@ -694,15 +694,20 @@ __device__ __forceinline__ void compute_merge(OnlineLse& a, float* sm_m, float* 
 constexpr uint64_t kRingTimeoutNs = 2000000000ull;  // 2 s per wait
 
 // NW compute warps, each thread taking PER 16-byte vectors of every full
-// chunk; RING_KB KiB of shared memory in equal chunks.
-template <int NW, int PER, int RING_KB>
+// chunk; RING_KB KiB of shared memory in equal chunks, and PIN_KB KiB more that
+// keep the first chunks of the current row for its second pass.
+template <int NW, int PER, int RING_KB, int PIN_KB = 0>
 struct RingCfg {
     static constexpr int kThreads = NW * 32;                        // compute threads
     static constexpr uint32_t kChunk = uint32_t(kThreads) * PER * 16;  // bytes per ring slot
     static constexpr int kSlots = int(uint32_t(RING_KB) * 1024 / kChunk);
-    static constexpr size_t kSmemBytes = size_t(kSlots) * kChunk + 2 * kSlots * 8 + (3 * 32 + 2) * 4;
+    static constexpr int kPins = int(uint32_t(PIN_KB) * 1024 / kChunk);  // chunks kept for the second pass
+    static constexpr size_t kSmemBytes =
+        size_t(kSlots + kPins) * kChunk + (2 * kSlots + 2) * 8 + (3 * 32 + 2) * 4;
     static_assert(kSlots >= 2 && kSlots <= 16, "ring depth");
 };
+
+__device__ __forceinline__ uint64_t min_u64(uint64_t a, uint64_t b) { return a < b ? a : b; }
 
 // Bounded wait that ignores the abort flag (draining copies still in flight).
 __device__ __forceinline__ bool ring_drain_wait(uint64_t* bar, uint32_t parity) {
@@ -726,28 +731,39 @@ __device__ __forceinline__ bool ring_drain_wait(uint64_t* bar, uint32_t parity) 
 // first 16-byte boundary and after the last are read directly.  With kHint the
 // first pass's copies ask L2 to keep the row's lines (evict_last) and the second
 // pass's to drop them first (evict_first), so the next row's first-pass reads do
-// not push out lines the second pass still needs.
+// not push out lines the second pass still needs.  With PIN_KB > 0 the first
+// chunks of each row are copied once into a separate pinned area instead of the
+// ring and stay there until the second pass has read them, so the second pass
+// reads that much of the row from shared memory and each row holds less of L2
+// (it pays for rows of some 400 KiB and more, whose lines otherwise start to
+// leave L2 before their second read); the pinned area is released as soon as
+// the second pass has used it, and the next row's first chunks are copied in
+// while the rest of the row goes through the ring.
 // Every wait is bounded: on timeout the CTA sets its abort flag, every role
 // stops waiting, the producer waits for the copies it issued, and
 // VCE_DEVSTATUS_TIMEOUT is reported (the outputs are then undefined).
-template <int NW, int PER, int RING_KB, int MINB, bool kHint, typename T, bool kSmooth>
+template <int NW, int PER, int RING_KB, int MINB, bool kHint, typename T, bool kSmooth, int PIN_KB = 0>
 __global__ void __launch_bounds__(NW * 32 + 32, MINB)
 ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, const int64_t* __restrict__ target,
               float eps, int64_t ignore_idx, const int64_t* __restrict__ n_valid,
               const float* __restrict__ grad_output, int reduce_loss, float* __restrict__ loss_rows,
               float2* __restrict__ stats, T* dlogits, int* dev_status) {
     using E = Elem<T>;
-    using C = RingCfg<NW, PER, RING_KB>;
+    using C = RingCfg<NW, PER, RING_KB, PIN_KB>;
     using namespace sm100;
     constexpr int V = E::kVec;
     constexpr int NT = C::kThreads;
     constexpr uint32_t CH = C::kChunk;
     constexpr int S = C::kSlots;
+    constexpr int P = C::kPins;
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t* ring = smem;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(S) * CH);
+    uint8_t* pin = smem + size_t(S) * CH;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(S + P) * CH);
     uint64_t* empty = full + S;
-    float* sm_m = reinterpret_cast<float*>(empty + S);
+    uint64_t* pin_full = empty + S;
+    uint64_t* pin_empty = pin_full + 1;
+    float* sm_m = reinterpret_cast<float*>(pin_empty + 1);
     float* sm_s = sm_m + 32;
     float* sm_sum = sm_s + 32;
     float* sm_lse = sm_sum + 32;
@@ -759,6 +775,8 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], NW);
         }
+        mbar_init(pin_full, 1);
+        mbar_init(pin_empty, NW);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -767,7 +785,7 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
     if (tid >= NT) {
         // ---------------- producer ----------------
         if (tid != NT) return;
-        uint32_t slot = 0, ph = 0, issued = 0;
+        uint32_t slot = 0, ph = 0, issued = 0, pin_ph = 0, pin_issued = 0;
         bool ok = true;
         const uint64_t keep = kHint ? l2_policy_evict_last() : 0, drop = kHint ? l2_policy_evict_first() : 0;
         for (int64_t row = blockIdx.x; row < n_rows && ok; row += gridDim.x) {
@@ -778,8 +796,28 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
             const RowSplit<T> sp(p, vocab);
             const uint64_t total = uint64_t(sp.nvec) * 16;
             const uint8_t* src = reinterpret_cast<const uint8_t*>(p + sp.head);
+            const uint64_t nch = (total + CH - 1) / CH;
+            const uint64_t np = min_u64(nch, uint64_t(P));
+            if (np > 0) {
+                // the row's first np chunks go to the pinned area, kept for the second pass
+                if (!mbar_wait(pin_empty, pin_ph ^ 1, abort_flag, kRingTimeoutNs)) {
+                    ok = false;
+                    break;
+                }
+                const uint64_t pbytes = total < np * CH ? total : np * CH;
+                mbar_arrive_expect_tx(pin_full, uint32_t(pbytes));
+                for (uint64_t k = 0; k < np; ++k) {
+                    const uint32_t bytes = uint32_t(total - k * CH < CH ? total - k * CH : CH);
+                    if (kHint)
+                        bulk_load_shared_hint(smem_u32(pin + k * CH), src + k * CH, bytes, smem_u32(pin_full), drop);
+                    else
+                        bulk_load_shared(smem_u32(pin + k * CH), src + k * CH, bytes, smem_u32(pin_full));
+                }
+                pin_ph ^= 1;
+                ++pin_issued;
+            }
             for (int pass = 0; pass < (bad ? 1 : 2) && ok; ++pass) {
-                for (uint64_t off = 0; off < total; off += CH) {
+                for (uint64_t off = np * CH; off < total; off += CH) {
                     if (!mbar_wait(&empty[slot], ph ^ 1, abort_flag, kRingTimeoutNs)) {
                         ok = false;
                         break;
@@ -806,13 +844,14 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
             const uint32_t last = i + ((issued - 1 - i) / S) * S;
             ring_drain_wait(&full[i], (last / S) & 1);
         }
+        if (pin_issued > 0) ring_drain_wait(pin_full, (pin_issued - 1) & 1);
         if (!ok) report(dev_status, VCE_DEVSTATUS_TIMEOUT);
         return;
     }
 
     // ---------------- compute warps ----------------
     const int lane = tid & 31;
-    uint32_t slot = 0, ph = 0;
+    uint32_t slot = 0, ph = 0, pin_ph = 0;
     bool ok = true;
     // wait for the next chunk; false once this CTA has given up
     auto take = [&]() -> bool {
@@ -842,6 +881,8 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
         }
         const bool bad = y < 0 || y >= vocab;
         const uint64_t total = uint64_t(sp.nvec) * 16;
+        const uint64_t nch = (total + CH - 1) / CH;
+        const uint64_t np = min_u64(nch, uint64_t(P));
 
         // pass 1: online (max, sum exp) and sum of logits
         OnlineLse acc;
@@ -849,7 +890,21 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
             float v[1] = {E::load1(p + tid)};
             acc.push<1, kSmooth>(v);
         }
-        for (uint64_t off = 0; off < total; off += CH) {
+        if (np > 0) {
+            if (ok && !mbar_wait(pin_full, pin_ph, abort_flag, kRingTimeoutNs)) ok = false;
+            if (ok) {
+                for (uint64_t k = 0; k < np; ++k) {
+                    const uint4* src = reinterpret_cast<const uint4*>(pin + k * CH);
+                    const uint32_t nv = uint32_t(total - k * CH < CH ? total - k * CH : CH) / 16;
+                    for (uint32_t j = tid; j < nv; j += NT) {
+                        float v[V];
+                        E::unpack(src[j], v);
+                        acc.push<V, kSmooth>(v);
+                    }
+                }
+            }
+        }
+        for (uint64_t off = np * CH; off < total; off += CH) {
             if (take()) {
                 const uint4* src = reinterpret_cast<const uint4*>(ring + size_t(slot) * CH);
                 if (total - off >= CH) {
@@ -894,7 +949,15 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
             *sm_lse = lse;
         }
         compute_sync<NT>();
+        auto release_pin = [&]() {
+            if (np > 0) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(pin_empty);
+                pin_ph ^= 1;
+            }
+        };
         if (bad) {
+            release_pin();
             row_zero<NT, T>(q, sp, vocab);
             continue;
         }
@@ -925,7 +988,16 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
             }
             __stcs(qv + i, E::pack(v));
         };
-        for (uint64_t off = 0; off < total; off += CH) {
+        if (np > 0 && ok) {
+            for (uint64_t k = 0; k < np; ++k) {
+                const uint4* src = reinterpret_cast<const uint4*>(pin + k * CH);
+                const uint32_t nv = uint32_t(total - k * CH < CH ? total - k * CH : CH) / 16;
+                const int64_t i0 = int64_t(k * CH / 16);
+                for (uint32_t j = tid; j < nv; j += NT) gradv(src[j], i0 + j);
+            }
+        }
+        release_pin();
+        for (uint64_t off = np * CH; off < total; off += CH) {
             if (take()) {
                 const uint4* src = reinterpret_cast<const uint4*>(ring + size_t(slot) * CH);
                 const int64_t i0 = int64_t(off / 16);
@@ -946,14 +1018,14 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
     }
 }
 
-template <typename T, int NW, int PER, int RING_KB, int MINB, bool kHint>
+template <typename T, int NW, int PER, int RING_KB, int MINB, bool kHint, int PIN_KB = 0>
 void ring_launch(const void* logits, int64_t n_rows, int64_t vocab, int64_t stride, const int64_t* target,
                  float eps, int64_t ignore_idx, const int64_t* n_valid, const float* grad_output, int reduce_loss,
                  float* loss_rows, float* stats, void* dlogits, int* dev_status, cudaStream_t s,
                  const DeviceInfo& dev) {
-    using C = RingCfg<NW, PER, RING_KB>;
-    auto kern = eps != 0.f ? ce_fused_ring<NW, PER, RING_KB, MINB, kHint, T, true>
-                           : ce_fused_ring<NW, PER, RING_KB, MINB, kHint, T, false>;
+    using C = RingCfg<NW, PER, RING_KB, PIN_KB>;
+    auto kern = eps != 0.f ? ce_fused_ring<NW, PER, RING_KB, MINB, kHint, T, true, PIN_KB>
+                           : ce_fused_ring<NW, PER, RING_KB, MINB, kHint, T, false, PIN_KB>;
     // the dynamic shared-memory limit is a per-device attribute of each kernel
     static std::mutex mu;
     static bool raised[2][64] = {};
@@ -1014,9 +1086,13 @@ void fused_dispatch(const void* logits, int64_t n_rows, int64_t vocab, int64_t s
     //     (BF16 V = 12000: 0.69 [0.51]; 20000: 0.82 [0.65]; FP32 6000: 0.76 [0.59]);
     //   up to 112 KiB: two CTAs per SM, 8 compute warps, 96 KiB rings
     //     (BF16 32000: 0.84 [0.80]; 50257: 0.87 [0.80]; FP32 16000: 0.88 [0.85]);
-    //   longer: one CTA per SM, 16 compute warps, a 192 KiB ring and L2 hints
-    //     that keep the first pass's bytes for the second (BF16 65536: 0.88
-    //     [0.86]; 128256: 0.97 [0.86]; 151936: 0.93 [0.79]; FP32 50257: 0.93 [0.80]).
+    //   up to 400 KiB: one CTA per SM, 16 compute warps, a 192 KiB ring and L2
+    //     hints that keep the first pass's bytes for the second (BF16 65536:
+    //     0.88 [0.86]; 128256: 0.97 [0.86]; 151936: 0.93 [0.79]; FP32 50257: 0.93
+    //     [0.80]);
+    //   longer: the same with a 128 KiB ring and the first 64 KiB of each row
+    //     pinned in shared memory for the second pass (BF16 256000: 0.89 against
+    //     0.81 with the 192 KiB ring alone; FP32 128256: 0.89 against 0.83).
     // Where a ring has as many compute threads as the forward kernel has threads
     // per row, every thread takes the same vectors in the same order, so those
     // rows equal ce_forward + ce_backward bit for bit: rows of 48-64 KiB (8 warps,
@@ -1034,8 +1110,10 @@ void fused_dispatch(const void* logits, int64_t n_rows, int64_t vocab, int64_t s
         ring_launch<T, 4, 4, 48, 4, false>(VCE_FUSED_ARGS, dev);
     } else if (nvec * 16 <= 112 * 1024) {
         ring_launch<T, 8, 4, 96, 2, false>(VCE_FUSED_ARGS, dev);
-    } else {
+    } else if (nvec * 16 <= 400 * 1024) {
         ring_launch<T, 16, 4, 192, 1, true>(VCE_FUSED_ARGS, dev);
+    } else {
+        ring_launch<T, 16, 4, 128, 1, true, 64>(VCE_FUSED_ARGS, dev);
     }
 #undef VCE_FUSED_ARGS
 }
