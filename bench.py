@@ -835,6 +835,10 @@ def main():
                     help="linear workload N,H,V instead of the headline (e.g. a small profiling case)")
     ap.add_argument("--logits-rows", type=int, default=None,
                     help="rows of the logits workload instead of 4 x 4096 (profiling)")
+    ap.add_argument("--logits-vocab", type=int, default=None,
+                    help="vocabulary of the logits workload instead of 128256 (profiling)")
+    ap.add_argument("--logits-dtype", choices=("bf16", "f32"), default=None,
+                    help="logits dtype instead of bf16 (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -855,10 +859,12 @@ def main():
     logits_obj = None
     if args.workload in ("logits", "both"):
         lwl = wk.LOGITS_MEMBOUND
-        if args.logits_rows:
+        if args.logits_rows or args.logits_vocab or args.logits_dtype:
             import dataclasses
-            lwl = dataclasses.replace(lwl, n_rows=args.logits_rows,
-                                      name=f"logits_{args.logits_rows}x{lwl.vocab}")
+            lwl = dataclasses.replace(lwl, n_rows=args.logits_rows or lwl.n_rows,
+                                      vocab=args.logits_vocab or lwl.vocab, dtype=args.logits_dtype or lwl.dtype)
+            lwl = dataclasses.replace(lwl, name=f"logits_{lwl.n_rows}x{lwl.vocab}" +
+                                      ("" if lwl.dtype == "bf16" else "_" + lwl.dtype))
         st = LogitsStep(lwl, dev)
         with Clocks(local) as ck:
             total, ph = time_steps(st, args.steps, args.warmup, pg)
@@ -874,9 +880,10 @@ def main():
             "ms_per_step": total / args.steps, "fwd_gbs": fwd_gbs, "bwd_gbs": bwd_gbs,
             "fwd_ms": ph["forward"], "bwd_ms": ph["backward"],
             "config": {"workload": st.wl.name, "n_rows": st.wl.n_rows, "vocab": st.wl.vocab,
-                       "dtype": "bf16", "label_smoothing": st.wl.label_smoothing,
+                       "dtype": st.wl.dtype, "label_smoothing": st.wl.label_smoothing,
                        "reduce_loss": st.wl.reduce_loss, "n_valid": st.n_valid_count,
-                       "l2": "inputs larger than L2 (4.2 GB logits), no flush"},
+                       "l2": "inputs larger than L2 (%.2f GB logits), no flush" % (
+                           st.wl.n_rows * st.wl.vocab * st.d["logits"].element_size() / 1e9)},
             "roofline": {"kernel": "ce_backward_rows", "bound": "hbm", "achieved": bwd_gbs,
                          "peak": pk["hbm"], "unit": "GB/s", "frac": bwd_gbs / pk["hbm"],
                          "traffic": LOGITS_TRAFFIC_BYTES(st.wl, "backward"),
@@ -904,7 +911,7 @@ def main():
         line = dict(logits_obj)
         line.update({"n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                      "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                     "dtype": "bf16", "data": "synthetic"})
+                     "dtype": lwl.dtype, "data": "synthetic"})
         if args.vocab_sweep:
             torch.cuda.empty_cache()
             line["vocab_sweep"] = vocab_sweep(dev, args, pg, pk)
