@@ -767,7 +767,7 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
     float* sm_s = sm_m + 32;
     float* sm_sum = sm_s + 32;
     float* sm_lse = sm_sum + 32;
-    int* abort_flag = reinterpret_cast<int*>(sm_lse + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm_lse + 1);
     const int tid = threadIdx.x;
 
     if (tid == 0) {
@@ -845,7 +845,7 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
             ring_drain_wait(&full[i], (last / S) & 1);
         }
         if (pin_issued > 0) ring_drain_wait(pin_full, (pin_issued - 1) & 1);
-        if (!ok) report(dev_status, VCE_DEVSTATUS_TIMEOUT);
+        if (!ok || *abort_flag) report(dev_status, VCE_DEVSTATUS_TIMEOUT);
         return;
     }
 
@@ -1016,6 +1016,9 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
         }
         for (int64_t j = sp.tail0 + tid; j < vocab; j += NT) grad1(j);
     }
+    // a compute thread whose wait gave up reports it too: the producer may have
+    // issued its last copy and returned before the CTA gave up
+    if (!ok) report(dev_status, VCE_DEVSTATUS_TIMEOUT);
 }
 
 template <typename T, int NW, int PER, int RING_KB, int MINB, bool kHint, int PIN_KB = 0>
