@@ -1,8 +1,8 @@
 """ctypes wrapper of the plain-C FP64 oracle (oracle/vce_oracle.c).
 
 TEST INFRASTRUCTURE ONLY: a second, independent implementation of the logits
-form (and the linear form's product) that the tests compare with the NumPy
-oracle.  Built with gcc into oracle/_build/libvce_oracle.so.
+form and of the linear form's product, gradients and entropy, which the tests
+compare with the NumPy oracle.  Built with gcc into oracle/_build/libvce_oracle.so.
 """
 from __future__ import annotations
 
@@ -48,6 +48,10 @@ def _load():
         lib.oracle_ce_backward.restype = None
         lib.oracle_linear_logits.argtypes = [P, P, I64, I64, I64, P]
         lib.oracle_linear_logits.restype = None
+        lib.oracle_linear_grads.argtypes = [P, P, P, I64, I64, I64, P, P]
+        lib.oracle_linear_grads.restype = None
+        lib.oracle_entropy.argtypes = [P, I64, I64, P, P]
+        lib.oracle_entropy.restype = None
         _lib = lib
     return _lib
 
@@ -87,3 +91,24 @@ def linear_logits(x, w):
     z = np.empty((n, v))
     _load().oracle_linear_logits(_p(x), _p(w), n, h, v, _p(z))
     return z
+
+
+def linear_grads(dz, x, w):
+    """dX = dZ W and dW = dZ^T X in float64."""
+    dz = np.ascontiguousarray(dz, dtype=np.float64)
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    n, h = x.shape
+    v = w.shape[0]
+    dx, dw = np.empty((n, h)), np.empty((v, h))
+    _load().oracle_linear_grads(_p(dz), _p(x), _p(w), n, h, v, _p(dx), _p(dw))
+    return dx, dw
+
+
+def entropy(z, lse):
+    z = np.ascontiguousarray(z, dtype=np.float64)
+    lse = np.ascontiguousarray(lse, dtype=np.float64)
+    n, v = z.shape
+    ent = np.empty(n)
+    _load().oracle_entropy(_p(z), n, v, _p(lse), _p(ent))
+    return ent

@@ -16,7 +16,10 @@
  *   y_n outside [0, V) and not ignore_idx: loss NaN, gradient 0, flagged.
  *
  *   Linear form (Cut Cross-Entropy card "what_it_does"): z = X W^T, a naive
- *   triple loop.
+ *   triple loop; its gradients (Liger SM100 pull request "Summary": backward =
+ *   logits recomputation, dX, dW) dX = dZ W and dW = dZ^T X, naive loops.
+ *   Per-token entropy of the softmax (Liger pull request, optional entropy):
+ *     H_n = -sum_v p_v log p_v = lse_n - sum_v p_v z[n, v],  p_v = exp(z[n, v] - lse_n).
  *
  * Build: gcc -O2 -fPIC -shared -fopenmp (see oracle/c_oracle.py).
  */
@@ -93,4 +96,33 @@ void oracle_linear_logits(const double* X, const double* W, int64_t n, int64_t H
             for (int64_t k = 0; k < H; ++k) acc += X[r * H + k] * W[v * H + k];
             z[r * V + v] = acc;
         }
+}
+
+/* dX[n, H] = dZ[n, V] W[V, H] and dW[V, H] = dZ^T X, naive. */
+void oracle_linear_grads(const double* dz, const double* X, const double* W, int64_t n, int64_t H, int64_t V,
+                         double* dX, double* dW) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < n; ++r)
+        for (int64_t k = 0; k < H; ++k) {
+            double acc = 0.0;
+            for (int64_t v = 0; v < V; ++v) acc += dz[r * V + v] * W[v * H + k];
+            dX[r * H + k] = acc;
+        }
+#pragma omp parallel for schedule(static)
+    for (int64_t v = 0; v < V; ++v)
+        for (int64_t k = 0; k < H; ++k) {
+            double acc = 0.0;
+            for (int64_t r = 0; r < n; ++r) acc += dz[r * V + v] * X[r * H + k];
+            dW[v * H + k] = acc;
+        }
+}
+
+/* Entropy of each row's softmax from its logits and lse: ent[n]. */
+void oracle_entropy(const double* z, int64_t n, int64_t V, const double* lse, double* ent) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < n; ++r) {
+        double pz = 0.0;
+        for (int64_t v = 0; v < V; ++v) pz += exp(z[r * V + v] - lse[r]) * z[r * V + v];
+        ent[r] = lse[r] - pz;
+    }
 }
