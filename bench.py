@@ -51,10 +51,11 @@ PUBLISHED_MODEL_SHAPES_FB_MS = {"qwen3_30b_a3b_8192x2048x151936": 13.692,
 
 
 def FWD_GEMM_TRAFFIC_BYTES(wl):
-    """DRAM bytes (read + write) per launch of the forward GEMM, from the full-size ncu
-    capture in profiles/tc_gemm_traffic_headline_and_16384_tokens.md (N = H = 4096,
-    V = 131072), scaled to this workload's V: the X bytes stay, the W bytes and the
-    per-tile partials grow with V.  None for workloads outside that N = H = 4096 family."""
+    """DRAM bytes (read + write) per launch of the forward GEMM, from a one-pass ncu
+    capture (dram__bytes_read.sum, dram__bytes_write.sum) of a full-size launch at
+    N = H = 4096, V = 131072, scaled to this workload's V: the X bytes stay, the W
+    bytes and the per-tile partials grow with V.  None for workloads outside that
+    N = H = 4096 family."""
     captured_v, read_bytes, write_bytes = 131072, 1.108554752e9, 19.760128e6
     if wl.n != 4096 or wl.hidden != 4096:
         return None
@@ -63,9 +64,9 @@ def FWD_GEMM_TRAFFIC_BYTES(wl):
     return x_bytes + (read_bytes - x_bytes) * scale + write_bytes * scale
 
 
-# DRAM bytes (read, write) per launch of the logits-form row kernels, from the ncu
-# captures in profiles/ce_rows_logits_2048x128256.md and
-# profiles/ce_fused_ring_logits_2048x128256.md (2048 rows of V = 128256 BF16, 5% ignored)
+# DRAM bytes (read, write) per launch of the logits-form row kernels, from ncu
+# captures (dram__bytes_read.sum, dram__bytes_write.sum) of 2048 rows of
+# V = 128256 BF16 with 5% of the rows ignored
 LOGITS_CAPTURED_TRAFFIC = {
     "forward": (502.397952e6, 3.326976e6),
     "backward": (502.323968e6, 467.554560e6),

@@ -342,10 +342,12 @@ FUSED = [
     (25, 98304, "f32", 0.0, 2, True),
     (130, 128256, "bf16", 0.0, False, True),
     # several rows per persistent CTA on the TMA-fed ring kernel (rows above 16 KiB):
-    # one CTA per SM with a 192 KiB ring (bf16 128 KiB rows, f32 512 KiB rows), two
-    # CTAs per SM with 96 KiB rings (bf16 78 and 59 KiB rows, f32 78 KiB rows) and
-    # four CTAs per SM with 48 KiB rings (bf16 39 and 23 KiB rows)
+    # one CTA per SM with a 192 KiB ring (bf16 128 KiB rows, f32 196 KiB rows), the
+    # pinned shape for rows above 400 KiB (f32 512 KiB rows), two CTAs per SM with
+    # 96 KiB rings (bf16 78 and 59 KiB rows, f32 78 KiB rows) and four CTAs per SM
+    # with 48 KiB rings (bf16 39 and 23 KiB rows)
     (500, 65536, "bf16", 0.0, 2, True),
+    (300, 50257, "f32", 0.1, True, True),
     (400, 131072, "f32", 0.1, True, False),
     (700, 40000, "bf16", 0.1, True, True),
     (400, 30000, "bf16", 0.1, True, False),
