@@ -26,7 +26,10 @@
  * Common conventions
  *   - Every pointer argument is a DEVICE pointer unless said otherwise; the
  *     caller owns every buffer and the stream.  The library never allocates,
- *     frees or synchronises, so every call can be captured in a CUDA graph.
+ *     frees or synchronises, so calls can be captured in a CUDA graph once
+ *     each entry point has run eagerly on the device: the first call of a
+ *     kernel on a device may set that kernel's shared-memory limit, which is
+ *     not a stream operation.
  *   - ``stream`` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *   - The math: for a row n with logits z[n, 0..V) and target y_n,
  *         lse_n  = log sum_v exp(z[n, v])
@@ -200,7 +203,9 @@ vce_status ce_forward_backward(const void* logits, int dtype, int64_t n_rows, in
  * VCE_NOALLOC_MAX_ROWS returns VCE_ERR_WORKSPACE before any launch.  The call
  * allocates and frees nothing.  The first call on each device looks up the
  * array's device address (with that device current); make that first call
- * before any stream capture.  All calls share the array: each call writes
+ * before any stream capture.  The address is cached with the id of its
+ * context, so the first call after cudaDeviceReset looks it up again (make
+ * that one before any capture too).  All calls share the array: each call writes
  * every slot it reads, so nothing needs clearing, but calls that overlap on
  * the GPU (different streams or host threads) race on it.
  */
@@ -313,6 +318,35 @@ vce_status shift_targets(const int64_t* target, int64_t n, int64_t seq_len, int6
  */
 vce_status vce_selftest_wait_timeout(uint64_t timeout_ns, int* dev_status,
                                      unsigned long long* waited_ns, void* stream);
+
+/*
+ * Failure-detection self-tests of the timeout exits of the two pipelined
+ * kernels.  The pages have no counterpart of these calls.  Each runs the real
+ * kernel with every wait limited to ``timeout_ns`` (1 us .. 2 s) and its work
+ * held back, so that each role's first wait runs out while no copy or MMA is
+ * in flight; the kernel then takes its timeout exit (abort flag shared by the
+ * roles, drain of anything issued, tensor memory released) and ORs
+ * VCE_DEVSTATUS_TIMEOUT into *dev_status.  The kernels return normally and
+ * the context stays usable; the numeric outputs of these calls are undefined.
+ *
+ * vce_selftest_lce_forward_timeout: lce_forward's tensor-core GEMM, whose
+ *   work-unit scheduler publishes no unit.  Arguments as lce_forward with
+ *   label_smoothing 0, VCE_REDUCE_NONE, ignore_idx -100, no entropy or n_valid;
+ *   ws of lce_workspace_size(n, h, v, VCE_REDUCE_NONE, 0) bytes.
+ * vce_selftest_ce_fused_timeout: ce_forward_backward's ring kernel, whose copy
+ *   producer issues no copy.  Arguments as ce_forward_backward with
+ *   label_smoothing 0, VCE_REDUCE_NONE (grad_output [n_rows]), ignore_idx -100,
+ *   no n_valid or workspace.  Only rows of more than 16 KiB go through the
+ *   ring; shorter rows return VCE_ERR_INVALID_ARG.
+ */
+vce_status vce_selftest_lce_forward_timeout(const void* X, const void* W, int64_t n, int64_t h,
+                                            int64_t v, const int64_t* target, uint64_t timeout_ns,
+                                            float* loss, float* lse, void* ws, size_t ws_bytes,
+                                            int* dev_status, void* stream);
+vce_status vce_selftest_ce_fused_timeout(const void* logits, int dtype, int64_t n_rows,
+                                         int64_t vocab, int64_t row_stride, const int64_t* target,
+                                         const float* grad_output, uint64_t timeout_ns, float* loss,
+                                         float* stats, void* dlogits, int* dev_status, void* stream);
 
 #ifdef __cplusplus
 }

@@ -1,12 +1,14 @@
 """CUDA-graph capture of every entry point (the API card's CUDA-graph-capturable
 mode: no host synchronisation or allocation inside a call) and the bounded-wait
-failure detection of the tensor-core pipelines, exercised without a GPU fault."""
+failure detection of the pipelined kernels, exercised without a GPU fault: the
+waits run out because work is held back, never because a copy or MMA hangs."""
 import ctypes
 
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads as wk
 import vocabulary_cross_entropy_gb300 as vce
 
@@ -40,9 +42,11 @@ def test_all_entry_points_replay_in_a_cuda_graph():
     lws = torch.empty(vce.lce_workspace_size(n, h, vl, True), dtype=torch.uint8, device=DEV)
     dx, dw = torch.empty_like(x), torch.empty_like(w)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
-    # ce_forward_backward on the short-row kernel (v = 5003) and on two ring shapes
+    # ce_forward_backward on the short-row kernel (v = 5003) and on every ring shape:
+    # four CTAs per SM (24 KiB rows), two (78 KiB), one (137 KiB) and the pinned
+    # shape (410 KiB rows)
     fused = []
-    for vf in (5003, 40000, 70001):
+    for vf in (5003, 12000, 40000, 70001, 210000):
         zf = _bf16(wk.normal_matrix(7, wk.TID_LOGITS, n, vf, 3.0, True))
         yf = torch.from_numpy(wk.uniform_targets(7, n, vf, 0.1)).to(DEV)
         fused.append((zf, yf, torch.empty(1, device=DEV), torch.empty(n, 2, device=DEV),
@@ -134,3 +138,79 @@ def test_bounded_wait_times_out_and_reports(timeout_ns):
     # the context is still usable afterwards
     a = torch.arange(10, device=DEV)
     assert int(a.sum().item()) == 45
+
+
+def _f64(t):
+    return oracle.widen(t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16), "bf16")
+
+
+def _rel(a, b):
+    return np.linalg.norm(a - b) / np.linalg.norm(b)
+
+
+def test_gemm_timeout_exit_then_normal_call():
+    # The forward GEMM with its scheduler holding back every work unit: the MMA
+    # issuer, the epilogue warps and the odd CTA's producer each give up on their
+    # first wait for a unit after 1 ms, with no copy or MMA issued; the kernel
+    # takes its timeout exit (drain, tensor memory released) and reports it.
+    n, h, v = 700, 256, 3001
+    x = wk.normal_matrix(11, wk.TID_X, n, h, 1.0, True)
+    w = wk.normal_matrix(11, wk.TID_W, v, h, h ** -0.5, True)
+    y = wk.uniform_targets(11, n, v, 0.05)
+    xt, wt, yt = _bf16(x), _bf16(w), torch.from_numpy(y).to(DEV)
+    for _ in range(2):
+        status = vce.selftest_lce_forward_timeout(xt, wt, yt, 1_000_000)
+        torch.cuda.synchronize()
+        assert int(status.item()) == vce.DEVSTATUS_TIMEOUT
+    # the context and every SM's tensor memory are usable again: a normal
+    # forward + backward on the same device matches the oracle
+    f = vce.lce_forward(xt, wt, yt, 0.1, True)
+    b = vce.lce_backward(xt, wt, yt, f.lse, f.n_valid, torch.ones(1, device=DEV), 0.1, True)
+    torch.cuda.synchronize()
+    assert int(f.dev_status.item()) == 0 and int(b.dev_status.item()) == 0
+    ref = oracle.lce_forward(x, w, y, 0.1, True)
+    dx, dw, _ = oracle.lce_backward(x, w, y, ref["lse"], ref["n_valid"], [1.0], 0.1, True, z=ref["z"])
+    assert abs(f.loss.item() - ref["loss"]) <= 2e-3
+    assert np.max(np.abs(f.lse.double().cpu().numpy() - ref["lse"])) <= 2e-3
+    assert _rel(_f64(b.dX), dx) <= 1e-2 and _rel(_f64(b.dW), dw) <= 1e-2
+
+
+# every ring shape: four CTAs per SM (BF16 24 KiB rows, FP32 23 KiB rows), two
+# (78 KiB), one with a 192 KiB ring (137 KiB) and the pinned shape (410 KiB)
+@pytest.mark.parametrize("dtype,vocab", [("bf16", 12000), ("f32", 6000), ("bf16", 40000), ("bf16", 70001),
+                                         ("bf16", 210000)])
+def test_ring_timeout_exit_then_normal_call(dtype, vocab):
+    # The fused ring kernel with its producer issuing no copy: the compute warps'
+    # first wait for a chunk (or for the pinned area) runs out after 1 ms with
+    # nothing in flight, the CTA's roles stop and the timeout is reported.
+    n = 400
+    z = wk.normal_matrix(13, wk.TID_LOGITS, n, vocab, 3.0, dtype == "bf16")
+    y = wk.uniform_targets(13, n, vocab, 0.1)
+    g = wk.grad_rows(13, n)
+    zt = _bf16(z) if dtype == "bf16" else torch.from_numpy(z).to(DEV)
+    yt, gt = torch.from_numpy(y).to(DEV), torch.from_numpy(g).to(DEV)
+    status = vce.selftest_ce_fused_timeout(zt, yt, gt, 1_000_000)
+    torch.cuda.synchronize()
+    assert int(status.item()) == vce.DEVSTATUS_TIMEOUT
+    # then the normal fused call on the same context matches the oracle
+    r = vce.ce_forward_backward(zt, yt, gt, 0.1, False)
+    torch.cuda.synchronize()
+    assert int(r.dev_status.item()) == 0
+    ref = oracle.ce_forward(z, y, 0.1, False, dtype=dtype)
+    ref_dz = oracle.ce_backward(z, y, ref["lse"], ref["n_valid"], g, 0.1, False, dtype=dtype)
+    rel, ab = (1e-5, 0.0) if dtype == "f32" else (0.0, 2e-3)
+    loss = r.loss.double().cpu().numpy()
+    assert np.all(np.abs(loss - ref["loss_rows"]) <= ab + rel * np.maximum(np.abs(ref["loss_rows"]), 1.0))
+    got = (oracle.widen(r.dlogits.view(torch.int16).cpu().numpy().view(np.uint16), "bf16") if dtype == "bf16"
+           else r.dlogits.double().cpu().numpy())
+    lim = 1e-5 if dtype == "f32" else 1e-2
+    assert np.linalg.norm(got - ref_dz) <= lim * np.linalg.norm(ref_dz)
+
+
+def test_timeout_selftests_reject_bad_arguments():
+    x = torch.zeros(4, 16, dtype=torch.bfloat16, device=DEV)
+    y = torch.zeros(4, dtype=torch.int64, device=DEV)
+    with pytest.raises(vce.VceError):  # below the 1 us floor
+        vce.selftest_lce_forward_timeout(x, x, y, 10)
+    with pytest.raises(vce.VceError):  # 16-element rows never reach the ring kernel
+        vce.selftest_ce_fused_timeout(x, y, torch.ones(4, device=DEV), 1_000_000)

@@ -31,5 +31,7 @@ from ._binding import (  # noqa: F401
     lce_workspace_size,
     lce_forward,
     lce_backward,
+    selftest_lce_forward_timeout,
+    selftest_ce_fused_timeout,
 )
 from .autograd import parallel_cross_entropy, linear_cross_entropy  # noqa: F401,E402

@@ -11,14 +11,19 @@
 // The array below lives in global memory on every GPU that loads the library
 // and is held until the process exits (4 MiB per GPU).  Host code only knows
 // the array's name as a host-side stand-in, so the device address is fetched
-// with cudaGetSymbolAddress, once per device with that device current, on the
-// first call made on that device; make that first call before any stream
-// capture.  Every call uses the same array: each call writes every row slot it
-// reads, so no clearing is needed, but calls that overlap on the GPU (two
-// streams, or two host threads) race on it.
+// with cudaGetSymbolAddress, with the device current, on the first call made on
+// that device; make that first call before any stream capture.  The address
+// is cached per device together with the id of the context it belongs to; a
+// call that finds another context current (after cudaDeviceReset, which
+// destroys the context and unloads the array with it) looks the address up
+// again, so that call, too, should come before any capture.  Every call uses
+// the same array: each call writes every row slot it reads, so no clearing is
+// needed, but calls that overlap on the GPU (two streams, or two host threads)
+// race on it.
 
 #include "vce_internal.cuh"
 
+#include <cudaTypedefs.h>
 #include <mutex>
 
 namespace {
@@ -27,20 +32,50 @@ constexpr int64_t kNoAllocMaxRows = VCE_NOALLOC_MAX_ROWS;  // 1,048,576 rows = 4
 
 static __device__ __align__(256) float g_row_loss_scratch[kNoAllocMaxRows];
 
-std::mutex g_scratch_mu;
-void* g_scratch_addr[64] = {};
+struct ScratchEntry {
+    void* addr = nullptr;
+    unsigned long long ctx_id = 0;  // context the address belongs to (0: unknown)
+};
 
-// Device address of g_row_loss_scratch on the current device (cached per ordinal).
+std::mutex g_scratch_mu;
+ScratchEntry g_scratch[64];
+
+// Id of the calling thread's current context, or 0 when there is none or the
+// driver cannot say (the address is then looked up on every call).
+unsigned long long current_context_id() {
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+    return get_id(ctx, &id) == CUDA_SUCCESS ? id : 0;
+}
+
+// Device address of g_row_loss_scratch on the current device, cached per
+// device ordinal and context.
 vce_status scratch_address(int ordinal, void** out) {
     if (ordinal < 0 || ordinal >= 64) return VCE_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[ordinal]) {
+    ScratchEntry& e = g_scratch[ordinal];
+    const unsigned long long ctx = current_context_id();
+    if (!e.addr || ctx == 0 || ctx != e.ctx_id) {
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_row_loss_scratch) != cudaSuccess || p == nullptr)
-            return VCE_ERR_CUDA;
-        g_scratch_addr[ordinal] = p;
+        if (cudaGetSymbolAddress(&p, g_row_loss_scratch) != cudaSuccess || p == nullptr) return VCE_ERR_CUDA;
+        e.addr = p;
+        e.ctx_id = current_context_id();  // the lookup makes the device's context current if it was not
     }
-    *out = g_scratch_addr[ordinal];
+    *out = e.addr;
     return VCE_OK;
 }
 

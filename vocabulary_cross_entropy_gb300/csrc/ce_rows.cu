@@ -691,8 +691,6 @@ __device__ __forceinline__ void compute_merge(OnlineLse& a, float* sm_m, float* 
     }
 }
 
-constexpr uint64_t kRingTimeoutNs = 2000000000ull;  // 2 s per wait
-
 // NW compute warps, each thread taking PER 16-byte vectors of every full
 // chunk; RING_KB KiB of shared memory in equal chunks, and PIN_KB KiB more that
 // keep the first chunks of the current row for its second pass.
@@ -709,11 +707,13 @@ struct RingCfg {
 
 __device__ __forceinline__ uint64_t min_u64(uint64_t a, uint64_t b) { return a < b ? a : b; }
 
-// Bounded wait that ignores the abort flag (draining copies still in flight).
+// Bounded wait that ignores the abort flag (draining copies still in flight:
+// they complete on their own, so the long drain limit is never reached in
+// practice and the CTA does not exit while a copy into its shared memory runs).
 __device__ __forceinline__ bool ring_drain_wait(uint64_t* bar, uint32_t parity) {
     const uint64_t t0 = sm100::globaltimer();
     while (!sm100::mbar_try_wait(bar, parity))
-        if (sm100::globaltimer() - t0 > kRingTimeoutNs) return false;
+        if (sm100::globaltimer() - t0 > kDrainTimeoutNs) return false;
     return true;
 }
 
@@ -739,15 +739,17 @@ __device__ __forceinline__ bool ring_drain_wait(uint64_t* bar, uint32_t parity) 
 // leave L2 before their second read); the pinned area is released as soon as
 // the second pass has used it, and the next row's first chunks are copied in
 // while the rest of the row goes through the ring.
-// Every wait is bounded: on timeout the CTA sets its abort flag, every role
-// stops waiting, the producer waits for the copies it issued, and
-// VCE_DEVSTATUS_TIMEOUT is reported (the outputs are then undefined).
+// Every wait is bounded (``timeout_ns``): on timeout the CTA sets its abort
+// flag, every role stops waiting, the producer waits for the copies it issued,
+// and VCE_DEVSTATUS_TIMEOUT is reported (the outputs are then undefined).
+// ``hold`` (failure-detection self-test only) makes the producer issue no copy,
+// so the compute warps' first wait runs out with nothing in flight.
 template <int NW, int PER, int RING_KB, int MINB, bool kHint, typename T, bool kSmooth, int PIN_KB = 0>
 __global__ void __launch_bounds__(NW * 32 + 32, MINB)
 ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, const int64_t* __restrict__ target,
               float eps, int64_t ignore_idx, const int64_t* __restrict__ n_valid,
               const float* __restrict__ grad_output, int reduce_loss, float* __restrict__ loss_rows,
-              float2* __restrict__ stats, T* dlogits, int* dev_status) {
+              float2* __restrict__ stats, T* dlogits, int* dev_status, uint64_t timeout_ns, int hold) {
     using E = Elem<T>;
     using C = RingCfg<NW, PER, RING_KB, PIN_KB>;
     using namespace sm100;
@@ -788,7 +790,7 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
         uint32_t slot = 0, ph = 0, issued = 0, pin_ph = 0, pin_issued = 0;
         bool ok = true;
         const uint64_t keep = kHint ? l2_policy_evict_last() : 0, drop = kHint ? l2_policy_evict_first() : 0;
-        for (int64_t row = blockIdx.x; row < n_rows && ok; row += gridDim.x) {
+        for (int64_t row = blockIdx.x; row < n_rows && ok && !hold; row += gridDim.x) {
             const int64_t y = target[row];
             if (y == ignore_idx) continue;
             const bool bad = y < 0 || y >= vocab;
@@ -800,7 +802,7 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
             const uint64_t np = min_u64(nch, uint64_t(P));
             if (np > 0) {
                 // the row's first np chunks go to the pinned area, kept for the second pass
-                if (!mbar_wait(pin_empty, pin_ph ^ 1, abort_flag, kRingTimeoutNs)) {
+                if (!mbar_wait(pin_empty, pin_ph ^ 1, abort_flag, timeout_ns)) {
                     ok = false;
                     break;
                 }
@@ -818,7 +820,7 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
             }
             for (int pass = 0; pass < (bad ? 1 : 2) && ok; ++pass) {
                 for (uint64_t off = np * CH; off < total; off += CH) {
-                    if (!mbar_wait(&empty[slot], ph ^ 1, abort_flag, kRingTimeoutNs)) {
+                    if (!mbar_wait(&empty[slot], ph ^ 1, abort_flag, timeout_ns)) {
                         ok = false;
                         break;
                     }
@@ -855,7 +857,7 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
     bool ok = true;
     // wait for the next chunk; false once this CTA has given up
     auto take = [&]() -> bool {
-        if (ok && !mbar_wait(&full[slot], ph, abort_flag, kRingTimeoutNs)) ok = false;
+        if (ok && !mbar_wait(&full[slot], ph, abort_flag, timeout_ns)) ok = false;
         return ok;
     };
     auto release = [&]() {
@@ -891,7 +893,7 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
             acc.push<1, kSmooth>(v);
         }
         if (np > 0) {
-            if (ok && !mbar_wait(pin_full, pin_ph, abort_flag, kRingTimeoutNs)) ok = false;
+            if (ok && !mbar_wait(pin_full, pin_ph, abort_flag, timeout_ns)) ok = false;
             if (ok) {
                 for (uint64_t k = 0; k < np; ++k) {
                     const uint4* src = reinterpret_cast<const uint4*>(pin + k * CH);
@@ -1025,7 +1027,7 @@ template <typename T, int NW, int PER, int RING_KB, int MINB, bool kHint, int PI
 void ring_launch(const void* logits, int64_t n_rows, int64_t vocab, int64_t stride, const int64_t* target,
                  float eps, int64_t ignore_idx, const int64_t* n_valid, const float* grad_output, int reduce_loss,
                  float* loss_rows, float* stats, void* dlogits, int* dev_status, cudaStream_t s,
-                 const DeviceInfo& dev) {
+                 const DeviceInfo& dev, const PipeDiag& diag) {
     using C = RingCfg<NW, PER, RING_KB, PIN_KB>;
     auto kern = eps != 0.f ? ce_fused_ring<NW, PER, RING_KB, MINB, kHint, T, true, PIN_KB>
                            : ce_fused_ring<NW, PER, RING_KB, MINB, kHint, T, false, PIN_KB>;
@@ -1047,7 +1049,8 @@ void ring_launch(const void* logits, int64_t n_rows, int64_t vocab, int64_t stri
     count_launch();
     kern<<<grid, C::kThreads + 32, C::kSmemBytes, s>>>(
         static_cast<const T*>(logits), n_rows, vocab, stride, target, eps, ignore_idx, n_valid, grad_output,
-        reduce_loss, loss_rows, reinterpret_cast<float2*>(stats), static_cast<T*>(dlogits), dev_status);
+        reduce_loss, loss_rows, reinterpret_cast<float2*>(stats), static_cast<T*>(dlogits), dev_status,
+        diag.timeout_ns, diag.hold);
 }
 
 template <typename T, int THREADS, int MINB, int U1, int U2, bool kPrefetch>
@@ -1079,7 +1082,7 @@ template <typename T>
 void fused_dispatch(const void* logits, int64_t n_rows, int64_t vocab, int64_t stride, const int64_t* target,
                     float eps, int64_t ignore_idx, const int64_t* n_valid, const float* grad_output,
                     int reduce_loss, float* loss_rows, float* stats, void* dlogits, int* dev_status,
-                    cudaStream_t s, const DeviceInfo& dev) {
+                    cudaStream_t s, const DeviceInfo& dev, const PipeDiag& diag) {
     // Rows up to 1024 vectors (16 KiB): 128 threads per row, 8 CTAs per SM, and
     // the next-row L2 prefetch while two rows per CTA take at most two thirds of
     // L2.  Longer rows: the TMA-fed ring kernel, shaped by row length.  Measured
@@ -1110,16 +1113,26 @@ void fused_dispatch(const void* logits, int64_t n_rows, int64_t vocab, int64_t s
         if (double(grid) * 2 * row <= l2 * 2.0 / 3.0) fused_launch<T, 128, 8, 4, 2, true>(VCE_FUSED_ARGS, grid);
         else fused_launch<T, 128, 8, 4, 2, false>(VCE_FUSED_ARGS, grid);
     } else if (nvec * 16 <= 48 * 1024) {
-        ring_launch<T, 4, 4, 48, 4, false>(VCE_FUSED_ARGS, dev);
+        ring_launch<T, 4, 4, 48, 4, false>(VCE_FUSED_ARGS, dev, diag);
     } else if (nvec * 16 <= 112 * 1024) {
-        ring_launch<T, 8, 4, 96, 2, false>(VCE_FUSED_ARGS, dev);
+        ring_launch<T, 8, 4, 96, 2, false>(VCE_FUSED_ARGS, dev, diag);
     } else if (nvec * 16 <= 400 * 1024) {
-        ring_launch<T, 16, 4, 192, 1, true>(VCE_FUSED_ARGS, dev);
+        ring_launch<T, 16, 4, 192, 1, true>(VCE_FUSED_ARGS, dev, diag);
     } else {
-        ring_launch<T, 16, 4, 128, 1, true, 64>(VCE_FUSED_ARGS, dev);
+        ring_launch<T, 16, 4, 128, 1, true, 64>(VCE_FUSED_ARGS, dev, diag);
     }
 #undef VCE_FUSED_ARGS
 }
+
+}  // namespace
+
+bool ce_fused_uses_ring(int dtype, int64_t vocab) {
+    // fused_dispatch: rows of more than 1024 16-byte vectors go to the ring kernel
+    const int64_t nvec = dtype == VCE_BF16 ? vocab / Elem<__nv_bfloat16>::kVec : vocab / Elem<float>::kVec;
+    return nvec > 1024;
+}
+
+namespace {
 
 int row_grid(int64_t n_rows) {
     const int64_t cap = int64_t(1) << 30;
@@ -1186,7 +1199,7 @@ vce_status launch_ce_forward_backward(const void* logits, int dtype, int64_t n_r
                                       int64_t row_stride, const int64_t* target, float eps, int reduce_loss,
                                       int64_t ignore_idx, const float* grad_output, float* loss, float* stats,
                                       int64_t* n_valid, void* dlogits, void* ws, int* dev_status,
-                                      cudaStream_t s, const DeviceInfo& dev) {
+                                      cudaStream_t s, const DeviceInfo& dev, const PipeDiag& diag) {
     float* loss_rows = reduce_loss ? static_cast<float*>(ws) : loss;
     if (n_rows > 0) {
         // N_v first: the mean's upstream gradient g / N_v is needed inside the row pass
@@ -1195,10 +1208,11 @@ vce_status launch_ce_forward_backward(const void* logits, int dtype, int64_t n_r
                 return st;
         if (dtype == VCE_BF16)
             fused_dispatch<__nv_bfloat16>(logits, n_rows, vocab, row_stride, target, eps, ignore_idx, n_valid,
-                                          grad_output, reduce_loss, loss_rows, stats, dlogits, dev_status, s, dev);
+                                          grad_output, reduce_loss, loss_rows, stats, dlogits, dev_status, s, dev,
+                                          diag);
         else
             fused_dispatch<float>(logits, n_rows, vocab, row_stride, target, eps, ignore_idx, n_valid,
-                                  grad_output, reduce_loss, loss_rows, stats, dlogits, dev_status, s, dev);
+                                  grad_output, reduce_loss, loss_rows, stats, dlogits, dev_status, s, dev, diag);
         if (cudaGetLastError() != cudaSuccess) return VCE_ERR_CUDA;
     }
     if (reduce_loss || n_valid)

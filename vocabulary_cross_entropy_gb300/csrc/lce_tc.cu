@@ -32,9 +32,9 @@
 // Warp 0: TMA producer (both CTAs).  Warp 1: tensor-memory allocation (both
 // CTAs) and the MMA issuer (even CTA).  Warps 2-5: epilogue, one output row
 // per thread (tensor-memory lane).
-// Every mbarrier wait is bounded: past kTimeoutNs the CTA sets an abort flag,
-// the other roles stop, in-flight copies and MMAs are drained, tensor memory
-// is released and VCE_DEVSTATUS_TIMEOUT is reported.
+// Every mbarrier wait is bounded: past its limit (2 s) the CTA sets an abort
+// flag, the other roles stop, in-flight copies and MMAs are drained, tensor
+// memory is released and VCE_DEVSTATUS_TIMEOUT is reported.
 
 #include "vce_internal.cuh"
 #include "sm100_ptx.cuh"
@@ -55,7 +55,6 @@ constexpr int kVocabTile = 256;  // forward/dZ vocabulary tile width
 constexpr uint32_t kABytes = BM_CTA * BK * 2;
 constexpr int kThreads = 192;
 constexpr uint32_t kRingBytes = 196608;
-constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
 constexpr int kUnitRing = 8;                     // work units published ahead of the slowest reader
 constexpr uint32_t kUnitReaders = 10;            // odd CTA's producer, MMA issuer, 8 epilogue warps
 
@@ -77,6 +76,8 @@ struct GemmArgs {
     int group;         // tiles of the fast index per group of the unit order (see unit_coords)
     int* counter;      // work-unit tickets, zero at launch
     int* dev_status;
+    uint64_t timeout_ns;  // limit of every wait for work or data
+    int hold;             // self-test only: the scheduler publishes no unit
 };
 
 // Work unit u -> output tile (tm, tn), K chunk ks and its K-block range [kb0, kb1).
@@ -395,11 +396,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             uint32_t stage = 0, phase = 0, issued = 0, issued_phase = 0;
             bool ok = true;
             int next = leader ? atomicAdd(args.counter, 1) : 0;
+            // self-test of the timeout exits: no unit is published, so every
+            // other role's first wait for one runs out, with nothing in flight
+            if (leader && args.hold) ok = false;
             for (uint32_t seq = 0; ok; ++seq) {
                 const uint32_t slot = seq % kUnitRing, upar = (seq / kUnitRing) & 1u;
                 int t;
                 if (leader) {
-                    if (!mbar_wait<true>(&uempty[slot], upar ^ 1u, abort_flag, kTimeoutNs)) {
+                    if (!mbar_wait<true>(&uempty[slot], upar ^ 1u, abort_flag, args.timeout_ns)) {
                         ok = false;
                         break;
                     }
@@ -410,7 +414,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     mbar_arrive_cluster(mapa_shared(smem_u32(&ufull[slot]), 1));
                     if (t < T) next = atomicAdd(args.counter, 1);
                 } else {
-                    if (!mbar_wait<true>(&ufull[slot], upar, abort_flag, kTimeoutNs)) {
+                    if (!mbar_wait<true>(&ufull[slot], upar, abort_flag, args.timeout_ns)) {
                         ok = false;
                         break;
                     }
@@ -423,7 +427,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 const int a_row = tm * BM + int(rank) * BM_CTA;
                 const int b_row = tn * BN + int(rank) * (BN / 2);
                 for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, kTimeoutNs)) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, args.timeout_ns)) {
                         ok = false;
                         break;
                     }
@@ -458,7 +462,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 // let copies already in flight land before shared memory is released
                 volatile int no_abort = 0;
                 for (int s = 0; s < S; ++s)
-                    if ((issued >> s) & 1u) mbar_wait(&full[s], (issued_phase >> s) & 1u, &no_abort, kTimeoutNs);
+                    if ((issued >> s) & 1u)
+                        mbar_wait(&full[s], (issued_phase >> s) & 1u, &no_abort, kDrainTimeoutNs);
             }
         }
     } else if (warp == 1) {
@@ -469,17 +474,17 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             bool ok = true;
             for (uint32_t seq = 0; ok; ++seq) {
                 const uint32_t slot = seq % kUnitRing, upar = (seq / kUnitRing) & 1u;
-                if (!mbar_wait<true>(&ufull[slot], upar, abort_flag, kTimeoutNs)) break;
+                if (!mbar_wait<true>(&ufull[slot], upar, abort_flag, args.timeout_ns)) break;
                 const int t = sched[slot];
                 mbar_arrive_cluster(mapa_shared(smem_u32(&uempty[slot]), 0));
                 if (t >= T) break;
                 int tm, tn, ks, kb0, kb1;
                 unit_coords(args, t, tm, tn, ks, kb0, kb1);
-                if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, kTimeoutNs)) break;
+                if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, args.timeout_ns)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, abort_flag, kTimeoutNs)) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag, args.timeout_ns)) {
                         ok = false;
                         break;
                     }
@@ -508,7 +513,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             // every MMA issued so far completes before tensor memory is released
             umma_commit_pair(drain, 0x1);
             volatile int no_abort = 0;
-            mbar_wait(drain, 0, &no_abort, kTimeoutNs);
+            mbar_wait(drain, 0, &no_abort, kDrainTimeoutNs);
         }
     } else {
         // ---------------- epilogue (warps 2..5 of both CTAs) ----------------
@@ -517,13 +522,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         uint32_t acc = 0, acc_phase = 0;
         for (uint32_t seq = 0;; ++seq) {
             const uint32_t slot = seq % kUnitRing, upar = (seq / kUnitRing) & 1u;
-            bool ok = mbar_wait<true>(&ufull[slot], upar, abort_flag, kTimeoutNs);
+            bool ok = mbar_wait<true>(&ufull[slot], upar, abort_flag, args.timeout_ns);
             if (!__all_sync(0xffffffffu, ok)) break;
             const int t = sched[slot];
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&uempty[slot]), 0));
             if (t >= T) break;
-            ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, kTimeoutNs);
+            ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, args.timeout_ns);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
             int tm, tn, ks, kb0, kb1;
@@ -705,7 +710,7 @@ int raster_group(int tiles_fast, int64_t strip_bytes, const DeviceInfo& dev) {
 template <class Epi, bool kAMn, bool kBMn, int BN>
 vce_status launch_gemm(const CUtensorMap& a, const CUtensorMap& b, int64_t M, int64_t N, int64_t K, int m_fastest,
                        int k_splits, const Epi& epi, int* counter, int* dev_status, cudaStream_t s,
-                       const DeviceInfo& dev) {
+                       const DeviceInfo& dev, const PipeDiag& diag = PipeDiag()) {
     using C = PairCfg<BN>;
     auto kern = tc_gemm_kernel<Epi, kAMn, kBMn, BN>;
     // the shared-memory limit is a per-device attribute of the kernel: raise it
@@ -737,6 +742,8 @@ vce_status launch_gemm(const CUtensorMap& a, const CUtensorMap& b, int64_t M, in
     }
     args.counter = counter;
     args.dev_status = dev_status;
+    args.timeout_ns = diag.timeout_ns;
+    args.hold = diag.hold;
     const int64_t units = int64_t(args.tiles_m) * args.tiles_n * args.k_splits;
     if (units <= 0 || args.k_blocks <= 0) return VCE_OK;
     const int64_t pairs = dev.num_sms / 2;
@@ -870,7 +877,7 @@ int64_t lce_slab_for_ws(int64_t n, int64_t h, int64_t v, size_t ws_bytes) {
 vce_status launch_lce_forward(const void* X, const void* W, int64_t n, int64_t h, int64_t v,
                               const int64_t* target, float eps, int reduce_loss, int64_t ignore_idx,
                               float* loss, float* lse, float* entropy, int64_t* n_valid, void* ws,
-                              int* dev_status, cudaStream_t s, const DeviceInfo& dev) {
+                              int* dev_status, cudaStream_t s, const DeviceInfo& dev, const PipeDiag& diag) {
     if (n == 0) {
         if (reduce_loss || n_valid)
             return launch_mean_loss(nullptr, target, 0, ignore_idx, reduce_loss, reduce_loss ? loss : nullptr,
@@ -882,7 +889,8 @@ vce_status launch_lce_forward(const void* X, const void* W, int64_t n, int64_t h
     if (!map_kmajor(&tx, X, h, n, h, BM_CTA) || !map_kmajor(&tw, W, h, v, h, kVocabTile / 2)) return VCE_ERR_CUDA;
     FwdEpi epi{target, n, v, w.part_ms, w.part_sum, entropy ? w.part_t : nullptr, w.zy, eps != 0.f ? 1 : 0};
     if (vce_status st =
-            launch_gemm<FwdEpi, false, false, kVocabTile>(tx, tw, n, v, h, 1, 1, epi, w.counter, dev_status, s, dev))
+            launch_gemm<FwdEpi, false, false, kVocabTile>(tx, tw, n, v, h, 1, 1, epi, w.counter, dev_status, s, dev,
+                                                          diag))
         return st;
     const int nb = int((v + kVocabTile - 1) / kVocabTile);
     float* loss_rows = reduce_loss ? w.loss_rows : loss;

@@ -52,6 +52,26 @@ __device__ __forceinline__ void report(int* dev_status, int bits) {
 // Host-side count of the kernels this library has launched (diagnostics).
 void count_launch();
 
+// Limits of the bounded mbarrier waits in the pipelined kernels (the GEMM and
+// the fused ring kernel).  A wait for work or data gives up after
+// kPipeTimeoutNs, sets the CTA's abort flag and the kernel reports
+// VCE_DEVSTATUS_TIMEOUT.  A drain wait (for copies or MMAs that were already
+// issued, which complete on their own) ignores the abort flag and has a much
+// longer limit, so that a CTA gives up its shared and tensor memory only once
+// nothing issued into them is still running.
+constexpr uint64_t kPipeTimeoutNs = 2000000000ull;    // 2 s
+constexpr uint64_t kDrainTimeoutNs = 10000000000ull;  // 10 s
+
+// Settings of one pipelined launch.  The library's own calls use the defaults;
+// the failure-detection self-tests shorten the wait limit and set ``hold``: the
+// GEMM's scheduler then publishes no work unit and the ring kernel's producer
+// issues no copy, so every role's first wait runs out with no copy or MMA in
+// flight.
+struct PipeDiag {
+    uint64_t timeout_ns = kPipeTimeoutNs;
+    int hold = 0;
+};
+
 // Round up to a multiple of 256 bytes (workspace carving).
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -83,7 +103,9 @@ vce_status launch_ce_forward_backward(const void* logits, int dtype, int64_t n_r
                                       int64_t row_stride, const int64_t* target, float eps, int reduce_loss,
                                       int64_t ignore_idx, const float* grad_output, float* loss, float* stats,
                                       int64_t* n_valid, void* dlogits, void* ws, int* dev_status,
-                                      cudaStream_t s, const DeviceInfo& dev);
+                                      cudaStream_t s, const DeviceInfo& dev, const PipeDiag& diag = PipeDiag());
+// whether ce_forward_backward runs rows of this length through the ring kernel
+bool ce_fused_uses_ring(int dtype, int64_t vocab);
 vce_status launch_shift_targets(const int64_t* target, int64_t n, int64_t seq_len, int64_t ignore_idx,
                                 int64_t* shifted, cudaStream_t s);
 // mean of per-row losses over rows whose target is not ignore_idx, and the count
@@ -98,7 +120,8 @@ size_t lce_backward_ws_bytes(int64_t n, int64_t h, int64_t v, int64_t slab);
 vce_status launch_lce_forward(const void* X, const void* W, int64_t n, int64_t h, int64_t v,
                               const int64_t* target, float eps, int reduce_loss,
                               int64_t ignore_idx, float* loss, float* lse, float* entropy, int64_t* n_valid,
-                              void* ws, int* dev_status, cudaStream_t s, const DeviceInfo& dev);
+                              void* ws, int* dev_status, cudaStream_t s, const DeviceInfo& dev,
+                              const PipeDiag& diag = PipeDiag());
 vce_status launch_lce_backward(const void* X, const void* W, int64_t n, int64_t h, int64_t v,
                                const int64_t* target, const float* lse, const int64_t* n_valid,
                                const float* grad_output, float eps, int reduce_loss,
