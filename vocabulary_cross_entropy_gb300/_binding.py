@@ -70,6 +70,14 @@ def library() -> ctypes.CDLL:
     lib.lce_backward.argtypes = [_c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_p, _c_p, _c_p, _c_f32,
                                  _c_int, _c_i64, _c_p, _c_p, _c_p, _c_size, _c_p, _c_p]
     lib.lce_backward.restype = _c_int
+    lib.vce_selftest_wait_timeout.argtypes = [ctypes.c_uint64, _c_p, _c_p, _c_p]
+    lib.vce_selftest_wait_timeout.restype = _c_int
+    lib.vce_selftest_lce_forward_timeout.argtypes = [_c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_p, ctypes.c_uint64,
+                                                     _c_p, _c_p, _c_p, _c_size, _c_p, _c_p]
+    lib.vce_selftest_lce_forward_timeout.restype = _c_int
+    lib.vce_selftest_ce_fused_timeout.argtypes = [_c_p, _c_int, _c_i64, _c_i64, _c_i64, _c_p, _c_p,
+                                                  ctypes.c_uint64, _c_p, _c_p, _c_p, _c_p, _c_p]
+    lib.vce_selftest_ce_fused_timeout.restype = _c_int
     _lib = lib
     return lib
 
@@ -93,13 +101,39 @@ def _check(func: str, status: int):
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # a plain int: the argtypes bound in library() convert it to a pointer
+    return None if t is None else t.data_ptr()
+
+
+# torch's raw current-stream and current-device queries: the public
+# torch.cuda.current_stream() builds a Stream object on every call, which was
+# most of the host time of a small call; the public forms are the fallback
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+_raw_device = getattr(torch._C, "_cuda_getDevice", None)
 
 
 def _stream(device, stream):
-    if stream is None:
-        stream = torch.cuda.current_stream(device)
-    return ctypes.c_void_p(stream.cuda_stream)
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None and device.index is not None:
+        return _raw_stream(device.index)
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _on(device, fn, *args):
+    """fn(*args) with ``device`` current (switching only when another device is)."""
+    cur = _raw_device() if _raw_device is not None else torch.cuda.current_device()
+    if device.index is None or device.index == cur:
+        return fn(*args)
+    with torch.cuda.device(device):
+        return fn(*args)
+
+
+def _f32_on(t, device):
+    """``t`` as a contiguous FP32 tensor on ``device`` (no copy when it already is)."""
+    if t.dtype is torch.float32 and t.device == device and t.is_contiguous():
+        return t
+    return t.to(device=device, dtype=torch.float32).contiguous()
 
 
 def _dtype_code(t: torch.Tensor) -> int:
@@ -158,25 +192,25 @@ def ce_forward(logits, target, label_smoothing=0.0, reduce_loss=False, ignore_id
     dev = logits.device
     n, vocab, stride = _rows_view(logits)
     target = _target(target, n)
+    red = _reduce(reduce_loss)
     if loss is None:
-        loss = torch.empty(1 if _reduce(reduce_loss) else n, dtype=torch.float32, device=dev)
+        loss = torch.empty(1 if red else n, dtype=torch.float32, device=dev)
     if stats is None:
         stats = torch.empty(n, 2, dtype=torch.float32, device=dev)
     if n_valid is None:
         n_valid = torch.empty(1, dtype=torch.int64, device=dev)
     if dev_status is None:
         dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
-    ws_bytes = ce_workspace_size(n, vocab, reduce_loss)
-    if workspace is None and ws_bytes:
-        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    with torch.cuda.device(dev):
-        st = lib.ce_forward(_ptr(logits), _dtype_code(logits), n, vocab, stride, _ptr(target),
-                            float(label_smoothing), _reduce(reduce_loss), int(ignore_idx),
-                            _ptr(loss), _ptr(stats), _ptr(n_valid), _ptr(workspace),
-                            0 if workspace is None else workspace.numel() * workspace.element_size(),
-                            _ptr(dev_status), _stream(dev, stream))
+    if workspace is None:
+        ws_bytes = ce_workspace_size(n, vocab, red)
+        if ws_bytes:
+            workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    st = _on(dev, lib.ce_forward, _ptr(logits), _dtype_code(logits), n, vocab, stride, _ptr(target),
+             float(label_smoothing), red, int(ignore_idx), _ptr(loss), _ptr(stats), _ptr(n_valid),
+             _ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
+             _ptr(dev_status), _stream(dev, stream))
     _check("ce_forward", st)
-    return CEForward(loss if _reduce(reduce_loss) else loss.view(logits.shape[:-1]), stats, n_valid, dev_status)
+    return CEForward(loss if red else loss.view(logits.shape[:-1]), stats, n_valid, dev_status)
 
 
 def ce_forward_noalloc(logits, target, label_smoothing=0.0, reduce_loss=False, ignore_idx=-100, *,
@@ -196,11 +230,9 @@ def ce_forward_noalloc(logits, target, label_smoothing=0.0, reduce_loss=False, i
         n_valid = torch.empty(1, dtype=torch.int64, device=dev)
     if dev_status is None:
         dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
-    with torch.cuda.device(dev):
-        st = lib.ce_forward_noalloc(_ptr(logits), _dtype_code(logits), n, vocab, stride, _ptr(target),
-                                    float(label_smoothing), _reduce(reduce_loss), int(ignore_idx),
-                                    _ptr(loss), _ptr(stats), _ptr(n_valid), _ptr(dev_status),
-                                    _stream(dev, stream))
+    st = _on(dev, lib.ce_forward_noalloc, _ptr(logits), _dtype_code(logits), n, vocab, stride, _ptr(target),
+             float(label_smoothing), _reduce(reduce_loss), int(ignore_idx), _ptr(loss), _ptr(stats),
+             _ptr(n_valid), _ptr(dev_status), _stream(dev, stream))
     _check("ce_forward_noalloc", st)
     return CEForward(loss if _reduce(reduce_loss) else loss.view(logits.shape[:-1]), stats, n_valid, dev_status)
 
@@ -218,14 +250,12 @@ def ce_backward(logits, target, stats, n_valid, grad_output, label_smoothing=0.0
         dlogits = torch.empty_like(logits)
     if dlogits.stride() != logits.stride() or dlogits.dtype != logits.dtype:
         raise ValueError("dlogits must have the dtype and strides of logits")
-    grad_output = grad_output.to(device=dev, dtype=torch.float32).contiguous()
+    grad_output = _f32_on(grad_output, dev)
     if dev_status is None:
         dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
-    with torch.cuda.device(dev):
-        st = lib.ce_backward(_ptr(logits), _dtype_code(logits), n, vocab, stride, _ptr(target),
-                             _ptr(stats), _ptr(n_valid), _ptr(grad_output), float(label_smoothing),
-                             _reduce(reduce_loss), int(ignore_idx), _ptr(dlogits),
-                             _ptr(dev_status), _stream(dev, stream))
+    st = _on(dev, lib.ce_backward, _ptr(logits), _dtype_code(logits), n, vocab, stride, _ptr(target),
+             _ptr(stats), _ptr(n_valid), _ptr(grad_output), float(label_smoothing), _reduce(reduce_loss),
+             int(ignore_idx), _ptr(dlogits), _ptr(dev_status), _stream(dev, stream))
     _check("ce_backward", st)
     return dlogits
 
@@ -248,28 +278,26 @@ def ce_forward_backward(logits, target, grad_output, label_smoothing=0.0, reduce
         dlogits = torch.empty_like(logits)
     if dlogits.stride() != logits.stride() or dlogits.dtype != logits.dtype:
         raise ValueError("dlogits must have the dtype and strides of logits")
-    grad_output = grad_output.to(device=dev, dtype=torch.float32).contiguous()
+    grad_output = _f32_on(grad_output, dev)
+    red = _reduce(reduce_loss)
     if loss is None:
-        loss = torch.empty(1 if _reduce(reduce_loss) else n, dtype=torch.float32, device=dev)
+        loss = torch.empty(1 if red else n, dtype=torch.float32, device=dev)
     if stats is None:
         stats = torch.empty(n, 2, dtype=torch.float32, device=dev)
     if n_valid is None:
         n_valid = torch.empty(1, dtype=torch.int64, device=dev)
     if dev_status is None:
         dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
-    ws_bytes = ce_workspace_size(n, vocab, reduce_loss)
-    if workspace is None and ws_bytes:
-        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    with torch.cuda.device(dev):
-        st = lib.ce_forward_backward(_ptr(logits), _dtype_code(logits), n, vocab, stride, _ptr(target),
-                                     float(label_smoothing), _reduce(reduce_loss), int(ignore_idx),
-                                     _ptr(grad_output), _ptr(loss), _ptr(stats), _ptr(n_valid),
-                                     _ptr(dlogits), _ptr(workspace),
-                                     0 if workspace is None else workspace.numel(),
-                                     _ptr(dev_status), _stream(dev, stream))
+    if workspace is None:
+        ws_bytes = ce_workspace_size(n, vocab, red)
+        if ws_bytes:
+            workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    st = _on(dev, lib.ce_forward_backward, _ptr(logits), _dtype_code(logits), n, vocab, stride, _ptr(target),
+             float(label_smoothing), red, int(ignore_idx), _ptr(grad_output), _ptr(loss), _ptr(stats),
+             _ptr(n_valid), _ptr(dlogits), _ptr(workspace), 0 if workspace is None else workspace.numel(),
+             _ptr(dev_status), _stream(dev, stream))
     _check("ce_forward_backward", st)
-    return CEForwardBackward(loss if _reduce(reduce_loss) else loss.view(logits.shape[:-1]), stats, n_valid,
-                             dlogits, dev_status)
+    return CEForwardBackward(loss if red else loss.view(logits.shape[:-1]), stats, n_valid, dlogits, dev_status)
 
 
 def shift_targets(target, seq_len, ignore_idx=-100, *, out=None, stream=None):
@@ -282,9 +310,8 @@ def shift_targets(target, seq_len, ignore_idx=-100, *, out=None, stream=None):
     if out is None:
         out = torch.empty_like(flat)
     dev = flat.device
-    with torch.cuda.device(dev):
-        st = lib.shift_targets(_ptr(flat), flat.numel(), int(seq_len), int(ignore_idx), _ptr(out),
-                               _stream(dev, stream))
+    st = _on(dev, lib.shift_targets, _ptr(flat), flat.numel(), int(seq_len), int(ignore_idx), _ptr(out),
+             _stream(dev, stream))
     _check("shift_targets", st)
     return out.view(target.shape)
 
@@ -332,11 +359,9 @@ def lce_forward(X, W, target, label_smoothing=0.0, reduce_loss=False, ignore_idx
     if workspace is None:
         workspace = torch.empty(max(1, lce_workspace_size(n, h, v, reduce_loss, max_slab_bytes)),
                                 dtype=torch.uint8, device=dev)
-    with torch.cuda.device(dev):
-        st = lib.lce_forward(_ptr(X), _ptr(W), n, h, v, _ptr(target), float(label_smoothing),
-                             _reduce(reduce_loss), int(ignore_idx), _ptr(loss), _ptr(lse), _ptr(entropy),
-                             _ptr(n_valid), _ptr(workspace), workspace.numel(), _ptr(dev_status),
-                             _stream(dev, stream))
+    st = _on(dev, lib.lce_forward, _ptr(X), _ptr(W), n, h, v, _ptr(target), float(label_smoothing),
+             _reduce(reduce_loss), int(ignore_idx), _ptr(loss), _ptr(lse), _ptr(entropy), _ptr(n_valid),
+             _ptr(workspace), workspace.numel(), _ptr(dev_status), _stream(dev, stream))
     _check("lce_forward", st)
     return LCEForward(loss, lse, n_valid, dev_status, entropy)
 
@@ -356,16 +381,59 @@ def lce_backward(X, W, target, lse, n_valid, grad_output, label_smoothing=0.0, r
         dX = torch.empty_like(X)
     if dW is None:
         dW = torch.empty_like(W)
-    grad_output = grad_output.to(device=dev, dtype=torch.float32).contiguous()
+    grad_output = _f32_on(grad_output, dev)
     if dev_status is None:
         dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
     if workspace is None:
         workspace = torch.empty(max(1, lce_workspace_size(n, h, v, reduce_loss, max_slab_bytes)),
                                 dtype=torch.uint8, device=dev)
-    with torch.cuda.device(dev):
-        st = lib.lce_backward(_ptr(X), _ptr(W), n, h, v, _ptr(target), _ptr(lse), _ptr(n_valid),
-                              _ptr(grad_output), float(label_smoothing), _reduce(reduce_loss),
-                              int(ignore_idx), _ptr(dX), _ptr(dW), _ptr(workspace), workspace.numel(),
-                              _ptr(dev_status), _stream(dev, stream))
+    st = _on(dev, lib.lce_backward, _ptr(X), _ptr(W), n, h, v, _ptr(target), _ptr(lse), _ptr(n_valid),
+             _ptr(grad_output), float(label_smoothing), _reduce(reduce_loss), int(ignore_idx), _ptr(dX),
+             _ptr(dW), _ptr(workspace), workspace.numel(), _ptr(dev_status), _stream(dev, stream))
     _check("lce_backward", st)
     return LCEBackward(dX, dW, dev_status)
+
+
+# ---------------------------------------------------------------------------
+# failure-detection self-tests (diagnostics; see include/vce.h)
+# ---------------------------------------------------------------------------
+
+def selftest_lce_forward_timeout(X, W, target, timeout_ns, *, dev_status=None, stream=None):
+    """Runs lce_forward's GEMM with its work held back so that every wait runs out after
+    ``timeout_ns``; returns the device status word (VCE_DEVSTATUS_TIMEOUT expected)."""
+    lib = library()
+    X = _bf16_2d(X, "X")
+    W = _bf16_2d(W, "W")
+    n, h = X.shape
+    v = W.shape[0]
+    dev = X.device
+    target = _target(target, n)
+    loss = torch.empty(n, dtype=torch.float32, device=dev)
+    lse = torch.empty(n, dtype=torch.float32, device=dev)
+    ws = torch.empty(max(1, lce_workspace_size(n, h, v, REDUCE_NONE)), dtype=torch.uint8, device=dev)
+    if dev_status is None:
+        dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
+    st = _on(dev, lib.vce_selftest_lce_forward_timeout, _ptr(X), _ptr(W), n, h, v, _ptr(target),
+             int(timeout_ns), _ptr(loss), _ptr(lse), _ptr(ws), ws.numel(), _ptr(dev_status), _stream(dev, stream))
+    _check("vce_selftest_lce_forward_timeout", st)
+    return dev_status
+
+
+def selftest_ce_fused_timeout(logits, target, grad_output, timeout_ns, *, dev_status=None, stream=None):
+    """Runs ce_forward_backward's ring kernel with its copies held back so that every wait
+    runs out after ``timeout_ns``; returns the device status word."""
+    lib = library()
+    dev = logits.device
+    n, vocab, stride = _rows_view(logits)
+    target = _target(target, n)
+    grad_output = _f32_on(grad_output, dev)
+    loss = torch.empty(n, dtype=torch.float32, device=dev)
+    stats = torch.empty(n, 2, dtype=torch.float32, device=dev)
+    dlogits = torch.empty_like(logits)
+    if dev_status is None:
+        dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
+    st = _on(dev, lib.vce_selftest_ce_fused_timeout, _ptr(logits), _dtype_code(logits), n, vocab, stride,
+             _ptr(target), _ptr(grad_output), int(timeout_ns), _ptr(loss), _ptr(stats), _ptr(dlogits),
+             _ptr(dev_status), _stream(dev, stream))
+    _check("vce_selftest_ce_fused_timeout", st)
+    return dev_status
