@@ -28,6 +28,7 @@ workload (a few tokens / rows per step) on the host cores.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -50,6 +51,35 @@ PUBLISHED_MODEL_SHAPES_FB_MS = {"qwen3_30b_a3b_8192x2048x151936": 13.692,
                                 "deepseek_v3_8192x7168x129280": 43.588}
 
 
+CSRC = os.path.join(ROOT, "vocabulary_cross_entropy_gb300", "csrc")
+
+# Kernel sources behind each traffic figure below and their SHA-256 (first 16 hex
+# digits) when the counters were taken.  A traffic figure is reported only while
+# the sources still hash to that digest; after any change it is null until the
+# counters are taken again.
+TRAFFIC_SOURCES = {
+    "gemm": (("lce_tc.cu", "sm100_ptx.cuh", "vce_internal.cuh"), "3bff0630300c1b13"),
+    "rows": (("ce_rows.cu", "sm100_ptx.cuh", "vce_internal.cuh"), "42ff30f251b6e68b"),
+}
+
+
+def source_digest(names):
+    h = hashlib.sha256()
+    for name in names:
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_current(kind) -> bool:
+    """Whether the kernels behind the ``kind`` traffic figures are unchanged since their capture."""
+    names, digest = TRAFFIC_SOURCES[kind]
+    try:
+        return source_digest(names) == digest
+    except OSError:
+        return False
+
+
 def FWD_GEMM_TRAFFIC_BYTES(wl):
     """DRAM bytes (read + write) per launch of the forward GEMM, from a one-pass ncu
     capture (dram__bytes_read.sum, dram__bytes_write.sum) of a full-size launch at
@@ -57,7 +87,7 @@ def FWD_GEMM_TRAFFIC_BYTES(wl):
     bytes and the per-tile partials grow with V.  None for workloads outside that
     N = H = 4096 family."""
     captured_v, read_bytes, write_bytes = 131072, 1.108554752e9, 19.760128e6
-    if wl.n != 4096 or wl.hidden != 4096:
+    if wl.n != 4096 or wl.hidden != 4096 or not traffic_current("gemm"):
         return None
     x_bytes = wl.n * wl.hidden * 2
     scale = wl.vocab / captured_v
@@ -77,7 +107,7 @@ LOGITS_CAPTURED_TRAFFIC = {
 def LOGITS_TRAFFIC_BYTES(wl, kernel):
     """Read + write DRAM bytes per launch of one row kernel, scaled from the 2048-row
     capture by the row count.  None for other vocabularies or dtypes."""
-    if wl.vocab != 128256 or wl.dtype != "bf16":
+    if wl.vocab != 128256 or wl.dtype != "bf16" or not traffic_current("rows"):
         return None
     read_bytes, write_bytes = LOGITS_CAPTURED_TRAFFIC[kernel]
     return (read_bytes + write_bytes) * wl.n_rows / 2048
@@ -134,7 +164,7 @@ def max_over_ranks(pg, x: float) -> float:
 # ---------------------------------------------------------------------------
 
 class Clocks:
-    """nvidia-smi sampling (every 50 ms) around a timed region.
+    """nvidia-smi sampling (every 20 ms) around a timed region.
 
     Each sample carries nvidia-smi's own timestamp, and the summary keeps only the
     samples taken between entering and leaving the ``with`` block, so that idle
@@ -143,7 +173,7 @@ class Clocks:
     QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
-    INTERVAL_MS = 50
+    INTERVAL_MS = 20
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
@@ -324,9 +354,11 @@ class LogitsStep:
         return (self.bytes_fwd() + self.bytes_bwd()) / 1e9  # GB per step
 
 
-def time_steps(step, steps, warmup, pg, events_for=("forward", "backward")):
+def time_steps(step, steps, warmup, pg, phase_events=True):
     """Returns (total_ms max over ranks, {phase: mean ms per launch}); the library's kernel
-    launches inside the timed region are left in ``step.timed_launches``."""
+    launches inside the timed region are left in ``step.timed_launches``.  With
+    ``phase_events`` False only the region is timed (no per-call events: for steps of a
+    few microseconds, where recording events would add to the host time measured)."""
     import torch
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
@@ -335,27 +367,59 @@ def time_steps(step, steps, warmup, pg, events_for=("forward", "backward")):
     torch.cuda.synchronize()
     barrier(pg)
     torch.cuda.synchronize()
+    phases = ("forward", "backward") if phase_events else ()
     ev = {p: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(steps)] for p in events_for}
+              for _ in range(steps)] for p in phases}
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     launches0 = step.vce.vce_kernel_launches()
     start.record(stream)
-    for i in range(steps):
-        ev["forward"][i][0].record(stream)
-        step.forward()
-        ev["forward"][i][1].record(stream)
-        ev["backward"][i][0].record(stream)
-        step.backward()
-        ev["backward"][i][1].record(stream)
+    if phase_events:
+        for i in range(steps):
+            ev["forward"][i][0].record(stream)
+            step.forward()
+            ev["forward"][i][1].record(stream)
+            ev["backward"][i][0].record(stream)
+            step.backward()
+            ev["backward"][i][1].record(stream)
+    else:
+        for i in range(steps):
+            step.forward()
+            step.backward()
     end.record(stream)
     step.timed_launches = step.vce.vce_kernel_launches() - launches0
     torch.cuda.synchronize()
     barrier(pg)
     torch.cuda.synchronize()
     total = max_over_ranks(pg, start.elapsed_time(end))
-    phases = {p: statistics.mean(a.elapsed_time(b) for a, b in ev[p]) for p in events_for}
-    return total, phases
+    out = {p: statistics.mean(a.elapsed_time(b) for a, b in ev[p]) for p in phases}
+    return total, out
+
+
+MIN_REGION_S = 0.5  # the sub-measurements time at least this long: 20+ clock samples each
+
+
+def steps_for(fn, min_steps, min_s=MIN_REGION_S, pg=None):
+    """Step count whose timed region lasts at least ``min_s``, from the wall time of a
+    short untimed probe of ``fn`` (one step); the same count on every rank."""
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    k = 3
+    t0 = time.perf_counter()
+    for _ in range(k):
+        fn()
+    torch.cuda.synchronize()
+    per = max((time.perf_counter() - t0) / k, 1e-6)
+    return int(max_over_ranks(pg, float(max(min_steps, math.ceil(min_s / per)))))
+
+
+def both(step):
+    """One forward + backward of ``step`` (for steps_for)."""
+    def fn():
+        step.forward()
+        step.backward()
+    return fn
 
 
 def time_graph_replay(step, k, warmup):
@@ -408,16 +472,20 @@ def peak_extra_memory(step):
     return torch.cuda.max_memory_allocated() - base
 
 
+def fused_logits_call(step):
+    wl = step.wl
+    step.vce.ce_forward_backward(step.d["logits"], step.d["target"], step.d["grad"], wl.label_smoothing,
+                                 wl.reduce_loss, dlogits=step.dlogits, loss=step.loss, stats=step.stats,
+                                 n_valid=step.n_valid, workspace=step.ws, dev_status=step.status)
+
+
 def time_fused_logits(step, steps, warmup, pg):
     """Mean ms of ce_forward_backward over ``steps`` timed calls (separate output buffer)."""
     import torch
-    wl = step.wl
     stream = torch.cuda.current_stream()
 
     def one():
-        step.vce.ce_forward_backward(step.d["logits"], step.d["target"], step.d["grad"], wl.label_smoothing,
-                                     wl.reduce_loss, dlogits=step.dlogits, loss=step.loss, stats=step.stats,
-                                     n_valid=step.n_valid, workspace=step.ws, dev_status=step.status)
+        fused_logits_call(step)
 
     for _ in range(warmup):
         one()
@@ -754,13 +822,15 @@ LARGE_SLAB_CAP = 1 << 30  # dZ slab cap for the large workload: 1 GiB of BF16 gr
 LOGITS_SAMPLE_ROWS = 256
 
 
-def cpu_baseline_linear(wl):
-    smp = OracleLinearSample(wl, LIN_SAMPLE_TOKENS)
+def cpu_baseline_linear(wl, full=False):
+    """The oracle's forward + backward timed on the host cores: on every token of the
+    workload (``full``), else on its first LIN_SAMPLE_TOKENS tokens against the full W."""
+    smp = OracleLinearSample(wl, wl.n if full else LIN_SAMPLE_TOKENS)
     dt = smp.run()
+    what = (f"every token ({smp.tokens})" if smp.tokens == wl.n else f"the first {smp.tokens} tokens")
     return {"value": smp.flops / dt / 1e12, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
-            "sample": f"FP64 NumPy oracle forward+backward on the first {smp.tokens} tokens "
-                      f"of the workload against the full W ({wl.vocab}x{wl.hidden}); flops counted "
-                      f"as 8*tokens*H*V", "seconds": dt}
+            "sample": f"FP64 NumPy oracle forward+backward on {what} of the workload against the full W "
+                      f"({wl.vocab}x{wl.hidden}); flops counted as 8*tokens*H*V", "seconds": dt}
 
 
 def cpu_baseline_logits(wl):
@@ -768,6 +838,40 @@ def cpu_baseline_logits(wl):
     return {"value": nb / dt / 1e9, "unit": "GB/s", "cores": host_cores(), "kind": "oracle",
             "sample": f"FP64 NumPy oracle forward+backward on the first {LOGITS_SAMPLE_ROWS} rows",
             "seconds": dt}
+
+
+# ---------------------------------------------------------------------------
+# memory / speed trade of the dZ slab cap
+# ---------------------------------------------------------------------------
+
+# (workload, max_slab_bytes): the headline at 256 MiB and 64 MiB slabs (4 and 16
+# slabs instead of one 1 GiB slab) and the large workload at 256 MiB (16 slabs)
+SLAB_CAPS = (("headline", 256 << 20), ("headline", 64 << 20), ("large", 256 << 20))
+
+
+def slab_cap_sweep(dev, args, pg, local, headline_ms):
+    """lce_forward + lce_backward with the dZ slab capped: time, TFLOP/s and the peak
+    extra device memory of one call pair, against the uncapped headline step."""
+    import torch
+    out = {"headline_uncapped_ms": headline_ms, "runs": []}
+    for name, cap in SLAB_CAPS:
+        wl = wk.LINEAR_HEADLINE if name == "headline" else wk.LINEAR_LARGE
+        stp = LinearStep(wl, dev, max_slab_bytes=cap)
+        k = steps_for(both(stp), 3, pg=pg)
+        with Clocks(local) as ck:
+            t, ph = time_steps(stp, k, args.warmup, pg)
+        assert int(stp.status.item()) == 0, "device status reported an error"
+        ms = t / k
+        out["runs"].append({
+            "workload": wl.name, "max_slab_bytes": cap, "slabs": -(-wl.vocab // max(256, cap // (wl.n * 2) // 256 * 256)),
+            "ms_per_step": ms, "value": stp.units() / (ms / 1e3), "unit": "TFLOP/s",
+            "fwd_ms": ph["forward"], "bwd_ms": ph["backward"], "steps": k,
+            "workspace_bytes": stp.ws_bytes, "peak_extra_memory_bytes": peak_extra_memory(stp),
+            "vs_uncapped": (ms / headline_ms - 1.0) if name == "headline" else None,
+            "clocks": ck.summary()})
+        del stp
+        torch.cuda.empty_cache()
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -867,18 +971,23 @@ def main():
             lwl = dataclasses.replace(lwl, name=f"logits_{lwl.n_rows}x{lwl.vocab}" +
                                       ("" if lwl.dtype == "bf16" else "_" + lwl.dtype))
         st = LogitsStep(lwl, dev)
+        # as the headline (--workload logits) exactly K steps; as a sub-number, enough
+        # steps for a timed region of at least MIN_REGION_S
+        kl = args.steps if args.workload == "logits" else steps_for(both(st), args.steps, pg=pg)
         with Clocks(local) as ck:
-            total, ph = time_steps(st, args.steps, args.warmup, pg)
+            total, ph = time_steps(st, kl, args.warmup, pg)
         clocks_l = ck.summary()
-        gb = st.units() * world * args.steps / (total / 1e3)
+        gb = st.units() * world * kl / (total / 1e3)
         bwd_gbs = st.bytes_bwd() / (ph["backward"] / 1e3) / 1e9
         fwd_gbs = st.bytes_fwd() / (ph["forward"] / 1e3) / 1e9
         assert int(st.status.item()) == 0, "device status reported an error"
-        fused_ms = time_fused_logits(st, args.steps, args.warmup, pg)
+        kf = steps_for(lambda: fused_logits_call(st), args.steps, pg=pg)
+        with Clocks(local) as ckf:
+            fused_ms = time_fused_logits(st, kf, args.warmup, pg)
         fused_gbs = st.bytes_bwd() / (fused_ms / 1e3) / 1e9
         logits_obj = {
-            "metric": "logits-CE fwd+bwd HBM GB/s", "value": gb, "unit": "GB/s",
-            "ms_per_step": total / args.steps, "fwd_gbs": fwd_gbs, "bwd_gbs": bwd_gbs,
+            "metric": "logits-CE fwd+bwd HBM GB/s", "value": gb, "unit": "GB/s", "steps": kl,
+            "ms_per_step": total / kl, "fwd_gbs": fwd_gbs, "bwd_gbs": bwd_gbs,
             "fwd_ms": ph["forward"], "bwd_ms": ph["backward"],
             "config": {"workload": st.wl.name, "n_rows": st.wl.n_rows, "vocab": st.wl.vocab,
                        "dtype": st.wl.dtype, "label_smoothing": st.wl.label_smoothing,
@@ -898,10 +1007,10 @@ def main():
             "clocks": clocks_l,
             # ce_forward_backward: the same results as one forward + backward step with
             # one HBM read and one write per logit (timed separately, same workload)
-            "fused": {"ms_per_step": fused_ms, "value": fused_gbs, "unit": "GB/s",
+            "fused": {"ms_per_step": fused_ms, "value": fused_gbs, "unit": "GB/s", "steps": kf,
                       "algorithmic_bytes": st.bytes_bwd(), "frac": fused_gbs / pk["hbm"],
                       "traffic": LOGITS_TRAFFIC_BYTES(st.wl, "fused"),
-                      "speedup_vs_separate": (total / args.steps) / fused_ms},
+                      "speedup_vs_separate": (total / kl) / fused_ms, "clocks": ckf.summary()},
         }
         if rank == 0 and not args.no_cpu_baseline:
             logits_obj["cpu_baseline"] = cpu_baseline_logits(st.wl)
@@ -958,14 +1067,17 @@ def main():
                    "l2": "inputs larger than L2 (W is 1 GiB), no flush",
                    "workspace_bytes": st.ws_bytes},
         "fwd_ms": ph["forward"], "bwd_ms": ph["backward"], "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
-        # the forward GEMM is timed inside a continuous multi-step loop (power-capped
-        # regime), so its denominator is the sustained dense BF16 figure
+        # the timed region is K steps of ~10 ms, far shorter than the seconds-long loop
+        # behind the sustained figure, so the denominator is the burst figure; the
+        # sustained fraction is kept beside it
         "roofline": {"kernel": "tc_gemm_kernel<FwdEpi> (lce_forward: X W^T + softmax partials; "
                                "the combine and mean kernels add <2%)", "bound": "tensor",
-                     "achieved": fwd_tf, "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
-                     "frac": fwd_tf / pk["bf16_sustained"], "traffic": FWD_GEMM_TRAFFIC_BYTES(st.wl),
-                     "peak_source": pk["source"] + " bf16_tflops_sustained (cuBLAS, seconds-long loop)",
-                     "frac_of_burst_peak": fwd_tf / pk["bf16"],
+                     "achieved": fwd_tf, "peak": pk["bf16"], "unit": "TFLOP/s",
+                     "frac": fwd_tf / pk["bf16"], "traffic": FWD_GEMM_TRAFFIC_BYTES(st.wl),
+                     "peak_source": pk["source"] + " bf16_tflops (cuBLAS burst; timed region %.2f s)" % (
+                         total / 1e3),
+                     "frac_of_sustained_peak": fwd_tf / pk["bf16_sustained"],
+                     "step_frac_of_burst_peak": value / world / pk["bf16"],
                      # against the dense BF16 rate of the SMs at the clock they ran at:
                      # 8192 flops per SM per cycle x SM count x median SM clock
                      "frac_of_tensor_peak_at_clock": (
@@ -980,11 +1092,12 @@ def main():
     line["config"]["peak_extra_memory_bytes"] = peak_extra_memory(st)
     if logits_obj is not None:
         line["logits_ce"] = logits_obj
+    headline_ms = total / args.steps
     if args.large and lin is wk.LINEAR_HEADLINE:
         del st
         torch.cuda.empty_cache()
         big = LinearStep(wk.LINEAR_LARGE, dev, max_slab_bytes=LARGE_SLAB_CAP)
-        ksteps = max(3, args.steps // 3)
+        ksteps = steps_for(both(big), max(3, args.steps // 3), pg=pg)
         with Clocks(local) as ckb:
             tb, phb = time_steps(big, ksteps, args.warmup, pg)
         assert int(big.status.item()) == 0, "device status reported an error"
@@ -1000,32 +1113,43 @@ def main():
                        "peak_extra_memory_bytes": peak_extra_memory(big)},
             "clocks": ckb.summary(),
         }
+        if rank == 0 and not args.no_cpu_baseline:
+            line["linear_large"]["cpu_baseline"] = cpu_baseline_linear(big.wl)
         del big
+        torch.cuda.empty_cache()
+        line["slab_caps"] = slab_cap_sweep(dev, args, pg, local, headline_ms)
     if args.large and lin is wk.LINEAR_HEADLINE:
         # the two small configurations: the tiny FP32 logits case (launch latency)
         # and the 4096 x 2048 x 32000 linear case (per-token loss, 2% ignored)
         torch.cuda.empty_cache()
         tiny = LogitsStep(wk.LOGITS_TINY[3], dev)
         kt = 100
-        tt, pht = time_steps(tiny, kt, args.warmup, pg)
-        graph_us = time_graph_replay(tiny, kt, args.warmup)
+        _, pht = time_steps(tiny, kt, args.warmup, pg)
+        ktl = steps_for(both(tiny), kt, pg=pg)
+        with Clocks(local) as ckt:
+            tt, _ = time_steps(tiny, ktl, args.warmup, pg, phase_events=False)
+        graph_us = time_graph_replay(tiny, ktl, args.warmup)
         assert int(tiny.status.item()) == 0, "device status reported an error"
         sm = LinearStep(wk.LINEAR_SMALL, dev)
-        ks = max(3, args.steps // 3)
+        ks = steps_for(both(sm), max(3, args.steps // 3), pg=pg)
         with Clocks(local) as ckm:
             tsm, phm = time_steps(sm, ks, args.warmup, pg)
         assert int(sm.status.item()) == 0, "device status reported an error"
         line["small_configs"] = {
             "logits_tiny": {"workload": tiny.wl.name, "n_rows": tiny.wl.n_rows, "vocab": tiny.wl.vocab,
-                            "dtype": "f32", "us_per_step": 1e3 * tt / kt, "fwd_us": 1e3 * pht["forward"],
-                            "bwd_us": 1e3 * pht["backward"], "steps": kt, "graph_us_per_step": graph_us,
-                            "note": "ce_forward (+ mean) + ce_backward; launch-latency bound when called "
-                                    "from Python one by one; graph_us_per_step replays the step captured "
-                                    "in a CUDA graph"},
+                            "dtype": "f32", "us_per_step": 1e3 * tt / ktl, "steps": ktl,
+                            "fwd_us": 1e3 * pht["forward"], "bwd_us": 1e3 * pht["backward"],
+                            "phase_steps": kt, "graph_us_per_step": graph_us, "clocks": ckt.summary(),
+                            "note": "ce_forward (+ mean) + ce_backward called from Python one by one "
+                                    "(us_per_step: no per-call events; fwd_us/bwd_us: a separate run with "
+                                    "events around each call); graph_us_per_step replays the step "
+                                    "captured in a CUDA graph"},
             "linear_small": {"workload": sm.wl.name, "value": sm.units() * world * ks / (tsm / 1e3),
                              "unit": "TFLOP/s", "ms_per_step": tsm / ks, "fwd_ms": phm["forward"],
                              "bwd_ms": phm["backward"], "steps": ks, "clocks": ckm.summary()},
         }
+        if rank == 0 and not args.no_cpu_baseline:
+            line["small_configs"]["linear_small"]["cpu_baseline"] = cpu_baseline_linear(sm.wl, full=True)
         del tiny, sm
     if args.sweep and lin is wk.LINEAR_HEADLINE:
         torch.cuda.empty_cache()

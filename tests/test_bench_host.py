@@ -45,3 +45,22 @@ def test_clock_samples_without_readable_timestamps_all_count():
 def test_no_samples_gives_no_clock():
     c = _bench().Clocks(0)
     assert c.summary() == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+
+def test_traffic_figures_go_null_when_the_kernel_source_changes(monkeypatch):
+    b = _bench()
+    wl = b.wk.LINEAR_HEADLINE
+    for kind, (names, _) in b.TRAFFIC_SOURCES.items():
+        now = b.source_digest(names)
+        assert len(now) == 16 and int(now, 16) >= 0
+        # pretend the counters were taken on exactly the current sources
+        monkeypatch.setitem(b.TRAFFIC_SOURCES, kind, (names, now))
+    assert b.FWD_GEMM_TRAFFIC_BYTES(wl) is not None
+    assert b.LOGITS_TRAFFIC_BYTES(b.wk.LOGITS_MEMBOUND, "backward") is not None
+    # any other digest means the kernel changed after the capture: no traffic figure
+    names, _ = b.TRAFFIC_SOURCES["gemm"]
+    monkeypatch.setitem(b.TRAFFIC_SOURCES, "gemm", (names, "0" * 16))
+    assert b.FWD_GEMM_TRAFFIC_BYTES(wl) is None
+    names, _ = b.TRAFFIC_SOURCES["rows"]
+    monkeypatch.setitem(b.TRAFFIC_SOURCES, "rows", (names, "0" * 16))
+    assert b.LOGITS_TRAFFIC_BYTES(b.wk.LOGITS_MEMBOUND, "fused") is None
