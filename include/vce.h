@@ -82,6 +82,11 @@ typedef enum vce_dtype {
 
 #define VCE_DEVSTATUS_BAD_TARGET 1
 #define VCE_DEVSTATUS_TIMEOUT 2
+/* Set only by a library built with -DVCE_BOUNDS_CHECK (a debugging build; see
+ * vce_bounds_check_build): an address a kernel computed fell outside the
+ * element range, row or buffer it belongs to, or a bulk or tensor copy was not
+ * 16-byte aligned; that access was skipped instead of made. */
+#define VCE_DEVSTATUS_BOUNDS 4
 
 /* reduce_loss values */
 #define VCE_REDUCE_NONE 0 /* per-row loss */
@@ -97,6 +102,14 @@ int vce_version(void);
 /* Number of kernels this library has launched in this process so far (a host-side
  * counter; diagnostics, e.g. counting the launches of a timed region). */
 unsigned long long vce_kernel_launches(void);
+
+/* 1 when this library was built with -DVCE_BOUNDS_CHECK: every kernel then checks
+ * the addresses it computes (row element ranges, 16-byte vector and bulk-copy
+ * alignment, tensor-copy coordinates, output and workspace indices) before it
+ * uses them, ORs VCE_DEVSTATUS_BOUNDS into *dev_status and skips the access
+ * when one fails.  It stands in for a memory checker where none can run, and
+ * is slower; the normal build returns 0 and checks nothing. */
+int vce_bounds_check_build(void);
 
 /* ------------------------------------------------------------------------ */
 /* logits form                                                              */

@@ -329,6 +329,25 @@ def assert_fused_matches_separate(r, sep_f, sep_dz, target, dtype):
     assert np.linalg.norm(a - b) <= tol * np.linalg.norm(b) + 1e-30
 
 
+@pytest.mark.parametrize("vocab", [5003, 30000, 100000, 210000])
+def test_fused_bit_identical_where_threads_match(vocab):
+    # Rows the fused call gives the forward kernel's own thread count: up to
+    # 16 KiB (128 threads), 48-64 KiB (8 ring warps = 256 threads), above 112 KiB
+    # (16 ring warps = 512 threads, with and without the pinned area).  Each
+    # thread then takes the same elements in the same order as in ce_forward,
+    # and the second pass is ce_backward's arithmetic: every output bit matches.
+    n = 300
+    z = wk.normal_matrix(vocab, wk.TID_LOGITS, n, vocab, 3.0, True)
+    target = wk.uniform_targets(vocab, n, vocab, 0.1)
+    logits = to_dev(z, "bf16")
+    grad = np.ones(1, np.float32)
+    f, dz = run_gpu(logits, target, 0.1, True, grad)
+    r = run_fused(logits, target, 0.1, True, grad)
+    assert torch.equal(r.stats, f.stats) and torch.equal(r.loss, f.loss)
+    assert int(r.n_valid.item()) == int(f.n_valid.item())
+    assert torch.equal(r.dlogits.view(torch.int16), dz.view(torch.int16))
+
+
 FUSED = [
     # n, vocab, dtype, eps, reduce, inplace
     (128, 1024, "f32", 0.0, False, False),

@@ -106,6 +106,18 @@ def test_vocab_slabs_accumulate_dx(slab_rows):
     check_full(x, w, y, 0.1, True, np.ones(1, np.float32), max_slab_bytes=n * 2 * slab_rows)
 
 
+@pytest.mark.parametrize("n,h,v,slab_ids", [
+    # dX on 256 x 512 pair tiles (H >= 1024 and K chunks of at least 16384 ids):
+    (700, 1032, 70000, 0),        # a hidden size that ends 8 columns into its last 512-wide tile
+    (512, 1024, 100000, 65536),   # two slabs, the second narrower, FP32 dX summed across them
+])
+def test_dx_wide_tiles(n, h, v, slab_ids):
+    x = wk.normal_matrix(31, wk.TID_X, n, h, 1.0, True)
+    w = wk.normal_matrix(31, wk.TID_W, v, h, h ** -0.5, True)
+    y = wk.uniform_targets(31, n, v, 0.05)
+    check_full(x, w, y, 0.1, True, np.ones(1, np.float32), max_slab_bytes=n * 2 * slab_ids)
+
+
 def test_token_wave_boundaries():
     # 4097- and 5000-token shapes (one token past a 4K wave; a two-wave tail)
     for n in (4097, 5000):

@@ -14,6 +14,7 @@ from ._binding import (  # noqa: F401
     F32,
     DEVSTATUS_BAD_TARGET,
     DEVSTATUS_TIMEOUT,
+    DEVSTATUS_BOUNDS,
     REDUCE_NONE,
     REDUCE_MEAN,
     REDUCE_SUM,
@@ -22,6 +23,7 @@ from ._binding import (  # noqa: F401
     vce_status_string,
     vce_version,
     vce_kernel_launches,
+    vce_bounds_check_build,
     ce_workspace_size,
     ce_forward,
     ce_forward_noalloc,

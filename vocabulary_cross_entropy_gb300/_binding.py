@@ -8,12 +8,15 @@ from collections import namedtuple
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-library_path = os.path.join(_HERE, "libvce.so")
+# VCE_LIBRARY selects another build of the library (the bounds-checking
+# variant, libvce_bounds.so); by default the one built beside this file
+library_path = os.environ.get("VCE_LIBRARY") or os.path.join(_HERE, "libvce.so")
 
 BF16 = 0
 F32 = 1
 DEVSTATUS_BAD_TARGET = 1
 DEVSTATUS_TIMEOUT = 2
+DEVSTATUS_BOUNDS = 4
 REDUCE_NONE, REDUCE_MEAN, REDUCE_SUM = 0, 1, 2
 
 _c_i64 = ctypes.c_int64
@@ -46,6 +49,8 @@ def library() -> ctypes.CDLL:
     lib.vce_version.restype = _c_int
     lib.vce_kernel_launches.argtypes = []
     lib.vce_kernel_launches.restype = ctypes.c_ulonglong
+    lib.vce_bounds_check_build.argtypes = []
+    lib.vce_bounds_check_build.restype = _c_int
     lib.ce_workspace_size.argtypes = [_c_i64, _c_i64, _c_int]
     lib.ce_workspace_size.restype = _c_size
     lib.ce_forward.argtypes = [_c_p, _c_int, _c_i64, _c_i64, _c_i64, _c_p, _c_f32, _c_int, _c_i64,
@@ -93,6 +98,11 @@ def vce_version() -> int:
 def vce_kernel_launches() -> int:
     """Kernels the library has launched in this process (host-side count)."""
     return int(library().vce_kernel_launches())
+
+
+def vce_bounds_check_build() -> bool:
+    """Whether the loaded library is the bounds-checking variant."""
+    return bool(library().vce_bounds_check_build())
 
 
 def _check(func: str, status: int):
@@ -151,6 +161,9 @@ def _rows_view(logits: torch.Tensor):
     vocab = logits.shape[-1]
     if logits.dim() == 1:
         return 1, vocab, vocab
+    if logits.dim() == 2:  # the common case, read without building a view
+        n = logits.shape[0]
+        return n, vocab, logits.stride(0) if n > 1 else vocab
     flat = logits.view(-1, vocab) if logits.is_contiguous() else None
     if flat is None:
         try:

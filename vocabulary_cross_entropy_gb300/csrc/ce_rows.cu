@@ -100,6 +100,29 @@ struct RowSplit {
     }
 };
 
+// Checks of the bounds-checking build (VCE_BOUNDS; constant true otherwise):
+// element j of a row lies in [0, vocab); vector i of the row's 16-byte interior
+// lies inside the row and its address ``a`` is 16-byte aligned.
+__device__ __forceinline__ bool elem_ok(int64_t j, int64_t vocab, int* st) {
+    return VCE_BOUNDS(j >= 0 && j < vocab, st);
+}
+template <typename T>
+__device__ __forceinline__ bool vec_ok(const RowSplit<T>& sp, int64_t i, int64_t vocab, const void* a, int* st) {
+    return VCE_BOUNDS(i >= 0 && i < sp.nvec && sp.head + (i + 1) * Elem<T>::kVec <= vocab && aligned16(a), st);
+}
+
+// Writes a row of zeros (the gradient of an ignored row or of a bad target).
+template <int THREADS, typename T>
+__device__ __forceinline__ void row_zero(T* q, const RowSplit<T>& sp, int64_t vocab, int* st) {
+    using E = Elem<T>;
+    if (threadIdx.x < sp.head && elem_ok(threadIdx.x, vocab, st)) E::store1(q + threadIdx.x, 0.f);
+    uint4* qv = reinterpret_cast<uint4*>(q + sp.head);
+    for (int64_t i = threadIdx.x; i < sp.nvec; i += THREADS)
+        if (vec_ok(sp, i, vocab, qv + i, st)) qv[i] = make_uint4(0, 0, 0, 0);
+    for (int64_t j = sp.tail0 + threadIdx.x; j < vocab; j += THREADS)
+        if (elem_ok(j, vocab, st)) E::store1(q + j, 0.f);
+}
+
 // ---------------------------------------------------------------------------
 // online softmax accumulator: s = sum exp(z - m) over the values seen
 // ---------------------------------------------------------------------------
@@ -214,7 +237,7 @@ ce_forward_rows(const T* __restrict__ logits, int64_t n_rows, int64_t vocab, int
         const T* p = logits + row * stride;
         const RowSplit<T> sp(p, vocab);
         OnlineLse acc;
-        if (threadIdx.x < sp.head) {
+        if (threadIdx.x < sp.head && elem_ok(threadIdx.x, vocab, dev_status)) {
             float v[1] = {E::load1(p + threadIdx.x)};
             acc.push<1, kSmooth>(v);
         }
@@ -223,7 +246,9 @@ ce_forward_rows(const T* __restrict__ logits, int64_t n_rows, int64_t vocab, int
         for (; i + (U - 1) * THREADS < sp.nvec; i += U * THREADS) {
             uint4 raw[U];
 #pragma unroll
-            for (int u = 0; u < U; ++u) raw[u] = __ldcs(pv + i + u * THREADS);
+            for (int u = 0; u < U; ++u)
+                raw[u] = vec_ok(sp, i + u * THREADS, vocab, pv + i + u * THREADS, dev_status)
+                             ? __ldcs(pv + i + u * THREADS) : make_uint4(0, 0, 0, 0);
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 float v[V];
@@ -233,11 +258,11 @@ ce_forward_rows(const T* __restrict__ logits, int64_t n_rows, int64_t vocab, int
         }
         for (; i < sp.nvec; i += THREADS) {
             float v[V];
-            E::unpack(__ldcs(pv + i), v);
+            E::unpack(vec_ok(sp, i, vocab, pv + i, dev_status) ? __ldcs(pv + i) : make_uint4(0, 0, 0, 0), v);
             acc.push<V, kSmooth>(v);
         }
         for (int64_t j = sp.tail0 + threadIdx.x; j < vocab; j += THREADS) {
-            float v[1] = {E::load1(p + j)};
+            float v[1] = {elem_ok(j, vocab, dev_status) ? E::load1(p + j) : 0.f};
             acc.push<1, kSmooth>(v);
         }
         block_merge<THREADS, kSmooth>(acc, sm_m, sm_s, sm_sum);
@@ -282,10 +307,7 @@ ce_backward_rows(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride,
         const bool bad = !ignored && (y < 0 || y >= vocab);
         if (ignored || bad) {
             if (bad && threadIdx.x == 0) report(dev_status, VCE_DEVSTATUS_BAD_TARGET);
-            if (threadIdx.x < sp.head) E::store1(q + threadIdx.x, 0.f);
-            uint4* qv = reinterpret_cast<uint4*>(q + sp.head);
-            for (int64_t i = threadIdx.x; i < sp.nvec; i += THREADS) qv[i] = make_uint4(0, 0, 0, 0);
-            for (int64_t j = sp.tail0 + threadIdx.x; j < vocab; j += THREADS) E::store1(q + j, 0.f);
+            row_zero<THREADS, T>(q, sp, vocab, dev_status);
             continue;
         }
         const float g = upstream_grad(reduce_loss, grad_output, n_valid, row);
@@ -296,6 +318,7 @@ ce_backward_rows(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride,
         const float c = g * (1.f - eps);          // target class
 
         auto grad1 = [&](int64_t j) {
+            if (!elem_ok(j, vocab, dev_status)) return;
             const float z = E::load1(p + j);
             float d = fmaf(gp, ex2f(fmaf(z, kLog2e, negl)), -b);
             if (j == y) d -= c;
@@ -313,17 +336,20 @@ ce_backward_rows(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride,
 #pragma unroll
                 for (int k = 0; k < V; ++k) v[k] -= (base + k == y) ? c : 0.f;
             }
-            __stcs(qv + i, E::pack(v));
+            if (vec_ok(sp, i, vocab, qv + i, dev_status)) __stcs(qv + i, E::pack(v));
         };
         int64_t i = threadIdx.x;
         for (; i + (U - 1) * THREADS < sp.nvec; i += U * THREADS) {
             uint4 raw[U];
 #pragma unroll
-            for (int u = 0; u < U; ++u) raw[u] = __ldcs(pv + i + u * THREADS);
+            for (int u = 0; u < U; ++u)
+                raw[u] = vec_ok(sp, i + u * THREADS, vocab, pv + i + u * THREADS, dev_status)
+                             ? __ldcs(pv + i + u * THREADS) : make_uint4(0, 0, 0, 0);
 #pragma unroll
             for (int u = 0; u < U; ++u) gradv(raw[u], i + u * THREADS);
         }
-        for (; i < sp.nvec; i += THREADS) gradv(__ldcs(pv + i), i);
+        for (; i < sp.nvec; i += THREADS)
+            gradv(vec_ok(sp, i, vocab, pv + i, dev_status) ? __ldcs(pv + i) : make_uint4(0, 0, 0, 0), i);
         for (int64_t j = sp.tail0 + threadIdx.x; j < vocab; j += THREADS) grad1(j);
     }
 }
@@ -478,10 +504,11 @@ __device__ __forceinline__ void prefetch_row_l2(const T* row, int64_t vocab) {
 
 // Streams one row through the online (max, sum exp) accumulator.
 template <int THREADS, int U, typename T, bool kSmooth>
-__device__ __forceinline__ void row_online_lse(const T* p, const RowSplit<T>& sp, int64_t vocab, OnlineLse& acc) {
+__device__ __forceinline__ void row_online_lse(const T* p, const RowSplit<T>& sp, int64_t vocab, OnlineLse& acc,
+                                               int* st) {
     using E = Elem<T>;
     constexpr int V = E::kVec;
-    if (threadIdx.x < sp.head) {
+    if (threadIdx.x < sp.head && elem_ok(threadIdx.x, vocab, st)) {
         float v[1] = {E::load1(p + threadIdx.x)};
         acc.push<1, kSmooth>(v);
     }
@@ -490,7 +517,9 @@ __device__ __forceinline__ void row_online_lse(const T* p, const RowSplit<T>& sp
     for (; i + (U - 1) * THREADS < sp.nvec; i += U * THREADS) {
         uint4 raw[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) raw[u] = pv[i + u * THREADS];  // default caching: the row is read again
+        for (int u = 0; u < U; ++u)  // default caching: the row is read again
+            raw[u] = vec_ok(sp, i + u * THREADS, vocab, pv + i + u * THREADS, st) ? pv[i + u * THREADS]
+                                                                                  : make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             float v[V];
@@ -500,22 +529,13 @@ __device__ __forceinline__ void row_online_lse(const T* p, const RowSplit<T>& sp
     }
     for (; i < sp.nvec; i += THREADS) {
         float v[V];
-        E::unpack(pv[i], v);
+        E::unpack(vec_ok(sp, i, vocab, pv + i, st) ? pv[i] : make_uint4(0, 0, 0, 0), v);
         acc.push<V, kSmooth>(v);
     }
     for (int64_t j = sp.tail0 + threadIdx.x; j < vocab; j += THREADS) {
-        float v[1] = {E::load1(p + j)};
+        float v[1] = {elem_ok(j, vocab, st) ? E::load1(p + j) : 0.f};
         acc.push<1, kSmooth>(v);
     }
-}
-
-template <int THREADS, typename T>
-__device__ __forceinline__ void row_zero(T* q, const RowSplit<T>& sp, int64_t vocab) {
-    using E = Elem<T>;
-    if (threadIdx.x < sp.head) E::store1(q + threadIdx.x, 0.f);
-    uint4* qv = reinterpret_cast<uint4*>(q + sp.head);
-    for (int64_t i = threadIdx.x; i < sp.nvec; i += THREADS) qv[i] = make_uint4(0, 0, 0, 0);
-    for (int64_t j = sp.tail0 + threadIdx.x; j < vocab; j += THREADS) E::store1(q + j, 0.f);
 }
 
 // Row kernel doing the forward and, with the row still in L2, the backward:
@@ -548,11 +568,11 @@ ce_fused_rows(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
                 loss_rows[row] = 0.f;
                 stats[row] = make_float2(0.f, 0.f);
             }
-            row_zero<THREADS, T>(q, sp, vocab);
+            row_zero<THREADS, T>(q, sp, vocab, dev_status);
             continue;
         }
         OnlineLse acc;
-        row_online_lse<THREADS, U1, T, kSmooth>(p, sp, vocab, acc);
+        row_online_lse<THREADS, U1, T, kSmooth>(p, sp, vocab, acc, dev_status);
         block_merge<THREADS, kSmooth>(acc, sm_m, sm_s, sm_sum);
         const bool bad = y < 0 || y >= vocab;
         if (threadIdx.x == 0) {
@@ -576,7 +596,7 @@ ce_fused_rows(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
         }
         __syncthreads();
         if (bad) {
-            row_zero<THREADS, T>(q, sp, vocab);
+            row_zero<THREADS, T>(q, sp, vocab, dev_status);
             __syncthreads();
             continue;
         }
@@ -587,6 +607,7 @@ ce_fused_rows(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
         const float b = g * eps / float(vocab);
         const float c = g * (1.f - eps);
         auto grad1 = [&](int64_t j) {
+            if (!elem_ok(j, vocab, dev_status)) return;
             const float z = E::load1(p + j);
             float d = fmaf(gp, ex2f(fmaf(z, kLog2e, negl)), -b);
             if (j == y) d -= c;
@@ -607,17 +628,20 @@ ce_fused_rows(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
 #pragma unroll
                 for (int k = 0; k < V; ++k) v[k] -= (base + k == y) ? c : 0.f;
             }
-            __stcs(qv + i, E::pack(v));
+            if (vec_ok(sp, i, vocab, qv + i, dev_status)) __stcs(qv + i, E::pack(v));
         };
         int64_t i = threadIdx.x;
         for (; i + (U - 1) * THREADS < sp.nvec; i += U * THREADS) {
             uint4 raw[U];
 #pragma unroll
-            for (int u = 0; u < U; ++u) raw[u] = __ldcs(pv + i + u * THREADS);
+            for (int u = 0; u < U; ++u)
+                raw[u] = vec_ok(sp, i + u * THREADS, vocab, pv + i + u * THREADS, dev_status)
+                             ? __ldcs(pv + i + u * THREADS) : make_uint4(0, 0, 0, 0);
 #pragma unroll
             for (int u = 0; u < U; ++u) gradv(raw[u], i + u * THREADS);
         }
-        for (; i < sp.nvec; i += THREADS) gradv(__ldcs(pv + i), i);
+        for (; i < sp.nvec; i += THREADS)
+            gradv(vec_ok(sp, i, vocab, pv + i, dev_status) ? __ldcs(pv + i) : make_uint4(0, 0, 0, 0), i);
         for (int64_t j = sp.tail0 + threadIdx.x; j < vocab; j += THREADS) grad1(j);
         __syncthreads();  // shared scratch reused by the next row
     }
@@ -790,8 +814,20 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
         uint32_t slot = 0, ph = 0, issued = 0, pin_ph = 0, pin_issued = 0;
         bool ok = true;
         const uint64_t keep = kHint ? l2_policy_evict_last() : 0, drop = kHint ? l2_policy_evict_first() : 0;
+        // bounds-checking build: a copy of ``bytes`` from offset ``off`` of a row's
+        // 16-byte interior (``total`` bytes from ``src``) into shared memory at
+        // ``dst``, which must end by ``dst_end``
+        auto copy_ok = [&](const uint8_t* src, uint64_t total, uint64_t off, uint32_t bytes, const uint8_t* dst,
+                           const uint8_t* dst_end) {
+            return VCE_BOUNDS(aligned16(src + off) && aligned16(dst) && bytes > 0 && bytes % 16 == 0 &&
+                                  off + bytes <= total && dst + bytes <= dst_end,
+                              dev_status);
+        };
+        // the next row's target is loaded while this row's copies are issued
+        int64_t y_next = int64_t(blockIdx.x) < n_rows ? target[blockIdx.x] : ignore_idx;
         for (int64_t row = blockIdx.x; row < n_rows && ok && !hold; row += gridDim.x) {
-            const int64_t y = target[row];
+            const int64_t y = y_next;
+            y_next = row + gridDim.x < n_rows ? target[row + gridDim.x] : ignore_idx;
             if (y == ignore_idx) continue;
             const bool bad = y < 0 || y >= vocab;
             const T* p = logits + row * stride;
@@ -807,8 +843,13 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
                     break;
                 }
                 const uint64_t pbytes = total < np * CH ? total : np * CH;
-                mbar_arrive_expect_tx(pin_full, uint32_t(pbytes));
+                bool pin_ok = true;
                 for (uint64_t k = 0; k < np; ++k) {
+                    const uint32_t bytes = uint32_t(total - k * CH < CH ? total - k * CH : CH);
+                    pin_ok = pin_ok && copy_ok(src, total, k * CH, bytes, pin + k * CH, pin + size_t(P) * CH);
+                }
+                mbar_arrive_expect_tx(pin_full, pin_ok ? uint32_t(pbytes) : 0u);
+                for (uint64_t k = 0; k < np && pin_ok; ++k) {
                     const uint32_t bytes = uint32_t(total - k * CH < CH ? total - k * CH : CH);
                     if (kHint)
                         bulk_load_shared_hint(smem_u32(pin + k * CH), src + k * CH, bytes, smem_u32(pin_full), drop);
@@ -825,11 +866,13 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
                         break;
                     }
                     const uint32_t bytes = uint32_t(total - off < CH ? total - off : CH);
-                    mbar_arrive_expect_tx(&full[slot], bytes);
-                    if (kHint)
+                    const bool cok = copy_ok(src, total, off, bytes, ring + size_t(slot) * CH,
+                                             ring + size_t(slot + 1) * CH);
+                    mbar_arrive_expect_tx(&full[slot], cok ? bytes : 0u);
+                    if (cok && kHint)
                         bulk_load_shared_hint(smem_u32(ring + size_t(slot) * CH), src + off, bytes,
                                               smem_u32(&full[slot]), pass == 0 ? keep : drop);
-                    else
+                    else if (cok)
                         bulk_load_shared(smem_u32(ring + size_t(slot) * CH), src + off, bytes,
                                          smem_u32(&full[slot]));
                     ++issued;
@@ -852,6 +895,14 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
     }
 
     // ---------------- compute warps ----------------
+    // The scalars of a row (its target, its head and tail elements outside the
+    // copied interior, its target logit and, without reduction, its upstream
+    // gradient) are fetched one row ahead: the next row's target is loaded as a
+    // row starts, and once the first pass has given it time to arrive, the
+    // next row's other scalars are loaded, so no dependent global load stands
+    // between a row's chunks, its merge and its second pass.  Ignored rows are
+    // still never read, and every value enters the arithmetic in the same
+    // order as before (the head first, the tail last).
     const int lane = tid & 31;
     uint32_t slot = 0, ph = 0, pin_ph = 0;
     bool ok = true;
@@ -868,8 +919,32 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
             ph ^= 1;
         }
     };
+    const bool g_rows = reduce_loss == VCE_REDUCE_NONE;
+    const float g_all = g_rows ? 0.f : upstream_grad(reduce_loss, grad_output, n_valid, 0);
+    struct Scalars {
+        float zh = 0.f, zt = 0.f, zy = 0.f, g = 0.f;  // head element, tail element, target logit, gradient
+    };
+    // loads the scalars of a row that is not ignored (each thread those it uses)
+    auto fetch = [&](int64_t r, int64_t yr) {
+        Scalars sc;
+        const T* pr = logits + r * stride;
+        const RowSplit<T> spr(pr, vocab);
+        if (tid < spr.head && elem_ok(tid, vocab, dev_status)) sc.zh = E::load1(pr + tid);
+        if (spr.tail0 + tid < vocab && elem_ok(spr.tail0 + tid, vocab, dev_status))
+            sc.zt = E::load1(pr + spr.tail0 + tid);  // the tail is shorter than a vector
+        if (tid == 0 && yr >= 0 && yr < vocab) sc.zy = E::load1(pr + yr);
+        if (g_rows) sc.g = grad_output[r];
+        return sc;
+    };
+    int64_t y = 0;
+    Scalars cur;
+    if (int64_t(blockIdx.x) < n_rows) {
+        y = target[blockIdx.x];
+        if (y != ignore_idx) cur = fetch(blockIdx.x, y);
+    }
     for (int64_t row = blockIdx.x; row < n_rows; row += gridDim.x) {
-        const int64_t y = target[row];
+        const int64_t nrow = row + gridDim.x;
+        const int64_t ny = nrow < n_rows ? target[nrow] : ignore_idx;  // used after this row's first pass
         const T* p = logits + row * stride;
         T* q = dlogits + row * stride;
         const RowSplit<T> sp(p, vocab);
@@ -878,7 +953,9 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
                 loss_rows[row] = 0.f;
                 stats[row] = make_float2(0.f, 0.f);
             }
-            row_zero<NT, T>(q, sp, vocab);
+            row_zero<NT, T>(q, sp, vocab, dev_status);
+            cur = ny != ignore_idx ? fetch(nrow, ny) : Scalars();
+            y = ny;
             continue;
         }
         const bool bad = y < 0 || y >= vocab;
@@ -889,7 +966,7 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
         // pass 1: online (max, sum exp) and sum of logits
         OnlineLse acc;
         if (tid < sp.head) {
-            float v[1] = {E::load1(p + tid)};
+            float v[1] = {cur.zh};
             acc.push<1, kSmooth>(v);
         }
         if (np > 0) {
@@ -930,8 +1007,8 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
             }
             release();
         }
-        for (int64_t j = sp.tail0 + tid; j < vocab; j += NT) {
-            float v[1] = {E::load1(p + j)};
+        if (sp.tail0 + tid < vocab) {
+            float v[1] = {cur.zt};
             acc.push<1, kSmooth>(v);
         }
         compute_merge<NT, kSmooth>(acc, sm_m, sm_s, sm_sum);
@@ -939,8 +1016,7 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
             const float lse = acc.m + logf(acc.s);
             float loss;
             if (!bad) {
-                const float zy = E::load1(p + y);
-                loss = lse - zy;
+                loss = lse - cur.zy;
                 if (kSmooth) loss = (1.f - eps) * loss + eps * (lse - acc.sum / float(vocab));
             } else {
                 loss = __int_as_float(0x7fc00000);
@@ -951,6 +1027,9 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
             *sm_lse = lse;
         }
         compute_sync<NT>();
+        // the next row's target has arrived during the first pass: fetch its
+        // other scalars now, to arrive during this row's second pass
+        const Scalars nxt = ny != ignore_idx ? fetch(nrow, ny) : Scalars();
         auto release_pin = [&]() {
             if (np > 0) {
                 __syncwarp();
@@ -960,24 +1039,25 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
         };
         if (bad) {
             release_pin();
-            row_zero<NT, T>(q, sp, vocab);
+            row_zero<NT, T>(q, sp, vocab, dev_status);
+            cur = nxt;
+            y = ny;
             continue;
         }
 
         // pass 2: dlogits = g (softmax - (1 - eps) onehot - eps / V)
-        const float g = upstream_grad(reduce_loss, grad_output, n_valid, row);
+        const float g = g_rows ? cur.g : g_all;
         const Exp2Offset eo = exp2_offset(*sm_lse);
         const float negl = eo.neg;
         const float gp = g * eo.fix;
         const float b = g * eps / float(vocab);
         const float c = g * (1.f - eps);
-        auto grad1 = [&](int64_t j) {
-            const float z = E::load1(p + j);
+        auto grad1 = [&](int64_t j, float z) {
             float d = fmaf(gp, ex2f(fmaf(z, kLog2e, negl)), -b);
             if (j == y) d -= c;
-            E::store1(q + j, d);
+            if (elem_ok(j, vocab, dev_status)) E::store1(q + j, d);
         };
-        if (tid < sp.head) grad1(tid);
+        if (tid < sp.head) grad1(tid, cur.zh);
         uint4* qv = reinterpret_cast<uint4*>(q + sp.head);
         auto gradv = [&](const uint4& raw, int64_t i) {
             float v[V];
@@ -988,7 +1068,7 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
 #pragma unroll
                 for (int k = 0; k < V; ++k) v[k] -= (base + k == y) ? c : 0.f;
             }
-            __stcs(qv + i, E::pack(v));
+            if (vec_ok(sp, i, vocab, qv + i, dev_status)) __stcs(qv + i, E::pack(v));
         };
         if (np > 0 && ok) {
             for (uint64_t k = 0; k < np; ++k) {
@@ -1016,7 +1096,9 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
             }
             release();
         }
-        for (int64_t j = sp.tail0 + tid; j < vocab; j += NT) grad1(j);
+        if (sp.tail0 + tid < vocab) grad1(sp.tail0 + tid, cur.zt);
+        cur = nxt;
+        y = ny;
     }
     // a compute thread whose wait gave up reports it too: the producer may have
     // issued its last copy and returned before the CTA gave up
@@ -1089,9 +1171,11 @@ void fused_dispatch(const void* logits, int64_t n_rows, int64_t vocab, int64_t s
     // at 16384 rows (fraction of the copy peak; in brackets the previous 256-,
     // 512- and 1024-thread row kernels with next-row prefetch):
     //   up to 48 KiB: four CTAs per SM, 4 compute warps, 48 KiB rings
-    //     (BF16 V = 12000: 0.69 [0.51]; 20000: 0.82 [0.65]; FP32 6000: 0.76 [0.59]);
+    //     (BF16 V = 12000: 0.71 [0.51]; 20000: 0.82 [0.65]; FP32 6000: 0.76 [0.59]);
+    //   up to 64 KiB: three CTAs per SM, 8 compute warps, 64 KiB rings
+    //     (BF16 32000: 0.87 against 0.85 with two CTAs per SM and 96 KiB rings);
     //   up to 112 KiB: two CTAs per SM, 8 compute warps, 96 KiB rings
-    //     (BF16 32000: 0.84 [0.80]; 50257: 0.87 [0.80]; FP32 16000: 0.88 [0.85]);
+    //     (BF16 40000: 0.89 [0.80]; 50257: 0.90 [0.80]; FP32 16000: 0.88 [0.85]);
     //   up to 400 KiB: one CTA per SM, 16 compute warps, a 192 KiB ring and L2
     //     hints that keep the first pass's bytes for the second (BF16 65536:
     //     0.88 [0.86]; 128256: 0.97 [0.86]; 151936: 0.93 [0.79]; FP32 50257: 0.93
@@ -1099,11 +1183,12 @@ void fused_dispatch(const void* logits, int64_t n_rows, int64_t vocab, int64_t s
     //   longer: the same with a 128 KiB ring and the first 64 KiB of each row
     //     pinned in shared memory for the second pass (BF16 256000: 0.89 against
     //     0.81 with the 192 KiB ring alone; FP32 128256: 0.89 against 0.83).
-    // Where a ring has as many compute threads as the forward kernel has threads
-    // per row, every thread takes the same vectors in the same order, so those
-    // rows equal ce_forward + ce_backward bit for bit: rows of 48-64 KiB (8 warps,
-    // the forward's 256 threads) and rows above 112 KiB (16 warps, its 512), as
-    // the rows up to 16 KiB do.
+    // (Measured over 11 ring shapes at 12000-100352: these were the fastest, or
+    // within 1%, at every length.)  Where a ring has as many compute threads as
+    // the forward kernel has threads per row, every thread takes the same
+    // vectors in the same order, so those rows equal ce_forward + ce_backward bit
+    // for bit: rows of 48-64 KiB (8 warps, the forward's 256 threads) and rows
+    // above 112 KiB (16 warps, its 512), as the rows up to 16 KiB do.
     const int64_t nvec = vocab / Elem<T>::kVec;
     const double l2 = double(dev.l2_bytes), row = double(vocab) * double(sizeof(T));
 #define VCE_FUSED_ARGS logits, n_rows, vocab, stride, target, eps, ignore_idx, n_valid, grad_output, reduce_loss, \
@@ -1114,6 +1199,8 @@ void fused_dispatch(const void* logits, int64_t n_rows, int64_t vocab, int64_t s
         else fused_launch<T, 128, 8, 4, 2, false>(VCE_FUSED_ARGS, grid);
     } else if (nvec * 16 <= 48 * 1024) {
         ring_launch<T, 4, 4, 48, 4, false>(VCE_FUSED_ARGS, dev, diag);
+    } else if (nvec * 16 <= 64 * 1024) {
+        ring_launch<T, 8, 4, 64, 3, false>(VCE_FUSED_ARGS, dev, diag);
     } else if (nvec * 16 <= 112 * 1024) {
         ring_launch<T, 8, 4, 96, 2, false>(VCE_FUSED_ARGS, dev, diag);
     } else if (nvec * 16 <= 400 * 1024) {

@@ -58,14 +58,28 @@ constexpr uint32_t kRingBytes = 196608;
 constexpr int kUnitRing = 8;                     // work units published ahead of the slowest reader
 constexpr uint32_t kUnitReaders = 10;            // odd CTA's producer, MMA issuer, 8 epilogue warps
 
+// A pair's output tile is 256 x BN.  One MMA instruction covers N <= 256, so a
+// 512-wide tile takes two per K step (pieces), each over its own 256 columns
+// of B; in every piece the even CTA holds the first half of the B rows and
+// the odd CTA the second.  Tiles up to 256 wide get two accumulators in
+// tensor memory (the epilogue of one tile overlaps the main loop of the
+// next); a 512-wide tile fills tensor memory with one, which suits products
+// with a long K (dX, K = a vocabulary slab), where the epilogue is short
+// beside the main loop.
 template <int BN>
 struct PairCfg {
-    static constexpr uint32_t kBBytes = (BN / 2) * BK * 2;  // this CTA's half of B
+    static constexpr int kMmaN = BN > 256 ? 256 : BN;        // N of one MMA instruction
+    static constexpr int kPieces = BN / kMmaN;               // MMAs per 16-wide K step
+    static constexpr int kPieceRows = kMmaN / 2;             // B rows this CTA stages per piece
+    static constexpr uint32_t kPieceBytes = uint32_t(kPieceRows) * BK * 2;
+    static constexpr uint32_t kBBytes = kPieces * kPieceBytes;  // this CTA's half of B
     static constexpr uint32_t kStageBytes = kABytes + kBBytes;
     static constexpr int kStages = (kRingBytes / kStageBytes) > 8 ? 8 : int(kRingBytes / kStageBytes);
-    static constexpr uint32_t kTmemCols = 2 * BN;           // two accumulators
+    static constexpr int kAccs = BN > 256 ? 1 : 2;           // accumulators in tensor memory
+    static constexpr uint32_t kTmemCols = kAccs * BN;
     static constexpr size_t kSmemBytes = size_t(kStages) * kStageBytes + 1024 + 512;
-    static_assert(BN == 128 || BN == 256, "tile width");
+    static_assert(BN == 128 || BN == 256 || BN == 512, "tile width");
+    static_assert(kTmemCols <= 512, "tensor memory columns");
 };
 
 struct GemmArgs {
@@ -78,6 +92,7 @@ struct GemmArgs {
     int* dev_status;
     uint64_t timeout_ns;  // limit of every wait for work or data
     int hold;             // self-test only: the scheduler publishes no unit
+    int64_t M, N, K;      // product extents (bounds-checking build)
 };
 
 // Work unit u -> output tile (tm, tn), K chunk ks and its K-block range [kb0, kb1).
@@ -138,6 +153,7 @@ struct FwdEpi {
     float* part_t;   // [tiles_n][M] sum of exp(z - max) z (entropy), NULL when not requested
     float* zy;       // [M] target logit
     int smooth;
+    int* dev_status;
 
     template <int BN>
     __device__ __forceinline__ void run(int64_t gm, int tn, int ks, uint32_t taddr) const {
@@ -201,7 +217,7 @@ struct FwdEpi {
             }
             s += t;
         }
-        if (row_ok) {
+        if (row_ok && VCE_BOUNDS(tn >= 0 && int64_t(tn) * BN < V && gm >= 0, dev_status)) {
             part_ms[int64_t(tn) * M + gm] = make_float2(m, s);
             if (smooth) part_sum[int64_t(tn) * M + gm] = sum;
             if (want_t) part_t[int64_t(tn) * M + gm] = te;
@@ -266,7 +282,9 @@ struct DzEpi {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) d[j] = 0.f;
             }
-            store_row32_bf16(out + col0, d, left);
+            if (VCE_BOUNDS(gm >= 0 && col0 >= 0 && col0 + (left < 32 ? left : 32) <= ld && slab0 + col0 < V,
+                           dev_status))
+                store_row32_bf16(out + col0, d, left);
         }
     }
 };
@@ -280,6 +298,8 @@ struct StoreEpi {
     int64_t split_stride;  // elements between the FP32 buffers of consecutive K chunks
     int mode;            // 0: out = D; 1: acc = D; 2: acc += D
     int64_t M, N;
+    int splits;          // K chunks, one FP32 buffer each
+    int* dev_status;
 
     template <int BN>
     __device__ __forceinline__ void run(int64_t gm, int tn, int ks, uint32_t taddr) const {
@@ -296,10 +316,14 @@ struct StoreEpi {
             float d[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) d[j] = __uint_as_float(r[j]);
+            const int64_t w = left < 32 ? left : 32;
             if (mode == 0) {
-                store_row32_bf16(out + gm * ld_out + col0, d, left);
+                if (VCE_BOUNDS(gm >= 0 && col0 >= 0 && col0 + w <= ld_out, dev_status))
+                    store_row32_bf16(out + gm * ld_out + col0, d, left);
                 continue;
             }
+            if (!VCE_BOUNDS(ks >= 0 && ks < splits && gm >= 0 && col0 >= 0 && col0 + w <= ld_acc, dev_status))
+                continue;
             float* a = acc + int64_t(ks) * split_stride + gm * ld_acc + col0;
             if (left >= 32) {
                 float4* a4 = reinterpret_cast<float4*>(a);
@@ -425,7 +449,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 int tm, tn, ks, kb0, kb1;
                 unit_coords(args, t, tm, tn, ks, kb0, kb1);
                 const int a_row = tm * BM + int(rank) * BM_CTA;
-                const int b_row = tn * BN + int(rank) * (BN / 2);
+                const int b_row = tn * BN + int(rank) * C::kPieceRows;  // first row of piece 0
+                // bounds-checking build: a tensor copy starts 16-byte aligned (x, the
+                // innermost coordinate, a multiple of 8 elements) inside the tile grid
+                // (a box may reach past the tensor's edge: those elements read as 0);
+                // a failed check skips the copy and the MMA's wait runs out
+                const int64_t m_pad = int64_t(args.tiles_m) * BM, n_pad = int64_t(args.tiles_n) * BN;
+                auto tma_ok = [&](int64_t x, int64_t y, int64_t x_end, int64_t y_end) {
+                    return VCE_BOUNDS(x >= 0 && x % 8 == 0 && x < x_end && y >= 0 && y < y_end, args.dev_status);
+                };
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, args.timeout_ns)) {
                         ok = false;
@@ -439,16 +471,23 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     if (kAMn) {
 #pragma unroll
                         for (int j = 0; j < BM_CTA / 64; ++j)
-                            tma_load_2d_pair(smem_u32(sa + j * 8192), &tmA, fb, a_row + j * 64, kb * BK);
-                    } else {
+                            if (tma_ok(a_row + j * 64, kb * BK, m_pad, args.K))
+                                tma_load_2d_pair(smem_u32(sa + j * 8192), &tmA, fb, a_row + j * 64, kb * BK);
+                    } else if (tma_ok(kb * BK, a_row, args.K, m_pad)) {
                         tma_load_2d_pair(smem_u32(sa), &tmA, fb, kb * BK, a_row);
                     }
-                    if (kBMn) {
 #pragma unroll
-                        for (int j = 0; j < (BN / 2) / 64; ++j)
-                            tma_load_2d_pair(smem_u32(sb + j * 8192), &tmB, fb, b_row + j * 64, kb * BK);
-                    } else {
-                        tma_load_2d_pair(smem_u32(sb), &tmB, fb, kb * BK, b_row);
+                    for (int pc = 0; pc < C::kPieces; ++pc) {
+                        const int row = b_row + pc * C::kMmaN;
+                        uint8_t* dst = sb + pc * C::kPieceBytes;
+                        if (kBMn) {
+#pragma unroll
+                            for (int j = 0; j < C::kPieceRows / 64; ++j)
+                                if (tma_ok(row + j * 64, kb * BK, n_pad, args.K))
+                                    tma_load_2d_pair(smem_u32(dst + j * 8192), &tmB, fb, row + j * 64, kb * BK);
+                        } else if (tma_ok(kb * BK, row, args.K, n_pad)) {
+                            tma_load_2d_pair(smem_u32(dst), &tmB, fb, kb * BK, row);
+                        }
                     }
                     issued |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -469,7 +508,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     } else if (warp == 1) {
         if (lane == 0 && leader) {
             // ---------------- MMA issuer (even CTA) ----------------
-            constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN, kAMn, kBMn);
+            constexpr uint32_t kIdesc = idesc_bf16_f32(BM, C::kMmaN, kAMn, kBMn);
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
             for (uint32_t seq = 0; ok; ++seq) {
@@ -495,9 +534,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     for (int kk = 0; kk < BK / 16; ++kk) {
                         const uint64_t ad = kAMn ? smem_desc_sw128(sa + kk * 2048, 8192, 1024)
                                                  : smem_desc_sw128(sa + kk * 32, 16, 1024);
-                        const uint64_t bd = kBMn ? smem_desc_sw128(sb + kk * 2048, 8192, 1024)
-                                                 : smem_desc_sw128(sb + kk * 32, 16, 1024);
-                        umma_bf16_pair(d_tmem, ad, bd, kIdesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                        for (int pc = 0; pc < C::kPieces; ++pc) {
+                            const uint32_t sbp = sb + pc * C::kPieceBytes;
+                            const uint64_t bd = kBMn ? smem_desc_sw128(sbp + kk * 2048, 8192, 1024)
+                                                     : smem_desc_sw128(sbp + kk * 32, 16, 1024);
+                            umma_bf16_pair(d_tmem + pc * C::kMmaN, ad, bd, kIdesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+                        }
                     }
                     umma_commit_pair(&empty[stage], 0x3);  // frees the stage in both CTAs
                     if (++stage == uint32_t(S)) {
@@ -507,8 +550,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 }
                 if (!ok) break;
                 umma_commit_pair(&tfull[acc], 0x3);
-                acc ^= 1u;
-                if (acc == 0) acc_phase ^= 1u;
+                if (++acc == uint32_t(C::kAccs)) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
             }
             // every MMA issued so far completes before tensor memory is released
             umma_commit_pair(drain, 0x1);
@@ -538,8 +583,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(tempty_leader[acc]);
-            acc ^= 1u;
-            if (acc == 0) acc_phase ^= 1u;
+            if (++acc == uint32_t(C::kAccs)) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
         }
     }
 
@@ -695,10 +742,13 @@ __global__ void reset_counter_kernel(int* counter) { *counter = 0; }
 // narrower than about sqrt(CTA pairs) tiles: when strips are too long for L2
 // (K = a vocabulary slab), the pairs working at one time then still cover a
 // near-square block of output tiles and share their strips while they stream.
-int raster_group(int tiles_fast, int64_t strip_bytes, const DeviceInfo& dev) {
+// ``aspect`` is the fast index's tile extent over the slow index's (BM / BN when
+// M is fast): a block of ``pairs`` tiles g fast x (pairs / g) slow covers the
+// fewest operand rows at g = sqrt(pairs / aspect).
+int raster_group(int tiles_fast, int64_t strip_bytes, double aspect, const DeviceInfo& dev) {
     const int pairs = dev.num_sms / 2;
     int g_win = 1;
-    while (g_win * g_win < pairs) ++g_win;
+    while (double(g_win) * g_win * aspect < pairs) ++g_win;
     const int64_t budget = int64_t(dev.l2_bytes / 3);
     const int64_t g_l2 = strip_bytes > 0 ? budget / strip_bytes : tiles_fast;
     int64_t g = g_l2 > g_win ? g_l2 : g_win;
@@ -738,12 +788,16 @@ vce_status launch_gemm(const CUtensorMap& a, const CUtensorMap& b, int64_t M, in
     args.m_fastest = m_fastest;
     {
         const int64_t strip = int64_t(m_fastest ? BM : BN) * args.kb_per_split * BK * 2;
-        args.group = raster_group(m_fastest ? args.tiles_m : args.tiles_n, strip, dev);
+        const double aspect = m_fastest ? double(BM) / BN : double(BN) / BM;
+        args.group = raster_group(m_fastest ? args.tiles_m : args.tiles_n, strip, aspect, dev);
     }
     args.counter = counter;
     args.dev_status = dev_status;
     args.timeout_ns = diag.timeout_ns;
     args.hold = diag.hold;
+    args.M = M;
+    args.N = N;
+    args.K = K;
     const int64_t units = int64_t(args.tiles_m) * args.tiles_n * args.k_splits;
     if (units <= 0 || args.k_blocks <= 0) return VCE_OK;
     const int64_t pairs = dev.num_sms / 2;
@@ -757,8 +811,8 @@ vce_status launch_gemm(const CUtensorMap& a, const CUtensorMap& b, int64_t M, in
 
 // Number of K chunks for the dX GEMM (K = vocabulary slab): the smallest count
 // in 1..4 whose work units fill the CTA pairs' last round best.
-int dx_k_splits(int64_t n, int64_t h, int num_sms) {
-    const int64_t tiles = ((n + BM - 1) / BM) * ((h + 255) / 256);
+int dx_k_splits(int64_t n, int64_t h, int bn, int num_sms) {
+    const int64_t tiles = ((n + BM - 1) / BM) * ((h + bn - 1) / bn);
     const int64_t pairs = num_sms / 2;
     int best = 1;
     double best_eff = 0.0;
@@ -772,6 +826,19 @@ int dx_k_splits(int64_t n, int64_t h, int num_sms) {
         }
     }
     return best;
+}
+
+// Width of the dX GEMM's pair tile (dX = dZ W: M = tokens, N = hidden, K = a
+// vocabulary slab of ``slab`` ids).  With 512-wide tiles each 256-token strip
+// of dZ is read once per 512 hidden columns instead of once per 256, and the 76
+// pairs in flight cover a block of about 16 x 5 tiles that shares its strips
+// in L2.  Its single accumulator leaves the epilogue (an FP32 partial of
+// 256 x 512) outside the main loop, which costs little only when each work
+// unit runs over a long K range: at least 16384 vocabulary ids per K chunk,
+// and hidden sizes of at least two such tiles.  Otherwise the 256-wide tile.
+int dx_tile_n(int64_t n, int64_t h, int64_t slab, int num_sms) {
+    if (h < 1024) return 256;
+    return slab / dx_k_splits(n, h, 512, num_sms) >= 16384 ? 512 : 256;
 }
 
 // dX = sum of the FP32 partials of every K chunk, rounded to BF16 (fixed order).
@@ -826,6 +893,7 @@ int64_t slab_ld(int64_t slab) { return (slab + 7) / 8 * 8; }
 struct BwdPlan {
     int64_t ld;      // dZ slab leading dimension
     int splits;      // K chunks of the dX GEMM
+    int tile_n;      // width of the dX GEMM's pair tile (every slab)
     bool direct;     // dX written as BF16 by the GEMM itself
     size_t dz_bytes, acc_bytes;
 };
@@ -836,7 +904,8 @@ BwdPlan plan_backward(int64_t n, int64_t h, int64_t v, int64_t slab, int num_sms
     // the chunk count the dX launch of the first (widest) slab really uses:
     // at most one chunk per 64-wide K block, every chunk non-empty
     const int64_t kb = ((slab < v ? slab : v) + BK - 1) / BK;
-    int splits = dx_k_splits(n, h, num_sms);
+    p.tile_n = dx_tile_n(n, h, slab < v ? slab : v, num_sms);
+    int splits = dx_k_splits(n, h, p.tile_n, num_sms);
     if (splits > kb) splits = int(kb);
     const int64_t per = (kb + splits - 1) / splits;
     p.splits = int((kb + per - 1) / per);
@@ -887,7 +956,8 @@ vce_status launch_lce_forward(const void* X, const void* W, int64_t n, int64_t h
     const FwdWs w = carve_forward(ws, n, v, reduce_loss);
     CUtensorMap tx, tw;
     if (!map_kmajor(&tx, X, h, n, h, BM_CTA) || !map_kmajor(&tw, W, h, v, h, kVocabTile / 2)) return VCE_ERR_CUDA;
-    FwdEpi epi{target, n, v, w.part_ms, w.part_sum, entropy ? w.part_t : nullptr, w.zy, eps != 0.f ? 1 : 0};
+    FwdEpi epi{target, n, v, w.part_ms, w.part_sum, entropy ? w.part_t : nullptr, w.zy, eps != 0.f ? 1 : 0,
+               dev_status};
     if (vce_status st =
             launch_gemm<FwdEpi, false, false, kVocabTile>(tx, tw, n, v, h, 1, 1, epi, w.counter, dev_status, s, dev,
                                                           diag))
@@ -937,15 +1007,19 @@ vce_status launch_lce_backward(const void* X, const void* W, int64_t n, int64_t 
                                                              dev))
             return st;
         // dW_slab = dZ^T X: M = vs, N = h, K = n (both operands MN-major)
-        StoreEpi we{dWb + v0 * h, h, nullptr, 0, 0, 0, vs, h};
+        StoreEpi we{dWb + v0 * h, h, nullptr, 0, 0, 0, vs, h, 1, dev_status};
         if (vce_status st =
                 launch_gemm<StoreEpi, true, true, 256>(tdz_mn, tx_mn, vs, h, n, 0, 1, we, counter, dev_status, s, dev))
             return st;
         // dX (+)= dZ W_slab: M = n, N = h, K = vs (W_slab read MN-major), K cut into plan.splits chunks
-        StoreEpi xe{dXb, h, acc, h, split_stride, plan.direct ? 0 : (v0 == 0 ? 1 : 2), n, h};
-        if (vce_status st = launch_gemm<StoreEpi, false, true, 256>(tdz_k, tws_mn, n, h, vs, 1, plan.splits, xe,
-                                                                    counter, dev_status, s, dev))
-            return st;
+        StoreEpi xe{dXb, h, acc, h, split_stride, plan.direct ? 0 : (v0 == 0 ? 1 : 2), n, h, plan.splits, dev_status};
+        const vce_status st =
+            plan.tile_n == 512
+                ? launch_gemm<StoreEpi, false, true, 512>(tdz_k, tws_mn, n, h, vs, 1, plan.splits, xe, counter,
+                                                          dev_status, s, dev)
+                : launch_gemm<StoreEpi, false, true, 256>(tdz_k, tws_mn, n, h, vs, 1, plan.splits, xe, counter,
+                                                          dev_status, s, dev);
+        if (st != VCE_OK) return st;
     }
     if (!plan.direct) {
         const int64_t count4 = n * h / 4;  // h is a multiple of 8

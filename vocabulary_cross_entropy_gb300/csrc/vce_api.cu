@@ -78,6 +78,14 @@ int vce_version(void) { return 100; }
 
 unsigned long long vce_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
+int vce_bounds_check_build(void) {
+#ifdef VCE_BOUNDS_CHECK
+    return 1;
+#else
+    return 0;
+#endif
+}
+
 size_t ce_workspace_size(int64_t n_rows, int64_t vocab, int reduce_loss) {
     (void)vocab;
     if (!reduce_loss || n_rows <= 0) return 0;

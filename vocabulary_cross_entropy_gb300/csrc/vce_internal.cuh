@@ -49,6 +49,21 @@ __device__ __forceinline__ void report(int* dev_status, int bits) {
     if (dev_status) atomicOr(dev_status, bits);
 }
 
+// Bounds checks of the debugging build (-DVCE_BOUNDS_CHECK): VCE_BOUNDS(cond,
+// status) is ``cond``, and a false one reports VCE_DEVSTATUS_BOUNDS; callers
+// skip the access it guards.  In the normal build it is the constant true.
+#ifdef VCE_BOUNDS_CHECK
+__device__ __forceinline__ bool bounds_ok(bool ok, int* dev_status) {
+    if (!ok) report(dev_status, VCE_DEVSTATUS_BOUNDS);
+    return ok;
+}
+#define VCE_BOUNDS(cond, status) ::vce::bounds_ok(bool(cond), (status))
+#else
+#define VCE_BOUNDS(cond, status) true
+#endif
+
+__device__ __forceinline__ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
 // Host-side count of the kernels this library has launched (diagnostics).
 void count_launch();
 
