@@ -58,8 +58,8 @@ CSRC = os.path.join(ROOT, "vocabulary_cross_entropy_gb300", "csrc")
 # the sources still hash to that digest; after any change it is null until the
 # counters are taken again.
 TRAFFIC_SOURCES = {
-    "gemm": (("lce_tc.cu", "sm100_ptx.cuh", "vce_internal.cuh"), "3bff0630300c1b13"),
-    "rows": (("ce_rows.cu", "sm100_ptx.cuh", "vce_internal.cuh"), "42ff30f251b6e68b"),
+    "gemm": (("lce_tc.cu", "sm100_ptx.cuh", "vce_internal.cuh"), "3264225edba913eb"),
+    "rows": (("ce_rows.cu", "sm100_ptx.cuh", "vce_internal.cuh"), "da8afd2ec2384851"),
 }
 
 
@@ -86,7 +86,7 @@ def FWD_GEMM_TRAFFIC_BYTES(wl):
     N = H = 4096, V = 131072, scaled to this workload's V: the X bytes stay, the W
     bytes and the per-tile partials grow with V.  None for workloads outside that
     N = H = 4096 family."""
-    captured_v, read_bytes, write_bytes = 131072, 1.108554752e9, 19.760128e6
+    captured_v, read_bytes, write_bytes = 131072, 1.107989504e9, 19.868416e6
     if wl.n != 4096 or wl.hidden != 4096 or not traffic_current("gemm"):
         return None
     x_bytes = wl.n * wl.hidden * 2
@@ -98,9 +98,9 @@ def FWD_GEMM_TRAFFIC_BYTES(wl):
 # captures (dram__bytes_read.sum, dram__bytes_write.sum) of 2048 rows of
 # V = 128256 BF16 with 5% of the rows ignored
 LOGITS_CAPTURED_TRAFFIC = {
-    "forward": (502.397952e6, 3.326976e6),
-    "backward": (502.323968e6, 467.554560e6),
-    "fused": (505.122304e6, 464.573952e6),
+    "forward": (502.385152e6, 2.968320e6),
+    "backward": (502.316800e6, 464.387584e6),
+    "fused": (506.150912e6, 464.366336e6),
 }
 
 
