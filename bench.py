@@ -1088,7 +1088,11 @@ def main():
         "gpu_launches": st.timed_launches,
         "clocks": clocks,
     }
-    line["entropy_cost"] = time_forward_entropy(st, max(3, args.steps), 3, pg)
+    # pairs of forwards (without, with the entropy output) filling at least MIN_REGION_S
+    ke = steps_for(lambda: (st.forward(), st.forward()), max(3, args.steps), pg=pg)
+    with Clocks(local) as ckent:
+        line["entropy_cost"] = time_forward_entropy(st, ke, 3, pg)
+    line["entropy_cost"]["clocks"] = ckent.summary()
     line["config"]["peak_extra_memory_bytes"] = peak_extra_memory(st)
     if logits_obj is not None:
         line["logits_ce"] = logits_obj

@@ -819,26 +819,48 @@ int dx_k_splits(int64_t n, int64_t h, int bn, int num_sms) {
     for (int s = 1; s <= 4; ++s) {
         const int64_t units = tiles * s;
         const int64_t rounds = (units + pairs - 1) / pairs;
-        const double eff = double(units) / double(rounds * pairs);
-        if (eff > best_eff + 0.02) {
-            best_eff = eff;
+        const double e = double(units) / double(rounds * pairs);
+        if (e > best_eff + 0.02) {
+            best_eff = e;
             best = s;
         }
     }
     return best;
 }
 
-// Width of the dX GEMM's pair tile (dX = dZ W: M = tokens, N = hidden, K = a
-// vocabulary slab of ``slab`` ids).  With 512-wide tiles each 256-token strip
-// of dZ is read once per 512 hidden columns instead of once per 256, and the 76
-// pairs in flight cover a block of about 16 x 5 tiles that shares its strips
-// in L2.  Its single accumulator leaves the epilogue (an FP32 partial of
-// 256 x 512) outside the main loop, which costs little only when each work
-// unit runs over a long K range: at least 16384 vocabulary ids per K chunk,
-// and hidden sizes of at least two such tiles.  Otherwise the 256-wide tile.
-int dx_tile_n(int64_t n, int64_t h, int64_t slab, int num_sms) {
-    if (h < 1024) return 256;
-    return slab / dx_k_splits(n, h, 512, num_sms) >= 16384 ? 512 : 256;
+// Tile width and K chunks of the dX GEMM (dX = dZ W: M = tokens, N = hidden,
+// K = a vocabulary slab of ``slab`` ids).  With 512-wide tiles each 256-token
+// strip of dZ is read once per 512 hidden columns instead of once per 256: less
+// DRAM and L2 traffic, which under the power cap buys clock (same-box A/B runs:
+// 1-4% faster steps at 2048-4096 tokens even where its fewer units fill the
+// pairs' rounds worse).  Its single accumulator leaves the epilogue (an FP32
+// partial of 256 x 512) outside the main loop, which costs little only when
+// each work unit runs over a long K range, so the wide tile takes the chunk
+// count that fills the rounds best among those that keep chunks of at least
+// 16384 vocabulary ids (hidden sizes of at least two tiles).  Otherwise the
+// 256-wide tile, with the chunk count of dx_k_splits.
+struct DxPlan {
+    int tile_n, splits;
+};
+
+DxPlan dx_plan(int64_t n, int64_t h, int64_t slab, int num_sms) {
+    if (h >= 1024) {
+        const int64_t tiles = ((n + BM - 1) / BM) * ((h + 511) / 512);
+        const int64_t pairs = num_sms / 2;
+        int best = 0;
+        double best_eff = 0.0;
+        for (int s = 1; s <= 4 && slab / s >= 16384; ++s) {
+            const int64_t units = tiles * s;
+            const int64_t rounds = (units + pairs - 1) / pairs;
+            const double e = double(units) / double(rounds * pairs);
+            if (e > best_eff + 0.02) {
+                best_eff = e;
+                best = s;
+            }
+        }
+        if (best > 0) return {512, best};
+    }
+    return {256, dx_k_splits(n, h, 256, num_sms)};
 }
 
 // dX = sum of the FP32 partials of every K chunk, rounded to BF16 (fixed order).
@@ -904,8 +926,9 @@ BwdPlan plan_backward(int64_t n, int64_t h, int64_t v, int64_t slab, int num_sms
     // the chunk count the dX launch of the first (widest) slab really uses:
     // at most one chunk per 64-wide K block, every chunk non-empty
     const int64_t kb = ((slab < v ? slab : v) + BK - 1) / BK;
-    p.tile_n = dx_tile_n(n, h, slab < v ? slab : v, num_sms);
-    int splits = dx_k_splits(n, h, p.tile_n, num_sms);
+    const DxPlan dp = dx_plan(n, h, slab < v ? slab : v, num_sms);
+    p.tile_n = dp.tile_n;
+    int splits = dp.splits;
     if (splits > kb) splits = int(kb);
     const int64_t per = (kb + splits - 1) / splits;
     p.splits = int((kb + per - 1) / per);
