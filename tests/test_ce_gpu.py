@@ -296,6 +296,41 @@ def test_membound_full_size_sampled():
     check_rows(f._replace(stats=f.stats), dz[sel], ref, ref_dz, rows, wl.dtype, True, inp.target)
 
 
+def test_logits_beyond_2_31_elements_sampled():
+    # 17000 x 128257 BF16 logits: 2.18e9 elements, so the rows from 16744 on start
+    # past element 2^31 (every row offset is 64-bit).  ce_forward + ce_backward into a
+    # separate buffer, then the fused call in place over the logits; sampled rows
+    # element by element, the mean over every row, N_v exactly.
+    import dataclasses
+    wl = dataclasses.replace(wk.LOGITS_MEMBOUND, name="logits_17000x128257", n_rows=17000, vocab=128257)
+    assert wl.n_rows * wl.vocab > 2 ** 31
+    inp = wk.make_logits_inputs(wl)
+    logits = to_dev(inp.logits, wl.dtype)
+    del inp.logits
+    f, dz = run_gpu(logits, inp.target, wl.label_smoothing, wl.reduce_loss, inp.grad)
+    n_valid_ref = int((inp.target != -100).sum())
+    assert int(f.n_valid.item()) == n_valid_ref and int(f.dev_status.item()) == 0
+    loss_rows = _oracle_rows_chunked(wl, inp.target)
+    mean_ref = oracle.mean_loss(loss_rows, n_valid_ref)
+    assert abs(f.loss.item() - mean_ref) <= 2e-3
+    rng = np.random.default_rng(1)
+    first_far = -(-(2 ** 31) // wl.vocab)  # the first row that starts past element 2^31
+    rows = np.unique(np.concatenate([rng.choice(wl.n_rows, 16, replace=False),
+                                     rng.choice(np.arange(first_far, wl.n_rows), 16, replace=False),
+                                     [0, first_far - 1, first_far, wl.n_rows - 1]]))
+    z = wk.logits_rows(wl, rows)
+    ref = oracle.ce_forward(z, inp.target[rows], wl.label_smoothing, False, dtype=wl.dtype)
+    ref_dz = oracle.ce_backward(z, inp.target[rows], ref["lse"], n_valid_ref, inp.grad,
+                                wl.label_smoothing, True, dtype=wl.dtype)
+    sel = torch.from_numpy(rows).to(DEV)
+    check_rows(f, dz[sel], ref, ref_dz, rows, wl.dtype, True, inp.target)
+    del dz
+    r = run_fused(logits, inp.target, wl.label_smoothing, wl.reduce_loss, inp.grad, inplace=True)
+    assert int(r.n_valid.item()) == n_valid_ref and int(r.dev_status.item()) == 0
+    assert abs(r.loss.item() - mean_ref) <= 2e-3
+    check_rows(r, r.dlogits[sel], ref, ref_dz, rows, wl.dtype, True, inp.target)
+
+
 # ---------------------------------------------------------------------------
 # fused forward + backward (ce_forward_backward)
 # ---------------------------------------------------------------------------

@@ -244,6 +244,19 @@ def test_full_size_sampled(wl, slab_cap, entropy):
     _sampled_check(wl, inp, f, b, entropy)
 
 
+def test_dz_slab_beyond_2_31_elements_sampled():
+    # One uncapped dZ slab of 16384 x 131080 (the leading dimension of V = 131073
+    # rounded up to 8): 2.1476e9 elements, past 2^31, so the dZ epilogue's stores,
+    # the tensor maps over dZ and the dX/dW reads of it need 64-bit offsets.
+    # H = 1024 keeps the oracle's FP64 forward to 4.4e12 flop; the wide dX tile runs.
+    wl = wk.LinearWorkload("linear_16384x1024x131073", 16384, 1024, 131073, ignore_frac=0.02,
+                           label_smoothing=0.1, reduce_loss=True)
+    assert wl.n * ((wl.vocab + 7) // 8 * 8) > 2 ** 31
+    inp = wk.make_linear_inputs(wl)
+    f, b = run(inp.x, inp.w, inp.target, wl.label_smoothing, wl.reduce_loss, inp.grad, 0, False)
+    _sampled_check(wl, inp, f, b, False)
+
+
 def test_token_shifted_causal_lm_loss():
     # (B, SQ) = (3, 100) sequences: shifted targets from the library, losses and
     # gradients against the oracle's own shift of the same targets
