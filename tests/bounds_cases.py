@@ -119,7 +119,7 @@ def main():
         (300, 40000, 9, 3, "bf16", 0.1, 1, True, True),    # two CTAs per SM, in place
         (200, 70001, 4, 2, "bf16", 0.1, 2, True, False),   # one CTA per SM, 192 KiB ring
         (20, 50257, 3, 1, "f32", 0.0, 0, True, False),     # FP32, 192 KiB ring
-        (40, 210000, 8, 7, "bf16", 0.1, 1, True, False),   # pinned shape
+        (40, 210000, 8, 7, "bf16", 0.1, 1, True, False),   # rows split over a cluster pair
     ]
     for c in logits_cases:
         check_logits(*c)

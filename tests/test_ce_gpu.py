@@ -364,11 +364,11 @@ def assert_fused_matches_separate(r, sep_f, sep_dz, target, dtype):
     assert np.linalg.norm(a - b) <= tol * np.linalg.norm(b) + 1e-30
 
 
-@pytest.mark.parametrize("vocab", [5003, 30000, 100000, 210000])
+@pytest.mark.parametrize("vocab", [5003, 30000, 100000, 190000])
 def test_fused_bit_identical_where_threads_match(vocab):
     # Rows the fused call gives the forward kernel's own thread count: up to
-    # 16 KiB (128 threads), 48-64 KiB (8 ring warps = 256 threads), above 112 KiB
-    # (16 ring warps = 512 threads, with and without the pinned area).  Each
+    # 16 KiB (128 threads), 48-64 KiB (8 ring warps = 256 threads), 112-400 KiB
+    # (16 ring warps = 512 threads).  Each
     # thread then takes the same elements in the same order as in ce_forward,
     # and the second pass is ce_backward's arithmetic: every output bit matches.
     n = 300
@@ -396,10 +396,10 @@ FUSED = [
     (25, 98304, "f32", 0.0, 2, True),
     (130, 128256, "bf16", 0.0, False, True),
     # several rows per persistent CTA on the TMA-fed ring kernel (rows above 16 KiB):
-    # one CTA per SM with a 192 KiB ring (bf16 128 KiB rows, f32 196 KiB rows), the
-    # pinned shape for rows above 400 KiB (f32 512 KiB rows), two CTAs per SM with
-    # 96 KiB rings (bf16 78 and 59 KiB rows, f32 78 KiB rows) and four CTAs per SM
-    # with 48 KiB rings (bf16 39 and 23 KiB rows)
+    # one CTA per SM with a 192 KiB ring (bf16 128 KiB rows, f32 196 KiB rows), rows
+    # above 400 KiB split over the two CTAs of a cluster (f32 512 KiB rows), two CTAs
+    # per SM with 96 KiB rings (bf16 78 KiB rows, f32 78 KiB rows), three with 64 KiB
+    # rings (bf16 59 KiB rows) and four with 48 KiB rings (bf16 39 and 23 KiB rows)
     (500, 65536, "bf16", 0.0, 2, True),
     (300, 50257, "f32", 0.1, True, True),
     (400, 131072, "f32", 0.1, True, False),
@@ -434,7 +434,7 @@ def test_fused_matches_oracle_and_separate_path(n, vocab, dtype, eps, red, inpla
 @pytest.mark.parametrize("n,vocab,pad,dtype,eps,red", [
     (200, 50001, 3, "bf16", 0.1, True),   # ring kernel, two CTAs per SM, rows off 16-byte alignment
     (400, 70001, 7, "bf16", 0.0, 2),      # ring kernel, one CTA per SM, rows off 16-byte alignment
-    (160, 205003, 3, "bf16", 0.1, True),  # ring kernel with the row's first 64 KiB pinned, rows off alignment
+    (160, 205003, 3, "bf16", 0.1, True),  # rows split over a cluster pair, rows off alignment
     (150, 9001, 5, "f32", 0.0, False),    # ring kernel, four CTAs per SM
     (300, 129, 1, "bf16", 0.1, 2),        # 128 threads per row
 ])
@@ -466,7 +466,8 @@ def test_fused_ring_bad_and_ignored_rows(vocab, dtype, n):
     """Rows whose target is out of range get one pass through the ring kernel (their
     statistics) and a zero gradient, ignored rows none; the producer and the compute
     warps must agree on that sequence for every later row to be right (for the
-    longest rows also on the pinned area, released after a bad row's one pass)."""
+    longest rows also the two CTAs of a cluster pair, which exchange the partials
+    of every row that is not ignored, bad rows included)."""
     seed = 11 + vocab
     z = wk.normal_matrix(seed, wk.TID_LOGITS, n, vocab, 3.0, dtype == "bf16")
     target = wk.uniform_targets(seed, n, vocab, 0.1)

@@ -123,6 +123,22 @@ __device__ __forceinline__ void row_zero(T* q, const RowSplit<T>& sp, int64_t vo
         if (elem_ok(j, vocab, st)) E::store1(q + j, 0.f);
 }
 
+// Writes zeros over one CTA's share of a row: 16-byte vectors [v0, v1) of the
+// row's interior, with the head elements before it (``head``) and the tail
+// elements after it (``tail``).
+template <int NT, typename T>
+__device__ __forceinline__ void part_zero(T* q, const RowSplit<T>& sp, int64_t vocab, int64_t v0, int64_t v1,
+                                          bool head, bool tail, int* st) {
+    using E = Elem<T>;
+    if (head && threadIdx.x < sp.head && elem_ok(threadIdx.x, vocab, st)) E::store1(q + threadIdx.x, 0.f);
+    uint4* qv = reinterpret_cast<uint4*>(q + sp.head);
+    for (int64_t i = v0 + threadIdx.x; i < v1; i += NT)
+        if (vec_ok(sp, i, vocab, qv + i, st)) qv[i] = make_uint4(0, 0, 0, 0);
+    if (tail)
+        for (int64_t j = sp.tail0 + threadIdx.x; j < vocab; j += NT)
+            if (elem_ok(j, vocab, st)) E::store1(q + j, 0.f);
+}
+
 // ---------------------------------------------------------------------------
 // online softmax accumulator: s = sum exp(z - m) over the values seen
 // ---------------------------------------------------------------------------
@@ -716,20 +732,16 @@ __device__ __forceinline__ void compute_merge(OnlineLse& a, float* sm_m, float* 
 }
 
 // NW compute warps, each thread taking PER 16-byte vectors of every full
-// chunk; RING_KB KiB of shared memory in equal chunks, and PIN_KB KiB more that
-// keep the first chunks of the current row for its second pass.
-template <int NW, int PER, int RING_KB, int PIN_KB = 0>
+// chunk; RING_KB KiB of shared memory in equal chunks.
+template <int NW, int PER, int RING_KB>
 struct RingCfg {
     static constexpr int kThreads = NW * 32;                        // compute threads
     static constexpr uint32_t kChunk = uint32_t(kThreads) * PER * 16;  // bytes per ring slot
     static constexpr int kSlots = int(uint32_t(RING_KB) * 1024 / kChunk);
-    static constexpr int kPins = int(uint32_t(PIN_KB) * 1024 / kChunk);  // chunks kept for the second pass
-    static constexpr size_t kSmemBytes =
-        size_t(kSlots + kPins) * kChunk + (2 * kSlots + 2) * 8 + (3 * 32 + 2) * 4;
+    // ring, full/empty barriers per slot, merge scratch, lse and abort flag
+    static constexpr size_t kSmemBytes = size_t(kSlots) * kChunk + (2 * kSlots) * 8 + (3 * 32 + 2) * 4;
     static_assert(kSlots >= 2 && kSlots <= 16, "ring depth");
 };
-
-__device__ __forceinline__ uint64_t min_u64(uint64_t a, uint64_t b) { return a < b ? a : b; }
 
 // Bounded wait that ignores the abort flag (draining copies still in flight:
 // they complete on their own, so the long drain limit is never reached in
@@ -755,41 +767,30 @@ __device__ __forceinline__ bool ring_drain_wait(uint64_t* bar, uint32_t parity) 
 // first 16-byte boundary and after the last are read directly.  With kHint the
 // first pass's copies ask L2 to keep the row's lines (evict_last) and the second
 // pass's to drop them first (evict_first), so the next row's first-pass reads do
-// not push out lines the second pass still needs.  With PIN_KB > 0 the first
-// chunks of each row are copied once into a separate pinned area instead of the
-// ring and stay there until the second pass has read them, so the second pass
-// reads that much of the row from shared memory and each row holds less of L2
-// (it pays for rows of some 400 KiB and more, whose lines otherwise start to
-// leave L2 before their second read); the pinned area is released as soon as
-// the second pass has used it, and the next row's first chunks are copied in
-// while the rest of the row goes through the ring.
+// not push out lines the second pass still needs.
 // Every wait is bounded (``timeout_ns``): on timeout the CTA sets its abort
 // flag, every role stops waiting, the producer waits for the copies it issued,
 // and VCE_DEVSTATUS_TIMEOUT is reported (the outputs are then undefined).
 // ``hold`` (failure-detection self-test only) makes the producer issue no copy,
 // so the compute warps' first wait runs out with nothing in flight.
-template <int NW, int PER, int RING_KB, int MINB, bool kHint, typename T, bool kSmooth, int PIN_KB = 0>
+template <int NW, int PER, int RING_KB, int MINB, bool kHint, typename T, bool kSmooth>
 __global__ void __launch_bounds__(NW * 32 + 32, MINB)
 ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, const int64_t* __restrict__ target,
               float eps, int64_t ignore_idx, const int64_t* __restrict__ n_valid,
               const float* __restrict__ grad_output, int reduce_loss, float* __restrict__ loss_rows,
               float2* __restrict__ stats, T* dlogits, int* dev_status, uint64_t timeout_ns, int hold) {
     using E = Elem<T>;
-    using C = RingCfg<NW, PER, RING_KB, PIN_KB>;
+    using C = RingCfg<NW, PER, RING_KB>;
     using namespace sm100;
     constexpr int V = E::kVec;
     constexpr int NT = C::kThreads;
     constexpr uint32_t CH = C::kChunk;
     constexpr int S = C::kSlots;
-    constexpr int P = C::kPins;
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t* ring = smem;
-    uint8_t* pin = smem + size_t(S) * CH;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(S + P) * CH);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(S) * CH);
     uint64_t* empty = full + S;
-    uint64_t* pin_full = empty + S;
-    uint64_t* pin_empty = pin_full + 1;
-    float* sm_m = reinterpret_cast<float*>(pin_empty + 1);
+    float* sm_m = reinterpret_cast<float*>(empty + S);
     float* sm_s = sm_m + 32;
     float* sm_sum = sm_s + 32;
     float* sm_lse = sm_sum + 32;
@@ -801,8 +802,6 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], NW);
         }
-        mbar_init(pin_full, 1);
-        mbar_init(pin_empty, NW);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -811,7 +810,7 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
     if (tid >= NT) {
         // ---------------- producer ----------------
         if (tid != NT) return;
-        uint32_t slot = 0, ph = 0, issued = 0, pin_ph = 0, pin_issued = 0;
+        uint32_t slot = 0, ph = 0, issued = 0;
         bool ok = true;
         const uint64_t keep = kHint ? l2_policy_evict_last() : 0, drop = kHint ? l2_policy_evict_first() : 0;
         // bounds-checking build: a copy of ``bytes`` from offset ``off`` of a row's
@@ -834,33 +833,8 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
             const RowSplit<T> sp(p, vocab);
             const uint64_t total = uint64_t(sp.nvec) * 16;
             const uint8_t* src = reinterpret_cast<const uint8_t*>(p + sp.head);
-            const uint64_t nch = (total + CH - 1) / CH;
-            const uint64_t np = min_u64(nch, uint64_t(P));
-            if (np > 0) {
-                // the row's first np chunks go to the pinned area, kept for the second pass
-                if (!mbar_wait(pin_empty, pin_ph ^ 1, abort_flag, timeout_ns)) {
-                    ok = false;
-                    break;
-                }
-                const uint64_t pbytes = total < np * CH ? total : np * CH;
-                bool pin_ok = true;
-                for (uint64_t k = 0; k < np; ++k) {
-                    const uint32_t bytes = uint32_t(total - k * CH < CH ? total - k * CH : CH);
-                    pin_ok = pin_ok && copy_ok(src, total, k * CH, bytes, pin + k * CH, pin + size_t(P) * CH);
-                }
-                mbar_arrive_expect_tx(pin_full, pin_ok ? uint32_t(pbytes) : 0u);
-                for (uint64_t k = 0; k < np && pin_ok; ++k) {
-                    const uint32_t bytes = uint32_t(total - k * CH < CH ? total - k * CH : CH);
-                    if (kHint)
-                        bulk_load_shared_hint(smem_u32(pin + k * CH), src + k * CH, bytes, smem_u32(pin_full), drop);
-                    else
-                        bulk_load_shared(smem_u32(pin + k * CH), src + k * CH, bytes, smem_u32(pin_full));
-                }
-                pin_ph ^= 1;
-                ++pin_issued;
-            }
             for (int pass = 0; pass < (bad ? 1 : 2) && ok; ++pass) {
-                for (uint64_t off = np * CH; off < total; off += CH) {
+                for (uint64_t off = 0; off < total; off += CH) {
                     if (!mbar_wait(&empty[slot], ph ^ 1, abort_flag, timeout_ns)) {
                         ok = false;
                         break;
@@ -889,7 +863,6 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
             const uint32_t last = i + ((issued - 1 - i) / S) * S;
             ring_drain_wait(&full[i], (last / S) & 1);
         }
-        if (pin_issued > 0) ring_drain_wait(pin_full, (pin_issued - 1) & 1);
         if (!ok || *abort_flag) report(dev_status, VCE_DEVSTATUS_TIMEOUT);
         return;
     }
@@ -904,7 +877,7 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
     // still never read, and every value enters the arithmetic in the same
     // order as before (the head first, the tail last).
     const int lane = tid & 31;
-    uint32_t slot = 0, ph = 0, pin_ph = 0;
+    uint32_t slot = 0, ph = 0;
     bool ok = true;
     // wait for the next chunk; false once this CTA has given up
     auto take = [&]() -> bool {
@@ -960,8 +933,6 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
         }
         const bool bad = y < 0 || y >= vocab;
         const uint64_t total = uint64_t(sp.nvec) * 16;
-        const uint64_t nch = (total + CH - 1) / CH;
-        const uint64_t np = min_u64(nch, uint64_t(P));
 
         // pass 1: online (max, sum exp) and sum of logits
         OnlineLse acc;
@@ -969,21 +940,7 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
             float v[1] = {cur.zh};
             acc.push<1, kSmooth>(v);
         }
-        if (np > 0) {
-            if (ok && !mbar_wait(pin_full, pin_ph, abort_flag, timeout_ns)) ok = false;
-            if (ok) {
-                for (uint64_t k = 0; k < np; ++k) {
-                    const uint4* src = reinterpret_cast<const uint4*>(pin + k * CH);
-                    const uint32_t nv = uint32_t(total - k * CH < CH ? total - k * CH : CH) / 16;
-                    for (uint32_t j = tid; j < nv; j += NT) {
-                        float v[V];
-                        E::unpack(src[j], v);
-                        acc.push<V, kSmooth>(v);
-                    }
-                }
-            }
-        }
-        for (uint64_t off = np * CH; off < total; off += CH) {
+        for (uint64_t off = 0; off < total; off += CH) {
             if (take()) {
                 const uint4* src = reinterpret_cast<const uint4*>(ring + size_t(slot) * CH);
                 if (total - off >= CH) {
@@ -1030,15 +987,7 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
         // the next row's target has arrived during the first pass: fetch its
         // other scalars now, to arrive during this row's second pass
         const Scalars nxt = ny != ignore_idx ? fetch(nrow, ny) : Scalars();
-        auto release_pin = [&]() {
-            if (np > 0) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(pin_empty);
-                pin_ph ^= 1;
-            }
-        };
         if (bad) {
-            release_pin();
             row_zero<NT, T>(q, sp, vocab, dev_status);
             cur = nxt;
             y = ny;
@@ -1070,16 +1019,7 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
             }
             if (vec_ok(sp, i, vocab, qv + i, dev_status)) __stcs(qv + i, E::pack(v));
         };
-        if (np > 0 && ok) {
-            for (uint64_t k = 0; k < np; ++k) {
-                const uint4* src = reinterpret_cast<const uint4*>(pin + k * CH);
-                const uint32_t nv = uint32_t(total - k * CH < CH ? total - k * CH : CH) / 16;
-                const int64_t i0 = int64_t(k * CH / 16);
-                for (uint32_t j = tid; j < nv; j += NT) gradv(src[j], i0 + j);
-            }
-        }
-        release_pin();
-        for (uint64_t off = np * CH; off < total; off += CH) {
+        for (uint64_t off = 0; off < total; off += CH) {
             if (take()) {
                 const uint4* src = reinterpret_cast<const uint4*>(ring + size_t(slot) * CH);
                 const int64_t i0 = int64_t(off / 16);
@@ -1105,14 +1045,352 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
     if (!ok) report(dev_status, VCE_DEVSTATUS_TIMEOUT);
 }
 
-template <typename T, int NW, int PER, int RING_KB, int MINB, bool kHint, int PIN_KB = 0>
+// Rows whose two passes would keep too much of L2 busy when one SM takes the
+// whole row (above 256 KiB: 152 rows in flight hold 40-80 MB of lines between
+// their first and second reads, and the second pass starts to miss): the two
+// CTAs of a cluster (two SMs) split every row they take.  Rank 0 owns the
+// first half of the row's interior chunks and the head elements before it,
+// rank 1 the rest and the tail elements, so each SM keeps only half a row in
+// L2 between the passes.  Each CTA runs the ring kernel's producer and compute
+// warps over its half.  After the first pass each CTA merges its own partial
+// (max, sum of exp, sum of logits), sends it to the peer's shared memory
+// (st.shared::cluster, then a release-arrive on the peer's mbarrier), waits
+// for the peer's (bounded, acquire at cluster scope) and merges the two in
+// rank order, so both CTAs hold the same lse; rank 0 writes the loss and the
+// statistics.  The exchange uses two slots by row parity: a CTA writes slot
+// b for row k only after it received the peer's row k-1 partial, which the
+// peer sent after reading slot b for row k-2.  Every thread of both CTAs meets
+// at a cluster barrier before exiting, so no CTA leaves while its peer may
+// still write into its shared memory.  Waits are bounded as in the ring
+// kernel; ``hold`` (self-test) stops the producers' copies.
+template <int NW, int PER, int RING_KB, bool kHint, typename T, bool kSmooth>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NW * 32 + 32, 1)
+ce_fused_ring_pair(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride,
+                   const int64_t* __restrict__ target, float eps, int64_t ignore_idx,
+                   const int64_t* __restrict__ n_valid, const float* __restrict__ grad_output, int reduce_loss,
+                   float* __restrict__ loss_rows, float2* __restrict__ stats, T* dlogits, int* dev_status,
+                   uint64_t timeout_ns, int hold) {
+    using E = Elem<T>;
+    using C = RingCfg<NW, PER, RING_KB>;
+    using namespace sm100;
+    constexpr int V = E::kVec;
+    constexpr int NT = C::kThreads;
+    constexpr uint32_t CH = C::kChunk;
+    constexpr int S = C::kSlots;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t* ring = smem;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(S) * CH);
+    uint64_t* empty = full + S;
+    uint64_t* xbar = empty + S;                        // [2] the peer's partial has arrived (by row parity)
+    float* xval = reinterpret_cast<float*>(xbar + 2);  // [2][4] the peer's (max, sum exp, sum z)
+    float* sm_m = xval + 8;
+    float* sm_s = sm_m + 32;
+    float* sm_sum = sm_s + 32;
+    float* sm_lse = sm_sum + 32;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm_lse + 1);
+    const int tid = threadIdx.x;
+    const uint32_t rank = cluster_ctarank();
+    const int64_t cid = blockIdx.x / 2, ncl = gridDim.x / 2;
+
+    if (tid == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], NW);
+        }
+        mbar_init(&xbar[0], 1);
+        mbar_init(&xbar[1], 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    cluster_sync();  // both CTAs' exchange barriers exist before either arrives on the other's
+
+    // this CTA's share [lo, hi) of a row's 16-byte interior of ``total`` bytes
+    auto share = [&](uint64_t total, uint64_t& lo, uint64_t& hi) {
+        const uint64_t nch = (total + CH - 1) / CH, half = (nch + 1) / 2 * CH;
+        const uint64_t mid = half < total ? half : total;
+        lo = rank == 0 ? 0 : mid;
+        hi = rank == 0 ? mid : total;
+    };
+
+    if (tid >= NT) {
+        if (tid == NT) {
+            // ---------------- producer (this CTA's share of every row) ----------------
+            uint32_t slot = 0, ph = 0, issued = 0;
+            bool ok = true;
+            const uint64_t keep = kHint ? l2_policy_evict_last() : 0, drop = kHint ? l2_policy_evict_first() : 0;
+            auto copy_ok = [&](const uint8_t* src, uint64_t off, uint32_t bytes, uint64_t hi, const uint8_t* dst) {
+                return VCE_BOUNDS(aligned16(src + off) && aligned16(dst) && bytes > 0 && bytes % 16 == 0 &&
+                                      off + bytes <= hi && dst + bytes <= ring + size_t(S) * CH,
+                                  dev_status);
+            };
+            int64_t y_next = cid < n_rows ? target[cid] : ignore_idx;
+            for (int64_t row = cid; row < n_rows && ok && !hold; row += ncl) {
+                const int64_t y = y_next;
+                y_next = row + ncl < n_rows ? target[row + ncl] : ignore_idx;
+                if (y == ignore_idx) continue;
+                const bool bad = y < 0 || y >= vocab;
+                const T* p = logits + row * stride;
+                const RowSplit<T> sp(p, vocab);
+                uint64_t lo, hi;
+                share(uint64_t(sp.nvec) * 16, lo, hi);
+                const uint8_t* src = reinterpret_cast<const uint8_t*>(p + sp.head);
+                for (int pass = 0; pass < (bad ? 1 : 2) && ok; ++pass) {
+                    for (uint64_t off = lo; off < hi; off += CH) {
+                        if (!mbar_wait(&empty[slot], ph ^ 1, abort_flag, timeout_ns)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t bytes = uint32_t(hi - off < CH ? hi - off : CH);
+                        uint8_t* dst = ring + size_t(slot) * CH;
+                        const bool cok = copy_ok(src, off, bytes, hi, dst);
+                        mbar_arrive_expect_tx(&full[slot], cok ? bytes : 0u);
+                        if (cok && kHint)
+                            bulk_load_shared_hint(smem_u32(dst), src + off, bytes, smem_u32(&full[slot]),
+                                                  pass == 0 ? keep : drop);
+                        else if (cok)
+                            bulk_load_shared(smem_u32(dst), src + off, bytes, smem_u32(&full[slot]));
+                        ++issued;
+                        if (++slot == uint32_t(S)) {
+                            slot = 0;
+                            ph ^= 1;
+                        }
+                    }
+                }
+            }
+            for (uint32_t i = 0; i < uint32_t(S) && i < issued; ++i) {
+                const uint32_t last = i + ((issued - 1 - i) / S) * S;
+                ring_drain_wait(&full[i], (last / S) & 1);
+            }
+            if (!ok || *abort_flag) report(dev_status, VCE_DEVSTATUS_TIMEOUT);
+        }
+    } else {
+        // ---------------- compute warps (this CTA's share of every row) ----------------
+        const int lane = tid & 31;
+        uint32_t slot = 0, ph = 0, xk = 0;  // xk: rows whose partials were exchanged so far
+        bool ok = true;
+        auto take = [&]() -> bool {
+            if (ok && !mbar_wait(&full[slot], ph, abort_flag, timeout_ns)) ok = false;
+            return ok;
+        };
+        auto release = [&]() {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+            if (++slot == uint32_t(S)) {
+                slot = 0;
+                ph ^= 1;
+            }
+        };
+        const bool g_rows = reduce_loss == VCE_REDUCE_NONE;
+        const float g_all = g_rows ? 0.f : upstream_grad(reduce_loss, grad_output, n_valid, 0);
+        struct Scalars {
+            float zh = 0.f, zt = 0.f, zy = 0.f, g = 0.f;
+        };
+        // the next row's scalars, fetched a row ahead as in the ring kernel: rank 0
+        // owns the head elements and the loss (target logit), rank 1 the tail
+        auto fetch = [&](int64_t r, int64_t yr) {
+            Scalars sc;
+            const T* pr = logits + r * stride;
+            const RowSplit<T> spr(pr, vocab);
+            if (rank == 0 && tid < spr.head && elem_ok(tid, vocab, dev_status)) sc.zh = E::load1(pr + tid);
+            if (rank == 1 && spr.tail0 + tid < vocab && elem_ok(spr.tail0 + tid, vocab, dev_status))
+                sc.zt = E::load1(pr + spr.tail0 + tid);
+            if (rank == 0 && tid == 0 && yr >= 0 && yr < vocab) sc.zy = E::load1(pr + yr);
+            if (g_rows) sc.g = grad_output[r];
+            return sc;
+        };
+        int64_t y = 0;
+        Scalars cur;
+        if (cid < n_rows) {
+            y = target[cid];
+            if (y != ignore_idx) cur = fetch(cid, y);
+        }
+        for (int64_t row = cid; row < n_rows; row += ncl) {
+            const int64_t nrow = row + ncl;
+            const int64_t ny = nrow < n_rows ? target[nrow] : ignore_idx;
+            const T* p = logits + row * stride;
+            T* q = dlogits + row * stride;
+            const RowSplit<T> sp(p, vocab);
+            uint64_t lo, hi;
+            share(uint64_t(sp.nvec) * 16, lo, hi);
+            if (y == ignore_idx) {
+                if (rank == 0 && tid == 0) {
+                    loss_rows[row] = 0.f;
+                    stats[row] = make_float2(0.f, 0.f);
+                }
+                part_zero<NT, T>(q, sp, vocab, int64_t(lo / 16), int64_t(hi / 16), rank == 0, rank == 1, dev_status);
+                cur = ny != ignore_idx ? fetch(nrow, ny) : Scalars();
+                y = ny;
+                continue;
+            }
+            const bool bad = y < 0 || y >= vocab;
+
+            // pass 1 over this CTA's share
+            OnlineLse acc;
+            if (rank == 0 && tid < sp.head) {
+                float v[1] = {cur.zh};
+                acc.push<1, kSmooth>(v);
+            }
+            for (uint64_t off = lo; off < hi; off += CH) {
+                if (take()) {
+                    const uint4* src = reinterpret_cast<const uint4*>(ring + size_t(slot) * CH);
+                    if (hi - off >= CH) {
+                        uint4 raw[PER];
+#pragma unroll
+                        for (int u = 0; u < PER; ++u) raw[u] = src[tid + u * NT];
+#pragma unroll
+                        for (int u = 0; u < PER; ++u) {
+                            float v[V];
+                            E::unpack(raw[u], v);
+                            acc.push<V, kSmooth>(v);
+                        }
+                    } else {
+                        const uint32_t nv = uint32_t(hi - off) / 16;
+                        for (uint32_t j = tid; j < nv; j += NT) {
+                            float v[V];
+                            E::unpack(src[j], v);
+                            acc.push<V, kSmooth>(v);
+                        }
+                    }
+                }
+                release();
+            }
+            if (rank == 1 && sp.tail0 + tid < vocab) {
+                float v[1] = {cur.zt};
+                acc.push<1, kSmooth>(v);
+            }
+            compute_merge<NT, kSmooth>(acc, sm_m, sm_s, sm_sum);  // thread 0: this CTA's partial
+            if (tid == 0) {
+                // exchange the partials with the peer CTA, then merge them in rank order
+                const uint32_t b = xk & 1u;
+                const uint32_t peer = rank ^ 1u;
+                const uint32_t pv = mapa_shared(smem_u32(&xval[b * 4]), peer);
+                st_shared_cluster(pv, __float_as_int(acc.m));
+                st_shared_cluster(pv + 4, __float_as_int(acc.s));
+                st_shared_cluster(pv + 8, __float_as_int(acc.sum));
+                mbar_arrive_cluster(mapa_shared(smem_u32(&xbar[b]), peer));
+                if (ok && !mbar_wait<true>(&xbar[b], (xk >> 1) & 1u, abort_flag, timeout_ns)) ok = false;
+                OnlineLse other;
+                other.m = xval[b * 4];
+                other.s = xval[b * 4 + 1];
+                other.sum = xval[b * 4 + 2];
+                OnlineLse t = rank == 0 ? acc : other;
+                const OnlineLse& u = rank == 0 ? other : acc;
+                t.merge(u.m, u.s, u.sum);
+                const float lse = t.m + logf(t.s);
+                if (rank == 0) {
+                    float loss;
+                    if (!bad) {
+                        loss = lse - cur.zy;
+                        if (kSmooth) loss = (1.f - eps) * loss + eps * (lse - t.sum / float(vocab));
+                    } else {
+                        loss = __int_as_float(0x7fc00000);
+                        report(dev_status, VCE_DEVSTATUS_BAD_TARGET);
+                    }
+                    loss_rows[row] = loss;
+                    stats[row] = make_float2(t.m, lse);
+                }
+                *sm_lse = lse;
+            }
+            ++xk;
+            compute_sync<NT>();
+            const Scalars nxt = ny != ignore_idx ? fetch(nrow, ny) : Scalars();
+            if (bad) {
+                part_zero<NT, T>(q, sp, vocab, int64_t(lo / 16), int64_t(hi / 16), rank == 0, rank == 1, dev_status);
+                cur = nxt;
+                y = ny;
+                continue;
+            }
+
+            // pass 2 over this CTA's share: dlogits = g (softmax - (1 - eps) onehot - eps / V)
+            const float g = g_rows ? cur.g : g_all;
+            const Exp2Offset eo = exp2_offset(*sm_lse);
+            const float negl = eo.neg;
+            const float gp = g * eo.fix;
+            const float bsh = g * eps / float(vocab);
+            const float c = g * (1.f - eps);
+            auto grad1 = [&](int64_t j, float z) {
+                float d = fmaf(gp, ex2f(fmaf(z, kLog2e, negl)), -bsh);
+                if (j == y) d -= c;
+                if (elem_ok(j, vocab, dev_status)) E::store1(q + j, d);
+            };
+            if (rank == 0 && tid < sp.head) grad1(tid, cur.zh);
+            uint4* qv = reinterpret_cast<uint4*>(q + sp.head);
+            auto gradv = [&](const uint4& raw, int64_t i) {
+                float v[V];
+                E::unpack(raw, v);
+                grad_lanes<V>(v, gp, negl, bsh);
+                const int64_t base = sp.head + i * V;
+                if (uint64_t(y - base) < uint64_t(V)) {
+#pragma unroll
+                    for (int k = 0; k < V; ++k) v[k] -= (base + k == y) ? c : 0.f;
+                }
+                if (vec_ok(sp, i, vocab, qv + i, dev_status)) __stcs(qv + i, E::pack(v));
+            };
+            for (uint64_t off = lo; off < hi; off += CH) {
+                if (take()) {
+                    const uint4* src = reinterpret_cast<const uint4*>(ring + size_t(slot) * CH);
+                    const int64_t i0 = int64_t(off / 16);
+                    if (hi - off >= CH) {
+                        uint4 raw[PER];
+#pragma unroll
+                        for (int u = 0; u < PER; ++u) raw[u] = src[tid + u * NT];
+#pragma unroll
+                        for (int u = 0; u < PER; ++u) gradv(raw[u], i0 + tid + u * NT);
+                    } else {
+                        const uint32_t nv = uint32_t(hi - off) / 16;
+                        for (uint32_t j = tid; j < nv; j += NT) gradv(src[j], i0 + j);
+                    }
+                }
+                release();
+            }
+            if (rank == 1 && sp.tail0 + tid < vocab) grad1(sp.tail0 + tid, cur.zt);
+            cur = nxt;
+            y = ny;
+        }
+        if (!ok) report(dev_status, VCE_DEVSTATUS_TIMEOUT);
+    }
+    __syncwarp();
+    cluster_sync();  // the peer no longer writes into this CTA's shared memory
+}
+
+template <typename T, int NW, int PER, int RING_KB, bool kHint>
+void pair_launch(const void* logits, int64_t n_rows, int64_t vocab, int64_t stride, const int64_t* target,
+                 float eps, int64_t ignore_idx, const int64_t* n_valid, const float* grad_output, int reduce_loss,
+                 float* loss_rows, float* stats, void* dlogits, int* dev_status, cudaStream_t s,
+                 const DeviceInfo& dev, const PipeDiag& diag) {
+    using C = RingCfg<NW, PER, RING_KB>;
+    constexpr size_t kSmem = C::kSmemBytes + 64;  // two exchange barriers and slots beyond the ring's layout
+    auto kern = eps != 0.f ? ce_fused_ring_pair<NW, PER, RING_KB, kHint, T, true>
+                           : ce_fused_ring_pair<NW, PER, RING_KB, kHint, T, false>;
+    static std::mutex mu;
+    static bool raised[2][64] = {};
+    const int k = eps != 0.f ? 1 : 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!raised[k][dev.ordinal]) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmem)) != cudaSuccess)
+                return;  // not launched: the caller's cudaGetLastError() reports the failure
+            raised[k][dev.ordinal] = true;
+        }
+    }
+    const int64_t pairs = dev.num_sms / 2;
+    const int grid = int(2 * (n_rows < pairs ? n_rows : pairs));  // a cluster of two CTAs per row in flight
+    count_launch();
+    kern<<<grid, C::kThreads + 32, kSmem, s>>>(
+        static_cast<const T*>(logits), n_rows, vocab, stride, target, eps, ignore_idx, n_valid, grad_output,
+        reduce_loss, loss_rows, reinterpret_cast<float2*>(stats), static_cast<T*>(dlogits), dev_status,
+        diag.timeout_ns, diag.hold);
+}
+
+template <typename T, int NW, int PER, int RING_KB, int MINB, bool kHint>
 void ring_launch(const void* logits, int64_t n_rows, int64_t vocab, int64_t stride, const int64_t* target,
                  float eps, int64_t ignore_idx, const int64_t* n_valid, const float* grad_output, int reduce_loss,
                  float* loss_rows, float* stats, void* dlogits, int* dev_status, cudaStream_t s,
                  const DeviceInfo& dev, const PipeDiag& diag) {
-    using C = RingCfg<NW, PER, RING_KB, PIN_KB>;
-    auto kern = eps != 0.f ? ce_fused_ring<NW, PER, RING_KB, MINB, kHint, T, true, PIN_KB>
-                           : ce_fused_ring<NW, PER, RING_KB, MINB, kHint, T, false, PIN_KB>;
+    using C = RingCfg<NW, PER, RING_KB>;
+    auto kern = eps != 0.f ? ce_fused_ring<NW, PER, RING_KB, MINB, kHint, T, true>
+                           : ce_fused_ring<NW, PER, RING_KB, MINB, kHint, T, false>;
     // the dynamic shared-memory limit is a per-device attribute of each kernel
     static std::mutex mu;
     static bool raised[2][64] = {};
@@ -1180,15 +1458,19 @@ void fused_dispatch(const void* logits, int64_t n_rows, int64_t vocab, int64_t s
     //     hints that keep the first pass's bytes for the second (BF16 65536:
     //     0.88 [0.86]; 128256: 0.97 [0.86]; 151936: 0.93 [0.79]; FP32 50257: 0.93
     //     [0.80]);
-    //   longer: the same with a 128 KiB ring and the first 64 KiB of each row
-    //     pinned in shared memory for the second pass (BF16 256000: 0.89 against
-    //     0.81 with the 192 KiB ring alone; FP32 128256: 0.89 against 0.83).
+    //   longer: each row split between the two CTAs of a cluster (two SMs),
+    //     each with the 192 KiB ring over its half, so each SM keeps half a row
+    //     in L2 between the passes (BF16 256000: 0.90 against 0.88 for a
+    //     single-CTA ring that pinned the row's first 64 KiB in shared memory;
+    //     FP32 128256: 0.93 against 0.88).  Below 400 KiB the exchange of the
+    //     halves' partials costs more than it saves (BF16 202048: 0.83 against
+    //     0.86; 128256: 0.75 against 0.97).
     // (Measured over 11 ring shapes at 12000-100352: these were the fastest, or
     // within 1%, at every length.)  Where a ring has as many compute threads as
     // the forward kernel has threads per row, every thread takes the same
     // vectors in the same order, so those rows equal ce_forward + ce_backward bit
     // for bit: rows of 48-64 KiB (8 warps, the forward's 256 threads) and rows
-    // above 112 KiB (16 warps, its 512), as the rows up to 16 KiB do.
+    // of 112-400 KiB (16 warps, its 512), as the rows up to 16 KiB do.
     const int64_t nvec = vocab / Elem<T>::kVec;
     const double l2 = double(dev.l2_bytes), row = double(vocab) * double(sizeof(T));
 #define VCE_FUSED_ARGS logits, n_rows, vocab, stride, target, eps, ignore_idx, n_valid, grad_output, reduce_loss, \
@@ -1206,7 +1488,7 @@ void fused_dispatch(const void* logits, int64_t n_rows, int64_t vocab, int64_t s
     } else if (nvec * 16 <= 400 * 1024) {
         ring_launch<T, 16, 4, 192, 1, true>(VCE_FUSED_ARGS, dev, diag);
     } else {
-        ring_launch<T, 16, 4, 128, 1, true, 64>(VCE_FUSED_ARGS, dev, diag);
+        pair_launch<T, 16, 4, 192, true>(VCE_FUSED_ARGS, dev, diag);
     }
 #undef VCE_FUSED_ARGS
 }
