@@ -116,8 +116,11 @@ def main():
         (33, 32001, 7, 1, "bf16", 0.1, 2, False, True),    # 256/512-thread forward, in place
         (40, 5003, 2, 5, "bf16", 0.1, 1, True, False),     # fused, short rows
         (300, 12000, 1, 1, "bf16", 0.0, 0, True, False),   # fused ring: four CTAs per SM
-        (300, 40000, 9, 3, "bf16", 0.1, 1, True, True),    # two CTAs per SM, in place
-        (200, 70001, 4, 2, "bf16", 0.1, 2, True, False),   # one CTA per SM, 192 KiB ring
+        (300, 40000, 9, 3, "bf16", 0.1, 1, True, True),    # two CTAs per SM, 112 KiB rings, in place
+        (100, 52001, 2, 1, "bf16", 0.1, 1, True, False),   # two CTAs per SM, 96 KiB rings
+        (200, 70001, 4, 2, "bf16", 0.1, 2, True, False),   # one CTA per SM, 224 KiB ring
+        (60, 150001, 3, 1, "bf16", 0.0, 0, True, True),    # one CTA per SM, 192 KiB ring, in place
+        (50, 9001, 3, 1, "f32", 0.1, 1, True, False),      # FP32, two CTAs per SM, 96 KiB rings
         (20, 50257, 3, 1, "f32", 0.0, 0, True, False),     # FP32, 192 KiB ring
         (40, 210000, 8, 7, "bf16", 0.1, 1, True, False),   # rows split over a cluster pair
     ]

@@ -364,17 +364,19 @@ def assert_fused_matches_separate(r, sep_f, sep_dz, target, dtype):
     assert np.linalg.norm(a - b) <= tol * np.linalg.norm(b) + 1e-30
 
 
-@pytest.mark.parametrize("vocab", [5003, 30000, 100000, 190000])
-def test_fused_bit_identical_where_threads_match(vocab):
+@pytest.mark.parametrize("vocab,dtype", [(5003, "bf16"), (30000, "bf16"), (100000, "bf16"), (190000, "bf16"),
+                                         (9001, "f32"), (25000, "f32")])
+def test_fused_bit_identical_where_threads_match(vocab, dtype):
     # Rows the fused call gives the forward kernel's own thread count: up to
-    # 16 KiB (128 threads), 48-64 KiB (8 ring warps = 256 threads), 112-400 KiB
-    # (16 ring warps = 512 threads).  Each
-    # thread then takes the same elements in the same order as in ce_forward,
-    # and the second pass is ce_backward's arithmetic: every output bit matches.
+    # 16 KiB (128 threads), BF16 48-64 KiB and FP32 16-56 KiB (8 ring warps = 256
+    # threads), BF16 112-400 KiB and FP32 64-400 KiB (16 ring warps = 512
+    # threads).  Each thread then takes the same elements in the same order as
+    # in ce_forward, and the second pass is ce_backward's arithmetic: every
+    # output bit matches.
     n = 300
-    z = wk.normal_matrix(vocab, wk.TID_LOGITS, n, vocab, 3.0, True)
+    z = wk.normal_matrix(vocab, wk.TID_LOGITS, n, vocab, 3.0, dtype == "bf16")
     target = wk.uniform_targets(vocab, n, vocab, 0.1)
-    logits = to_dev(z, "bf16")
+    logits = to_dev(z, dtype)
     grad = np.ones(1, np.float32)
     f, dz = run_gpu(logits, target, 0.1, True, grad)
     r = run_fused(logits, target, 0.1, True, grad)
@@ -395,16 +397,20 @@ FUSED = [
     (40, 49152, "bf16", 0.1, True, False),
     (25, 98304, "f32", 0.0, 2, True),
     (130, 128256, "bf16", 0.0, False, True),
-    # several rows per persistent CTA on the TMA-fed ring kernel (rows above 16 KiB):
-    # one CTA per SM with a 192 KiB ring (bf16 128 KiB rows, f32 196 KiB rows), rows
-    # above 400 KiB split over the two CTAs of a cluster (f32 512 KiB rows), two CTAs
-    # per SM with 96 KiB rings (bf16 78 KiB rows, f32 78 KiB rows), three with 64 KiB
-    # rings (bf16 59 KiB rows) and four with 48 KiB rings (bf16 39 and 23 KiB rows)
+    # several rows per persistent CTA on every shape of the TMA-fed ring kernel
+    # (rows above 16 KiB): one CTA per SM with a 224 KiB ring (bf16 128 KiB rows) or
+    # a 192 KiB ring (bf16 293 KiB rows, f32 196 and 78 KiB rows), rows above 400 KiB
+    # split over the two CTAs of a cluster (f32 512 KiB rows), two CTAs per SM with
+    # 112 KiB rings (bf16 78 and 59 KiB rows) or 96 KiB rings (bf16 102 KiB rows,
+    # f32 35 KiB rows), and four with 48 KiB rings (bf16 39 and 23 KiB rows)
     (500, 65536, "bf16", 0.0, 2, True),
+    (400, 150001, "bf16", 0.1, True, False),
     (300, 50257, "f32", 0.1, True, True),
     (400, 131072, "f32", 0.1, True, False),
     (700, 40000, "bf16", 0.1, True, True),
     (400, 30000, "bf16", 0.1, True, False),
+    (900, 52000, "bf16", 0.0, 2, False),
+    (600, 9001, "f32", 0.1, True, True),
     (333, 20001, "f32", 0.0, False, False),
     (1000, 20000, "bf16", 0.1, True, False),
     (1500, 12000, "bf16", 0.0, 2, True),
@@ -432,10 +438,13 @@ def test_fused_matches_oracle_and_separate_path(n, vocab, dtype, eps, red, inpla
 
 
 @pytest.mark.parametrize("n,vocab,pad,dtype,eps,red", [
-    (200, 50001, 3, "bf16", 0.1, True),   # ring kernel, two CTAs per SM, rows off 16-byte alignment
-    (400, 70001, 7, "bf16", 0.0, 2),      # ring kernel, one CTA per SM, rows off 16-byte alignment
+    (200, 50001, 3, "bf16", 0.1, True),   # ring kernel, two CTAs per SM, 96 KiB rings, rows off 16-byte alignment
+    (300, 40001, 5, "bf16", 0.1, True),   # ring kernel, two CTAs per SM, 112 KiB rings
+    (400, 70001, 7, "bf16", 0.0, 2),      # ring kernel, one CTA per SM, 224 KiB ring, rows off 16-byte alignment
+    (100, 150001, 3, "bf16", 0.0, False), # ring kernel, one CTA per SM, 192 KiB ring
     (160, 205003, 3, "bf16", 0.1, True),  # rows split over a cluster pair, rows off alignment
-    (150, 9001, 5, "f32", 0.0, False),    # ring kernel, four CTAs per SM
+    (400, 12001, 1, "bf16", 0.0, 2),      # ring kernel, four CTAs per SM
+    (150, 9001, 5, "f32", 0.0, False),    # ring kernel, FP32, two CTAs per SM, 96 KiB rings
     (300, 129, 1, "bf16", 0.1, 2),        # 128 threads per row
 ])
 def test_fused_padded_rows(n, vocab, pad, dtype, eps, red):

@@ -200,31 +200,75 @@ struct OnlineLse {
     }
 };
 
-template <int THREADS, bool kSum>
-__device__ __forceinline__ void block_merge(OnlineLse& a, float* sm_m, float* sm_s, float* sm_sum) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// Warp-wide max of an FP32 value in one instruction (redux.sync, sm_100 family).
+__device__ __forceinline__ float warp_max(float x) {
+    float r;
+    asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+// Combines the 32 lanes' (m, s, sum) of a warp, max first: the warp's max M in
+// one step, each lane's s rescaled to it once (s e^(m - M), 0 for a lane that
+// saw nothing), then the rescaled sums added over a butterfly, so no exponent
+// waits on a shuffle.  Every lane ends with the same result.
+template <bool kSum>
+__device__ __forceinline__ void warp_combine(OnlineLse& a) {
+    const float mx = warp_max(a.m);
+    float s = a.m == -INFINITY ? 0.f : a.s * ex2f((a.m - mx) * kLog2e);
+    float u = a.sum;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, a.m, off);
-        const float s2 = __shfl_xor_sync(0xffffffffu, a.s, off);
-        const float u2 = kSum ? __shfl_xor_sync(0xffffffffu, a.sum, off) : 0.f;
-        a.merge(m2, s2, u2);
+        s += __shfl_xor_sync(0xffffffffu, s, off);
+        if (kSum) u += __shfl_xor_sync(0xffffffffu, u, off);
     }
+    a.m = mx;
+    a.s = s;
+    a.sum = u;
+}
+
+// Combines the partials of a CTA's W warps: each warp combines its lanes, lane
+// 0 of each writes the warp's partial to shared memory, and warp 0 combines
+// those; ``sync`` is the barrier of the participating threads.  Thread 0 holds
+// the result.
+template <int W, bool kSum, typename Sync>
+__device__ __forceinline__ void group_merge(OnlineLse& a, float* sm_m, float* sm_s, float* sm_sum, Sync sync) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    warp_combine<kSum>(a);
     if (lane == 0) { sm_m[warp] = a.m; sm_s[warp] = a.s; sm_sum[warp] = a.sum; }
-    __syncthreads();
+    sync();
     if (warp == 0) {
-        constexpr int W = THREADS / 32;
         OnlineLse b;
         if (lane < W) { b.m = sm_m[lane]; b.s = sm_s[lane]; b.sum = sm_sum[lane]; }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float m2 = __shfl_xor_sync(0xffffffffu, b.m, off);
-            const float s2 = __shfl_xor_sync(0xffffffffu, b.s, off);
-            const float u2 = kSum ? __shfl_xor_sync(0xffffffffu, b.sum, off) : 0.f;
-            b.merge(m2, s2, u2);
-        }
+        warp_combine<kSum>(b);
         a = b;
     }
+}
+
+// As group_merge, but every warp ends with the combined result, so no second
+// barrier is needed to share it.  ``sm`` holds two sets of W partials (6 x 32
+// floats) and ``set`` (0 or 1) picks the one this merge uses: callers alternate
+// it from one merge to the next, so a warp that runs ahead into the next merge
+// writes the other set while slower warps still read this one, and it cannot
+// reach the merge after that before every warp has passed the next merge's
+// barrier.  Each warp combines all W partials with warp 0's operations of
+// group_merge in the same order, so every thread holds the same bits as thread
+// 0 of group_merge over the same partials.
+template <int W, bool kSum, typename Sync>
+__device__ __forceinline__ void group_merge_all(OnlineLse& a, float* sm, uint32_t set, Sync sync) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float* pm = sm + set * 96;
+    warp_combine<kSum>(a);
+    if (lane == 0) { pm[warp] = a.m; pm[32 + warp] = a.s; pm[64 + warp] = a.sum; }
+    sync();
+    OnlineLse b;
+    if (lane < W) { b.m = pm[lane]; b.s = pm[32 + lane]; b.sum = pm[64 + lane]; }
+    warp_combine<kSum>(b);
+    a = b;
+}
+
+template <int THREADS, bool kSum>
+__device__ __forceinline__ void block_merge(OnlineLse& a, float* sm_m, float* sm_s, float* sm_sum) {
+    group_merge<THREADS / 32, kSum>(a, sm_m, sm_s, sm_sum, [] { __syncthreads(); });
 }
 
 // ---------------------------------------------------------------------------
@@ -475,15 +519,16 @@ template <typename T>
 void fwd_dispatch(const void* logits, int64_t n_rows, int64_t vocab, int64_t stride,
                   const int64_t* target, float eps, int64_t ignore_idx, float* loss_rows,
                   float* stats, int* dev_status, cudaStream_t s, int grid) {
-    // One CTA per row, threads by row length (MINB 0 leaves the register budget
-    // to the compiler).  512 threads were measured faster than 1024 for every
-    // row above 4096 vectors (0.24 against 0.31 ms at 16384 x 50257 BF16, 0.56
-    // against 0.58 ms at 16384 x 128256).
+    // One CTA per row, threads by row length.  The 128- and 256-thread kernels
+    // are held to 32 registers, so 2048 threads (16 or 8 rows) fit on an SM; the
+    // 512-thread kernel needs no bound for its 4 rows.  512 threads were measured
+    // faster than 1024 for every row above 4096 vectors (0.24 against 0.31 ms at
+    // 16384 x 50257 BF16, 0.56 against 0.58 ms at 16384 x 128256).
     const int64_t nvec = vocab / Elem<T>::kVec;
     if (nvec <= 1024)
-        fwd_launch<T, 128, 0>(logits, n_rows, vocab, stride, target, eps, ignore_idx, loss_rows, stats, dev_status, s, grid);
+        fwd_launch<T, 128, 16>(logits, n_rows, vocab, stride, target, eps, ignore_idx, loss_rows, stats, dev_status, s, grid);
     else if (nvec <= 4096)
-        fwd_launch<T, 256, 0>(logits, n_rows, vocab, stride, target, eps, ignore_idx, loss_rows, stats, dev_status, s, grid);
+        fwd_launch<T, 256, 8>(logits, n_rows, vocab, stride, target, eps, ignore_idx, loss_rows, stats, dev_status, s, grid);
     else
         fwd_launch<T, 512, 0>(logits, n_rows, vocab, stride, target, eps, ignore_idx, loss_rows, stats, dev_status, s, grid);
 }
@@ -579,8 +624,8 @@ ce_fused_rows(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
     using E = Elem<T>;
     constexpr int V = E::kVec;
     constexpr int U = U2;
-    __shared__ float sm_m[32], sm_s[32], sm_sum[32];
-    __shared__ float sm_lse;
+    __shared__ float sm_part[6 * 32];  // two sets of warp partials (group_merge_all)
+    uint32_t set = 0;
     // the upstream gradient of the mean and sum reductions is the same for every row
     const bool g_rows = reduce_loss == VCE_REDUCE_NONE;
     const float g_all = g_rows ? 0.f : upstream_grad(reduce_loss, grad_output, n_valid, 0);
@@ -605,9 +650,10 @@ ce_fused_rows(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
         const float g_row = g_rows ? grad_output[row] : 0.f;
         OnlineLse acc;
         row_online_lse<THREADS, U1, T, kSmooth>(p, sp, vocab, acc, dev_status);
-        block_merge<THREADS, kSmooth>(acc, sm_m, sm_s, sm_sum);
+        group_merge_all<THREADS / 32, kSmooth>(acc, sm_part, set, [] { __syncthreads(); });
+        set ^= 1u;
+        const float lse = acc.m + logf(acc.s);
         if (threadIdx.x == 0) {
-            const float lse = acc.m + logf(acc.s);
             float loss;
             if (!bad) {
                 loss = lse - zy;
@@ -618,20 +664,17 @@ ce_fused_rows(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
             }
             loss_rows[row] = loss;
             stats[row] = make_float2(acc.m, lse);
-            sm_lse = lse;
         }
         if (kPrefetch && threadIdx.x == 32) {
             const int64_t next = row + gridDim.x;
             if (next < n_rows && target[next] != ignore_idx) prefetch_row_l2(logits + next * stride, vocab);
         }
-        __syncthreads();
         if (bad) {
             row_zero<THREADS, T>(q, sp, vocab, dev_status);
-            __syncthreads();
             continue;
         }
         const float g = g_rows ? g_row : g_all;
-        const Exp2Offset eo = exp2_offset(sm_lse);
+        const Exp2Offset eo = exp2_offset(lse);
         const float negl = eo.neg;
         const float gp = g * eo.fix;
         const float b = g * eps / float(vocab);
@@ -673,7 +716,6 @@ ce_fused_rows(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
         for (; i < sp.nvec; i += THREADS)
             gradv(vec_ok(sp, i, vocab, pv + i, dev_status) ? __ldcs(pv + i) : make_uint4(0, 0, 0, 0), i);
         for (int64_t j = sp.tail0 + threadIdx.x; j < vocab; j += THREADS) grad1(j);
-        __syncthreads();  // shared scratch reused by the next row
     }
 }
 
@@ -720,29 +762,7 @@ __device__ __forceinline__ void compute_sync() {
 // block_merge over the compute threads of the ring kernel
 template <int NT, bool kSum>
 __device__ __forceinline__ void compute_merge(OnlineLse& a, float* sm_m, float* sm_s, float* sm_sum) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, a.m, off);
-        const float s2 = __shfl_xor_sync(0xffffffffu, a.s, off);
-        const float u2 = kSum ? __shfl_xor_sync(0xffffffffu, a.sum, off) : 0.f;
-        a.merge(m2, s2, u2);
-    }
-    if (lane == 0) { sm_m[warp] = a.m; sm_s[warp] = a.s; sm_sum[warp] = a.sum; }
-    compute_sync<NT>();
-    if (warp == 0) {
-        constexpr int W = NT / 32;
-        OnlineLse b;
-        if (lane < W) { b.m = sm_m[lane]; b.s = sm_s[lane]; b.sum = sm_sum[lane]; }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float m2 = __shfl_xor_sync(0xffffffffu, b.m, off);
-            const float s2 = __shfl_xor_sync(0xffffffffu, b.s, off);
-            const float u2 = kSum ? __shfl_xor_sync(0xffffffffu, b.sum, off) : 0.f;
-            b.merge(m2, s2, u2);
-        }
-        a = b;
-    }
+    group_merge<NT / 32, kSum>(a, sm_m, sm_s, sm_sum, [] { compute_sync<NT>(); });
 }
 
 // NW compute warps, each thread taking PER 16-byte vectors of every full
@@ -752,8 +772,9 @@ struct RingCfg {
     static constexpr int kThreads = NW * 32;                        // compute threads
     static constexpr uint32_t kChunk = uint32_t(kThreads) * PER * 16;  // bytes per ring slot
     static constexpr int kSlots = int(uint32_t(RING_KB) * 1024 / kChunk);
-    // ring, full/empty barriers per slot, merge scratch, lse and abort flag
-    static constexpr size_t kSmemBytes = size_t(kSlots) * kChunk + (2 * kSlots) * 8 + (3 * 32 + 2) * 4;
+    // ring, full/empty barriers per slot, two sets of merge partials and the abort
+    // flag (the cluster kernel adds its exchange slots and keeps one set)
+    static constexpr size_t kSmemBytes = size_t(kSlots) * kChunk + (2 * kSlots) * 8 + (6 * 32 + 2) * 4;
     static_assert(kSlots >= 2 && kSlots <= 16, "ring depth");
 };
 
@@ -804,11 +825,8 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
     uint8_t* ring = smem;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(S) * CH);
     uint64_t* empty = full + S;
-    float* sm_m = reinterpret_cast<float*>(empty + S);
-    float* sm_s = sm_m + 32;
-    float* sm_sum = sm_s + 32;
-    float* sm_lse = sm_sum + 32;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm_lse + 1);
+    float* sm_part = reinterpret_cast<float*>(empty + S);  // two sets of warp partials (group_merge_all)
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm_part + 6 * 32);
     const int tid = threadIdx.x;
 
     if (tid == 0) {
@@ -892,6 +910,7 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
     // order as before (the head first, the tail last).
     const int lane = tid & 31;
     uint32_t slot = 0, ph = 0;
+    uint32_t set = 0;  // merge partial set (group_merge_all)
     bool ok = true;
     // wait for the next chunk; false once this CTA has given up
     auto take = [&]() -> bool {
@@ -982,9 +1001,10 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
             float v[1] = {cur.zt};
             acc.push<1, kSmooth>(v);
         }
-        compute_merge<NT, kSmooth>(acc, sm_m, sm_s, sm_sum);
+        group_merge_all<NW, kSmooth>(acc, sm_part, set, [] { compute_sync<NT>(); });
+        set ^= 1u;
+        const float lse = acc.m + logf(acc.s);
         if (tid == 0) {
-            const float lse = acc.m + logf(acc.s);
             float loss;
             if (!bad) {
                 loss = lse - cur.zy;
@@ -995,9 +1015,7 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
             }
             loss_rows[row] = loss;
             stats[row] = make_float2(acc.m, lse);
-            *sm_lse = lse;
         }
-        compute_sync<NT>();
         // the next row's target has arrived during the first pass: fetch its
         // other scalars now, to arrive during this row's second pass
         const Scalars nxt = ny != ignore_idx ? fetch(nrow, ny) : Scalars();
@@ -1010,7 +1028,7 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
 
         // pass 2: dlogits = g (softmax - (1 - eps) onehot - eps / V)
         const float g = g_rows ? cur.g : g_all;
-        const Exp2Offset eo = exp2_offset(*sm_lse);
+        const Exp2Offset eo = exp2_offset(lse);
         const float negl = eo.neg;
         const float gp = g * eo.fix;
         const float b = g * eps / float(vocab);
@@ -1459,19 +1477,26 @@ void fused_dispatch(const void* logits, int64_t n_rows, int64_t vocab, int64_t s
                     cudaStream_t s, const DeviceInfo& dev, const PipeDiag& diag) {
     // Rows up to 1024 vectors (16 KiB): 128 threads per row, 8 CTAs per SM, and
     // the next-row L2 prefetch while two rows per CTA take at most two thirds of
-    // L2.  Longer rows: the TMA-fed ring kernel, shaped by row length.  Measured
-    // at 16384 rows (fraction of the copy peak; in brackets the previous 256-,
-    // 512- and 1024-thread row kernels with next-row prefetch):
-    //   up to 48 KiB: four CTAs per SM, 4 compute warps, 48 KiB rings
-    //     (BF16 V = 12000: 0.71 [0.51]; 20000: 0.82 [0.65]; FP32 6000: 0.76 [0.59]);
-    //   up to 64 KiB: three CTAs per SM, 8 compute warps, 64 KiB rings
-    //     (BF16 32000: 0.87 against 0.85 with two CTAs per SM and 96 KiB rings);
-    //   up to 112 KiB: two CTAs per SM, 8 compute warps, 96 KiB rings
-    //     (BF16 40000: 0.89 [0.80]; 50257: 0.90 [0.80]; FP32 16000: 0.88 [0.85]);
-    //   up to 400 KiB: one CTA per SM, 16 compute warps, a 192 KiB ring and L2
-    //     hints that keep the first pass's bytes for the second (BF16 65536:
-    //     0.88 [0.86]; 128256: 0.97 [0.86]; 151936: 0.93 [0.79]; FP32 50257: 0.93
-    //     [0.80]);
+    // L2.  Longer rows: the TMA-fed ring kernel, shaped by row length and element
+    // size (an FP32 row carries half the arithmetic per byte of a BF16 row, so it
+    // favours fewer, larger CTAs).  Measured at 16384 rows, fraction of the copy
+    // peak:
+    //   BF16 up to 48 KiB: four CTAs per SM, 4 compute warps, 48 KiB rings
+    //     (V = 12000: 0.75; 20000: 0.84; 24000: 0.84);
+    //   BF16 up to 88 KiB: two CTAs per SM, 8 compute warps, 112 KiB rings
+    //     (30000: 0.86; 32000: 0.88; 40000: 0.91; 44000: 0.915);
+    //   BF16 up to 112 KiB: two CTAs per SM, 8 compute warps, 96 KiB rings
+    //     (48000: 0.92; 50257: 0.92; 56000: 0.89; from 90 KiB the 112 KiB
+    //     rings fell behind by 1-2%);
+    //   BF16 up to 240 KiB: one CTA per SM, 16 compute warps, a 224 KiB ring
+    //     and L2 hints that keep the first pass's bytes for the second
+    //     (65536: 0.95; 100352: 0.96; 120000: 0.96; the 192 KiB ring 0.94);
+    //   BF16 up to 400 KiB: the same with a 192 KiB ring (128256: 0.98;
+    //     150000: 0.96; the 224 KiB ring 0.94-0.96);
+    //   FP32 up to 56 KiB: two CTAs per SM, 8 compute warps, 96 KiB rings
+    //     (V = 8000: 0.84; 12000: 0.80);
+    //   FP32 up to 400 KiB: one CTA per SM, 16 compute warps, 192 KiB ring with
+    //     L2 hints (16000: 0.91; 25000: 0.955; 50257: 0.94; 60000: 0.93);
     //   longer: each row split between the two CTAs of a cluster (two SMs),
     //     each with the 192 KiB ring over its half, so each SM keeps half a row
     //     in L2 between the passes (BF16 256000: 0.90 against 0.88 for a
@@ -1479,30 +1504,34 @@ void fused_dispatch(const void* logits, int64_t n_rows, int64_t vocab, int64_t s
     //     FP32 128256: 0.93 against 0.88).  Below 400 KiB the exchange of the
     //     halves' partials costs more than it saves (BF16 202048: 0.83 against
     //     0.86; 128256: 0.75 against 0.97).
-    // (Measured over 11 ring shapes at 12000-100352: these were the fastest, or
-    // within 1%, at every length.)  Where a ring has as many compute threads as
+    // (Over 10 ring shapes of 4-16 compute warps, 8-32 KiB chunks, 48-224 KiB
+    // rings and 1-4 CTAs per SM.)  Where a ring has as many compute threads as
     // the forward kernel has threads per row, every thread takes the same
     // vectors in the same order, so those rows equal ce_forward + ce_backward bit
-    // for bit: rows of 48-64 KiB (8 warps, the forward's 256 threads) and rows
-    // of 112-400 KiB (16 warps, its 512), as the rows up to 16 KiB do.
+    // for bit: BF16 rows of 48-64 KiB and FP32 rows of 16-56 KiB (8 warps, the
+    // forward's 256 threads), and rows of 112-400 KiB BF16 or 64-400 KiB FP32 (16
+    // warps, its 512), as the rows up to 16 KiB do.
     const int64_t nvec = vocab / Elem<T>::kVec;
+    const int64_t bytes = nvec * 16;
     const double l2 = double(dev.l2_bytes), row = double(vocab) * double(sizeof(T));
 #define VCE_FUSED_ARGS logits, n_rows, vocab, stride, target, eps, ignore_idx, n_valid, grad_output, reduce_loss, \
                        loss_rows, stats, dlogits, dev_status, s
+    constexpr int64_t KiB = 1024;
     if (nvec <= 1024) {
         const int grid = fused_grid(n_rows, dev.num_sms, 8);
         if (double(grid) * 2 * row <= l2 * 2.0 / 3.0) fused_launch<T, 128, 8, 4, 2, true>(VCE_FUSED_ARGS, grid);
         else fused_launch<T, 128, 8, 4, 2, false>(VCE_FUSED_ARGS, grid);
-    } else if (nvec * 16 <= 48 * 1024) {
-        ring_launch<T, 4, 4, 48, 4, false>(VCE_FUSED_ARGS, dev, diag);
-    } else if (nvec * 16 <= 64 * 1024) {
-        ring_launch<T, 8, 4, 64, 3, false>(VCE_FUSED_ARGS, dev, diag);
-    } else if (nvec * 16 <= 112 * 1024) {
-        ring_launch<T, 8, 4, 96, 2, false>(VCE_FUSED_ARGS, dev, diag);
-    } else if (nvec * 16 <= 400 * 1024) {
-        ring_launch<T, 16, 4, 192, 1, true>(VCE_FUSED_ARGS, dev, diag);
-    } else {
+    } else if (bytes > 400 * KiB) {
         pair_launch<T, 16, 4, 192, true>(VCE_FUSED_ARGS, dev, diag);
+    } else if constexpr (sizeof(T) == 4) {
+        if (bytes <= 56 * KiB) ring_launch<T, 8, 4, 96, 2, false>(VCE_FUSED_ARGS, dev, diag);
+        else ring_launch<T, 16, 4, 192, 1, true>(VCE_FUSED_ARGS, dev, diag);
+    } else {
+        if (bytes <= 48 * KiB) ring_launch<T, 4, 4, 48, 4, false>(VCE_FUSED_ARGS, dev, diag);
+        else if (bytes <= 88 * KiB) ring_launch<T, 8, 4, 112, 2, false>(VCE_FUSED_ARGS, dev, diag);
+        else if (bytes <= 112 * KiB) ring_launch<T, 8, 4, 96, 2, false>(VCE_FUSED_ARGS, dev, diag);
+        else if (bytes <= 240 * KiB) ring_launch<T, 16, 4, 224, 1, true>(VCE_FUSED_ARGS, dev, diag);
+        else ring_launch<T, 16, 4, 192, 1, true>(VCE_FUSED_ARGS, dev, diag);
     }
 #undef VCE_FUSED_ARGS
 }
