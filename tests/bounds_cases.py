@@ -5,7 +5,7 @@ Every entry point runs on small, ragged and padded inputs that reach each kernel
 shape: the short-row, 128/256/512-thread row kernels, every ring shape of the
 fused kernel (with rows off 16-byte alignment and padding between rows, in
 place and not), the linear form's GEMMs with ragged M/N/K, several vocabulary
-slabs and the 512-wide dX tile, the no-alloc forward and the token shift.  Each
+slabs and the 512-wide dX and dW tiles, the no-alloc forward and the token shift.  Each
 result is checked against the FP64 oracle at the stated tolerances, and the
 device status word must stay 0: no address failed a check.  Exit status 0 when
 everything passes.
@@ -132,6 +132,7 @@ def main():
         (129, 72, 300, 0.1, 1, 0),
         (384, 256, 1800, 0.1, 1, 256),     # several slabs, FP32 dX across them
         (300, 1032, 70000, 0.0, 2, 0),     # 512-wide dX tile, ragged H
+        (8200, 1032, 600, 0.1, 1, 0),      # 512-wide dW tile (8192 tokens or more), ragged M, N and K
     ]
     for c in linear_cases:
         check_linear(*c)

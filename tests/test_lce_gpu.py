@@ -118,6 +118,17 @@ def test_dx_wide_tiles(n, h, v, slab_ids):
     check_full(x, w, y, 0.1, True, np.ones(1, np.float32), max_slab_bytes=n * 2 * slab_ids)
 
 
+@pytest.mark.parametrize("n,h,v,slab_ids", [
+    (8200, 1032, 600, 0),         # 512-wide dW tiles (8192 tokens or more); ragged M, N and K
+    (8192, 1024, 1800, 512),      # several slabs, each with its own wide dW launch
+])
+def test_dw_wide_tiles(n, h, v, slab_ids):
+    x = wk.normal_matrix(37, wk.TID_X, n, h, 1.0, True)
+    w = wk.normal_matrix(37, wk.TID_W, v, h, h ** -0.5, True)
+    y = wk.uniform_targets(37, n, v, 0.05)
+    check_full(x, w, y, 0.1, True, np.ones(1, np.float32), max_slab_bytes=n * 2 * slab_ids)
+
+
 def test_token_wave_boundaries():
     # 4097- and 5000-token shapes (one token past a 4K wave; a two-wave tail)
     for n in (4097, 5000):

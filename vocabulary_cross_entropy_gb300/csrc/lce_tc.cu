@@ -863,6 +863,16 @@ DxPlan dx_plan(int64_t n, int64_t h, int64_t slab, int num_sms) {
     return {256, dx_k_splits(n, h, 256, num_sms)};
 }
 
+// Tile width of the dW GEMM (dW_slab = dZ^T X: M = slab ids, N = hidden, K =
+// tokens).  Each work unit streams a strip of the slab's dZ and one of X over all
+// tokens; with 512-wide tiles the CTA pairs working at one time cover half as
+// many hidden tiles, so each round reads fewer X strips, and the tile's single
+// accumulator leaves its epilogue outside the main loop, which K ranges of
+// kDwWideTokens tokens or more amortise.
+constexpr int64_t kDwWideTokens = 8192;
+
+int dw_tile(int64_t n, int64_t h) { return n >= kDwWideTokens && h >= 1024 ? 512 : 256; }
+
 // dX = sum of the FP32 partials of every K chunk, rounded to BF16 (fixed order).
 __global__ void dx_finalize_kernel(const float* __restrict__ acc, int splits, int64_t split_stride,
                                    int64_t count4, __nv_bfloat16* __restrict__ dx) {
@@ -1032,7 +1042,11 @@ vce_status launch_lce_backward(const void* X, const void* W, int64_t n, int64_t 
         // dW_slab = dZ^T X: M = vs, N = h, K = n (both operands MN-major)
         StoreEpi we{dWb + v0 * h, h, nullptr, 0, 0, 0, vs, h, 1, dev_status};
         if (vce_status st =
-                launch_gemm<StoreEpi, true, true, 256>(tdz_mn, tx_mn, vs, h, n, 0, 1, we, counter, dev_status, s, dev))
+                dw_tile(n, h) == 512
+                    ? launch_gemm<StoreEpi, true, true, 512>(tdz_mn, tx_mn, vs, h, n, 0, 1, we, counter, dev_status, s,
+                                                             dev)
+                    : launch_gemm<StoreEpi, true, true, 256>(tdz_mn, tx_mn, vs, h, n, 0, 1, we, counter, dev_status, s,
+                                                             dev))
             return st;
         // dX (+)= dZ W_slab: M = n, N = h, K = vs (W_slab read MN-major), K cut into plan.splits chunks
         StoreEpi xe{dXb, h, acc, h, split_stride, plan.direct ? 0 : (v0 == 0 ? 1 : 2), n, h, plan.splits, dev_status};
