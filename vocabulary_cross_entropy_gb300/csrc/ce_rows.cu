@@ -514,22 +514,41 @@ ce_backward_rows(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride,
 
 constexpr int kMeanThreads = 1024;
 
+// Adds the compensated pair (h2, l2) to (hi, lo) with TwoSum, so the pair keeps
+// the rounding error of every addition; an infinite or NaN sum propagates alone.
+__device__ __forceinline__ void pair_add(float& hi, float& lo, float h2, float l2) {
+    const float s = hi + h2;
+    if (!isfinite(s)) {
+        hi = s;
+        lo = 0.f;
+        return;
+    }
+    const float bb = s - hi;
+    const float e = (hi - (s - bb)) + (h2 - bb);
+    const float l = lo + l2 + e;
+    hi = s + l;
+    lo = l - (hi - s);
+}
+
 __global__ void __launch_bounds__(kMeanThreads)
 mean_loss_kernel(const float* __restrict__ loss_rows, const int64_t* __restrict__ target,
                  int64_t n, int64_t ignore_idx, int reduce, float* __restrict__ loss_out,
                  int64_t* __restrict__ n_valid) {
-    __shared__ double sm_s[32];
+    __shared__ float sm_h[32], sm_l[32];
     __shared__ long long sm_c[32];
     // Each thread adds its rows eight at a time (a small FP32 tree per batch of
     // loads) into a running FP32 sum with Neumaier compensation (the rounding
     // error each addition dropped is kept and added back), which keeps it within
-    // FP32 rounding of the exact total; only the 1024 per-thread results are
-    // widened to FP64 for the block reduction.  FP64 arithmetic runs at a small
-    // fraction of the FP32 rate on this GPU: converting and adding every row in
-    // FP64 took 14 us for 16384 rows and 585 us for 1M rows.
+    // FP32 rounding of the exact total.  The 1024 per-thread (sum, error) pairs
+    // are then combined in a fixed order by TwoSum additions, which carry the
+    // error along as FP64 additions would, in FP32 arithmetic: FP64 runs at a
+    // small fraction of the FP32 rate on this GPU (an FP64 combine took 8.2 us
+    // per launch at 16384 rows against 6.1 us, and converting and adding every
+    // row in FP64 took 14 us for 16384 rows and 585 us for 1M rows).
     float fs = 0.f, fc = 0.f;
     int ci = 0;  // this thread's count (at most n / 1024 + 8)
-    constexpr int U = 8;  // loads in flight per thread, summed as a small tree
+    constexpr int U = 8;  // loads in flight per thread, summed as a small tree (16 measured
+                          // 4-10 us slower at 65536-131072 rows)
     for (int64_t i0 = threadIdx.x; i0 < n; i0 += int64_t(kMeanThreads) * U) {
         float l[U];
 #pragma unroll
@@ -539,33 +558,50 @@ mean_loss_kernel(const float* __restrict__ loss_rows, const int64_t* __restrict_
             ci += (in && target[i] != ignore_idx) ? 1 : 0;
             l[u] = (in && loss_rows) ? loss_rows[i] : 0.f;
         }
-        const float b = ((l[0] + l[1]) + (l[2] + l[3])) + ((l[4] + l[5]) + (l[6] + l[7]));
-        const float t = fs + b;
+#pragma unroll
+        for (int w = U / 2; w >= 1; w >>= 1)
+#pragma unroll
+            for (int u = 0; u < w; ++u) l[u] = l[2 * u] + l[2 * u + 1];
+        const float bsum = l[0];
+        const float t = fs + bsum;
         if (isfinite(t))  // an infinite or NaN loss propagates through fs alone
-            fc += fabsf(fs) >= fabsf(b) ? (fs - t) + b : (b - t) + fs;
+            fc += fabsf(fs) >= fabsf(bsum) ? (fs - t) + bsum : (bsum - t) + fs;
         fs = t;
     }
-    double s = double(fs) + double(fc);
+    float hi = fs, lo = 0.f;
+    pair_add(hi, lo, fc, 0.f);
     long long c = ci;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
-        s += __shfl_xor_sync(0xffffffffu, s, off);
+        const float h2 = __shfl_xor_sync(0xffffffffu, hi, off), l2 = __shfl_xor_sync(0xffffffffu, lo, off);
+        pair_add(hi, lo, h2, l2);
         c += __shfl_xor_sync(0xffffffffu, c, off);
     }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (lane == 0) { sm_s[warp] = s; sm_c[warp] = c; }
+    if (lane == 0) { sm_h[warp] = hi; sm_l[warp] = lo; sm_c[warp] = c; }
     __syncthreads();
     if (warp == 0) {
-        s = sm_s[lane];
+        hi = sm_h[lane];
+        lo = sm_l[lane];
         c = sm_c[lane];
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
-            s += __shfl_xor_sync(0xffffffffu, s, off);
+            const float h2 = __shfl_xor_sync(0xffffffffu, hi, off), l2 = __shfl_xor_sync(0xffffffffu, lo, off);
+            pair_add(hi, lo, h2, l2);
             c += __shfl_xor_sync(0xffffffffu, c, off);
         }
         if (lane == 0) {
-            // mean: 0/0 = NaN when every row is ignored; sum: the plain total
-            if (loss_out) loss_out[0] = reduce == VCE_REDUCE_SUM ? float(s) : float(s / double(c));
+            // mean: (hi + lo) / N_v with one correction step (0/0 = NaN when every
+            // row is ignored); sum: the plain total
+            float out;
+            if (reduce == VCE_REDUCE_SUM) {
+                out = hi + lo;
+            } else {
+                const float cf = float(c);
+                const float q = __fdiv_rn(hi, cf);
+                out = isfinite(q) ? q + __fdiv_rn(fmaf(-q, cf, hi) + lo, cf) : q;
+            }
+            if (loss_out) loss_out[0] = out;
             if (n_valid) n_valid[0] = c;
         }
     }
