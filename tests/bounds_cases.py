@@ -119,7 +119,8 @@ def main():
         (300, 40000, 9, 3, "bf16", 0.1, 1, True, True),    # two CTAs per SM, 112 KiB rings, in place
         (100, 52001, 2, 1, "bf16", 0.1, 1, True, False),   # two CTAs per SM, 96 KiB rings
         (200, 70001, 4, 2, "bf16", 0.1, 2, True, False),   # one CTA per SM, 224 KiB ring
-        (60, 150001, 3, 1, "bf16", 0.0, 0, True, True),    # one CTA per SM, 192 KiB ring, in place
+        (40, 130001, 5, 3, "bf16", 0.1, 1, True, False),   # one CTA per SM, 192 KiB ring, 4 vectors per thread
+        (60, 150001, 3, 1, "bf16", 0.0, 0, True, True),    # 192 KiB ring, 8 vectors per thread, in place
         (50, 9001, 3, 1, "f32", 0.1, 1, True, False),      # FP32, two CTAs per SM, 96 KiB rings
         (20, 50257, 3, 1, "f32", 0.0, 0, True, False),     # FP32, 192 KiB ring
         (40, 210000, 8, 7, "bf16", 0.1, 1, True, False),   # rows split over a cluster pair

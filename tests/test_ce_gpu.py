@@ -364,8 +364,8 @@ def assert_fused_matches_separate(r, sep_f, sep_dz, target, dtype):
     assert np.linalg.norm(a - b) <= tol * np.linalg.norm(b) + 1e-30
 
 
-@pytest.mark.parametrize("vocab,dtype", [(5003, "bf16"), (30000, "bf16"), (100000, "bf16"), (190000, "bf16"),
-                                         (9001, "f32"), (25000, "f32")])
+@pytest.mark.parametrize("vocab,dtype", [(5003, "bf16"), (30000, "bf16"), (100000, "bf16"), (130001, "bf16"),
+                                         (190000, "bf16"), (9001, "f32"), (25000, "f32")])
 def test_fused_bit_identical_where_threads_match(vocab, dtype):
     # Rows the fused call gives the forward kernel's own thread count: up to
     # 16 KiB (128 threads), BF16 48-64 KiB and FP32 16-56 KiB (8 ring warps = 256

@@ -1612,24 +1612,31 @@ void fused_dispatch(const void* logits, int64_t n_rows, int64_t vocab, int64_t s
     // the next-row L2 prefetch while two rows per CTA take at most two thirds of
     // L2.  Longer rows: the TMA-fed ring kernel, shaped by row length and element
     // size (an FP32 row carries half the arithmetic per byte of a BF16 row, so it
-    // favours fewer, larger CTAs).  Measured at 16384 rows, fraction of the copy
-    // peak:
-    //   BF16 up to 48 KiB: four CTAs per SM, 4 compute warps, 48 KiB rings
-    //     (V = 12000: 0.75; 20000: 0.84; 24000: 0.84);
-    //   BF16 up to 88 KiB: two CTAs per SM, 8 compute warps, 112 KiB rings
-    //     (30000: 0.86; 32000: 0.88; 40000: 0.91; 44000: 0.915);
-    //   BF16 up to 112 KiB: two CTAs per SM, 8 compute warps, 96 KiB rings
-    //     (48000: 0.92; 50257: 0.92; 56000: 0.89; from 90 KiB the 112 KiB
-    //     rings fell behind by 1-2%);
-    //   BF16 up to 240 KiB: one CTA per SM, 16 compute warps, a 224 KiB ring
-    //     and L2 hints that keep the first pass's bytes for the second
-    //     (65536: 0.95; 100352: 0.96; 120000: 0.96; the 192 KiB ring 0.94);
-    //   BF16 up to 400 KiB: the same with a 192 KiB ring (128256: 0.98;
-    //     150000: 0.96; the 224 KiB ring 0.94-0.96);
-    //   FP32 up to 56 KiB: two CTAs per SM, 8 compute warps, 96 KiB rings
-    //     (V = 8000: 0.84; 12000: 0.80);
-    //   FP32 up to 400 KiB: one CTA per SM, 16 compute warps, 192 KiB ring with
-    //     L2 hints (16000: 0.91; 25000: 0.955; 50257: 0.94; 60000: 0.93);
+    // favours fewer, larger CTAs).  Each compute thread takes PER 16-byte vectors
+    // of every chunk: more vectors between two waits on the ring give it more
+    // independent arithmetic to interleave, which the latency-bound short and mid
+    // rows need.  Measured at 16384 rows, fraction of the copy peak (in brackets
+    // the same ring with 4 vectors per thread):
+    //   BF16 up to 44 KiB: four CTAs per SM, 4 compute warps x 8 vectors, 48 KiB
+    //     rings of three chunks (V = 10000: 0.72; 13000: 0.79; 16000: 0.85;
+    //     22500: 0.87 [0.70-0.87]);
+    //   BF16 up to 88 KiB: two CTAs per SM, 8 compute warps x 7 vectors, 112 KiB
+    //     rings of four 28 KiB chunks (25000: 0.86; 32000: 0.90; 35000: 0.90;
+    //     38000: 0.92; 44500: 0.92 [0.82-0.92]);
+    //   BF16 up to 112 KiB: two CTAs per SM, 8 compute warps x 8 vectors, 96 KiB
+    //     rings of three chunks (47000: 0.93; 50257: 0.92; 55000: 0.925
+    //     [0.91-0.93]);
+    //   BF16 up to 240 KiB: one CTA per SM, 16 compute warps x 4 vectors, a 224
+    //     KiB ring and L2 hints that keep the first pass's bytes for the second
+    //     (65536: 0.95; 100352: 0.97; 120000: 0.96; the 192 KiB ring 0.94);
+    //   BF16 up to 288 KiB: the same with a 192 KiB ring (128256: 0.97-0.98;
+    //     140000: 0.96; 8 vectors per thread 0.94-0.97);
+    //   BF16 up to 400 KiB: the 192 KiB ring with 8 vectors per thread, in three
+    //     64 KiB chunks (160000: 0.95; 180000: 0.94; 195000: 0.91 [0.87-0.92]);
+    //   FP32 up to 56 KiB: two CTAs per SM, 8 compute warps x 8 vectors, 96 KiB
+    //     rings (V = 7000: 0.85; 10000: 0.90; 13500: 0.87 [0.81-0.87]);
+    //   FP32 up to 400 KiB: one CTA per SM, 16 compute warps x 4 vectors, the 192
+    //     KiB ring with L2 hints (16000: 0.91; 25000: 0.955; 50257: 0.94);
     //   longer: each row split between the two CTAs of a cluster (two SMs),
     //     each with the 192 KiB ring over its half, so each SM keeps half a row
     //     in L2 between the passes (BF16 256000: 0.90 against 0.88 for a
@@ -1637,13 +1644,14 @@ void fused_dispatch(const void* logits, int64_t n_rows, int64_t vocab, int64_t s
     //     FP32 128256: 0.93 against 0.88).  Below 400 KiB the exchange of the
     //     halves' partials costs more than it saves (BF16 202048: 0.83 against
     //     0.86; 128256: 0.75 against 0.97).
-    // (Over 10 ring shapes of 4-16 compute warps, 8-32 KiB chunks, 48-224 KiB
-    // rings and 1-4 CTAs per SM.)  Where a ring has as many compute threads as
-    // the forward kernel has threads per row, every thread takes the same
-    // vectors in the same order, so those rows equal ce_forward + ce_backward bit
-    // for bit: BF16 rows of 48-64 KiB and FP32 rows of 16-56 KiB (8 warps, the
-    // forward's 256 threads), and rows of 112-400 KiB BF16 or 64-400 KiB FP32 (16
-    // warps, its 512), as the rows up to 16 KiB do.
+    // (Over ring shapes of 4-16 compute warps, 2-8 vectors per thread, 8-64 KiB
+    // chunks, 48-224 KiB rings and 1-4 CTAs per SM.)  Where a ring has as many
+    // compute threads as the forward kernel has threads per row, every thread
+    // takes the same vectors in the same order, whatever its chunk size, so those
+    // rows equal ce_forward + ce_backward bit for bit: BF16 rows of 48-64 KiB and
+    // FP32 rows of 16-56 KiB (8 warps, the forward's 256 threads), and rows of
+    // 112-400 KiB BF16 or 64-400 KiB FP32 (16 warps, its 512), as the rows up to
+    // 16 KiB do.
     const int64_t nvec = vocab / Elem<T>::kVec;
     const int64_t bytes = nvec * 16;
     const double l2 = double(dev.l2_bytes), row = double(vocab) * double(sizeof(T));
@@ -1657,14 +1665,15 @@ void fused_dispatch(const void* logits, int64_t n_rows, int64_t vocab, int64_t s
     } else if (bytes > 400 * KiB) {
         pair_launch<T, 16, 4, 192, true>(VCE_FUSED_ARGS, dev, diag);
     } else if constexpr (sizeof(T) == 4) {
-        if (bytes <= 56 * KiB) ring_launch<T, 8, 4, 96, 2, false>(VCE_FUSED_ARGS, dev, diag);
+        if (bytes <= 56 * KiB) ring_launch<T, 8, 8, 96, 2, false>(VCE_FUSED_ARGS, dev, diag);
         else ring_launch<T, 16, 4, 192, 1, true>(VCE_FUSED_ARGS, dev, diag);
     } else {
-        if (bytes <= 48 * KiB) ring_launch<T, 4, 4, 48, 4, false>(VCE_FUSED_ARGS, dev, diag);
-        else if (bytes <= 88 * KiB) ring_launch<T, 8, 4, 112, 2, false>(VCE_FUSED_ARGS, dev, diag);
-        else if (bytes <= 112 * KiB) ring_launch<T, 8, 4, 96, 2, false>(VCE_FUSED_ARGS, dev, diag);
+        if (bytes <= 44 * KiB) ring_launch<T, 4, 8, 48, 4, false>(VCE_FUSED_ARGS, dev, diag);
+        else if (bytes <= 88 * KiB) ring_launch<T, 8, 7, 112, 2, false>(VCE_FUSED_ARGS, dev, diag);
+        else if (bytes <= 112 * KiB) ring_launch<T, 8, 8, 96, 2, false>(VCE_FUSED_ARGS, dev, diag);
         else if (bytes <= 240 * KiB) ring_launch<T, 16, 4, 224, 1, true>(VCE_FUSED_ARGS, dev, diag);
-        else ring_launch<T, 16, 4, 192, 1, true>(VCE_FUSED_ARGS, dev, diag);
+        else if (bytes <= 288 * KiB) ring_launch<T, 16, 4, 192, 1, true>(VCE_FUSED_ARGS, dev, diag);
+        else ring_launch<T, 16, 8, 192, 1, true>(VCE_FUSED_ARGS, dev, diag);
     }
 #undef VCE_FUSED_ARGS
 }
