@@ -184,12 +184,13 @@ vce_status ce_backward(const void* logits, int dtype, int64_t n_rows, int64_t vo
  *   Arguments are those of ce_forward and ce_backward combined; the results are
  *   those of ce_forward followed by ce_backward with the same grad_output (loss,
  *   stats, n_valid, dlogits): bit for bit for rows of at most 16 KiB, BF16
- *   rows of 48 to 64 KiB and of 112 to 400 KiB, and FP32 rows of 16 to 56 KiB
+ *   rows of 48 to 64 KiB and of 112 to 448 KiB, and FP32 rows of 16 to 56 KiB
  *   and of 64 to 400 KiB, where both calls give every thread the same elements
  *   in the same order; for other rows this call splits a row's sum
  *   differently, so lse and the loss agree to FP32 rounding (row maxima,
- *   n_valid and ignored rows exactly).  Rows above 400 KiB are each split
- *   between the two CTAs of a cluster on two SMs.  For rows above 16 KiB the
+ *   n_valid and ignored rows exactly).  BF16 rows above 448 KiB and FP32 rows
+ *   above 400 KiB are each split between the two CTAs of a cluster on two
+ *   SMs.  For rows above 16 KiB the
  *   call uses up to about 226 KiB of shared memory per SM and raises its
  *   kernels' dynamic shared-memory limit on the first call on each device.  A
  *   timeout of its internal copy pipeline (not expected) sets

@@ -123,7 +123,8 @@ def main():
         (60, 150001, 3, 1, "bf16", 0.0, 0, True, True),    # 192 KiB ring, 8 vectors per thread, in place
         (50, 9001, 3, 1, "f32", 0.1, 1, True, False),      # FP32, two CTAs per SM, 96 KiB rings
         (20, 50257, 3, 1, "f32", 0.0, 0, True, False),     # FP32, 192 KiB ring
-        (40, 210000, 8, 7, "bf16", 0.1, 1, True, False),   # rows split over a cluster pair
+        (40, 210000, 8, 7, "bf16", 0.1, 1, True, False),   # 192 KiB ring, 8 vectors per thread, 410 KiB rows
+        (40, 240000, 8, 7, "bf16", 0.1, 1, True, False),   # rows split over a cluster pair
     ]
     for c in logits_cases:
         check_logits(*c)

@@ -365,11 +365,12 @@ def assert_fused_matches_separate(r, sep_f, sep_dz, target, dtype):
 
 
 @pytest.mark.parametrize("vocab,dtype", [(5003, "bf16"), (30000, "bf16"), (100000, "bf16"), (130001, "bf16"),
-                                         (190000, "bf16"), (9001, "f32"), (25000, "f32")])
+                                         (190000, "bf16"), (210000, "bf16"), (9001, "f32"), (25000, "f32"),
+                                         (60001, "f32")])
 def test_fused_bit_identical_where_threads_match(vocab, dtype):
     # Rows the fused call gives the forward kernel's own thread count: up to
     # 16 KiB (128 threads), BF16 48-64 KiB and FP32 16-56 KiB (8 ring warps = 256
-    # threads), BF16 112-400 KiB and FP32 64-400 KiB (16 ring warps = 512
+    # threads), BF16 112-448 KiB and FP32 64-400 KiB (16 ring warps = 512
     # threads).  Each thread then takes the same elements in the same order as
     # in ce_forward, and the second pass is ce_backward's arithmetic: every
     # output bit matches.
@@ -402,7 +403,7 @@ FUSED = [
     (130, 128256, "bf16", 0.0, False, True),
     # several rows per persistent CTA on every shape of the TMA-fed ring kernel
     # (rows above 16 KiB): one CTA per SM with a 224 KiB ring (bf16 128 KiB rows) or
-    # a 192 KiB ring (bf16 293 KiB rows, f32 196 and 78 KiB rows), rows above 400 KiB
+    # a 192 KiB ring (bf16 293 KiB rows, f32 196 and 78 KiB rows), longer rows
     # split over the two CTAs of a cluster (f32 512 KiB rows), two CTAs per SM with
     # 112 KiB rings (bf16 78 and 59 KiB rows) or 96 KiB rings (bf16 102 KiB rows,
     # f32 35 KiB rows), and four with 48 KiB rings (bf16 39 and 23 KiB rows)
@@ -445,7 +446,7 @@ def test_fused_matches_oracle_and_separate_path(n, vocab, dtype, eps, red, inpla
     (300, 40001, 5, "bf16", 0.1, True),   # ring kernel, two CTAs per SM, 112 KiB rings
     (400, 70001, 7, "bf16", 0.0, 2),      # ring kernel, one CTA per SM, 224 KiB ring, rows off 16-byte alignment
     (100, 150001, 3, "bf16", 0.0, False), # ring kernel, one CTA per SM, 192 KiB ring
-    (160, 205003, 3, "bf16", 0.1, True),  # rows split over a cluster pair, rows off alignment
+    (160, 240003, 3, "bf16", 0.1, True),  # rows split over a cluster pair, rows off alignment
     (400, 12001, 1, "bf16", 0.0, 2),      # ring kernel, four CTAs per SM
     (150, 9001, 5, "f32", 0.0, False),    # ring kernel, FP32, two CTAs per SM, 96 KiB rings
     (300, 129, 1, "bf16", 0.1, 2),        # 128 threads per row

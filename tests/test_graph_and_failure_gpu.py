@@ -46,9 +46,9 @@ def test_all_entry_points_replay_in_a_cuda_graph():
     # shape: four CTAs per SM (24 KiB rows), two with 112 KiB rings (59 KiB) and with
     # 96 KiB rings (98 KiB), one with a 224 KiB ring (137 KiB) and with a 192 KiB
     # ring (254 KiB, 4 vectors per thread; 293 KiB, 8), and rows split over a
-    # cluster pair (410 KiB)
+    # cluster pair (469 KiB)
     fused = []
-    for vf in (5003, 12000, 30000, 50257, 70001, 130001, 150001, 210000):
+    for vf in (5003, 12000, 30000, 50257, 70001, 130001, 150001, 240000):
         zf = _bf16(wk.normal_matrix(7, wk.TID_LOGITS, n, vf, 3.0, True))
         yf = torch.from_numpy(wk.uniform_targets(7, n, vf, 0.1)).to(DEV)
         fused.append((zf, yf, torch.empty(1, device=DEV), torch.empty(n, 2, device=DEV),
@@ -180,11 +180,11 @@ def test_gemm_timeout_exit_then_normal_call():
 # every ring shape: BF16 four CTAs per SM (24 KiB rows), two with 112 KiB rings (59
 # KiB) and with 96 KiB rings (98 KiB), one with a 224 KiB ring (137 KiB) and with a
 # 192 KiB ring (254 KiB, 4 vectors per thread; 293 KiB, 8); FP32 two CTAs per SM
-# with 96 KiB rings (23 KiB rows) and one with a 192 KiB ring (117 KiB); rows split
-# over a cluster pair (BF16 410 KiB)
+# with 96 KiB rings (23 KiB rows) and one with a 192 KiB ring (117 KiB, 4 vectors
+# per thread; 234 KiB, 8); rows split over a cluster pair (BF16 469 KiB)
 @pytest.mark.parametrize("dtype,vocab", [("bf16", 12000), ("bf16", 30000), ("bf16", 50257), ("bf16", 70001),
                                          ("bf16", 130001), ("bf16", 150001), ("f32", 6000), ("f32", 30000),
-                                         ("bf16", 210000)])
+                                         ("f32", 60001), ("bf16", 240000)])
 def test_ring_timeout_exit_then_normal_call(dtype, vocab):
     # The fused ring kernel with its producer issuing no copy: the compute warps'
     # first wait for a chunk runs out after 1 ms with nothing in flight, the

@@ -1631,26 +1631,30 @@ void fused_dispatch(const void* logits, int64_t n_rows, int64_t vocab, int64_t s
     //     (65536: 0.95; 100352: 0.97; 120000: 0.96; the 192 KiB ring 0.94);
     //   BF16 up to 288 KiB: the same with a 192 KiB ring (128256: 0.97-0.98;
     //     140000: 0.96; 8 vectors per thread 0.94-0.97);
-    //   BF16 up to 400 KiB: the 192 KiB ring with 8 vectors per thread, in three
-    //     64 KiB chunks (160000: 0.95; 180000: 0.94; 195000: 0.91 [0.87-0.92]);
+    //   BF16 up to 448 KiB: the 192 KiB ring with 8 vectors per thread, in three
+    //     64 KiB chunks (160000: 0.95; 180000: 0.94; 205000: 0.90; 210000: 0.87
+    //     [0.83-0.92]);
     //   FP32 up to 56 KiB: two CTAs per SM, 8 compute warps x 8 vectors, 96 KiB
     //     rings (V = 7000: 0.85; 10000: 0.90; 13500: 0.87 [0.81-0.87]);
-    //   FP32 up to 400 KiB: one CTA per SM, 16 compute warps x 4 vectors, the 192
-    //     KiB ring with L2 hints (16000: 0.91; 25000: 0.955; 50257: 0.94);
+    //   FP32 up to 128 KiB: one CTA per SM, 16 compute warps x 4 vectors, the 192
+    //     KiB ring with L2 hints (16000: 0.91; 25000: 0.96);
+    //   FP32 up to 400 KiB: the same with 8 vectors per thread (50257: 0.96;
+    //     95000: 0.885; 102000: 0.88 [0.86-0.95]);
     //   longer: each row split between the two CTAs of a cluster (two SMs),
-    //     each with the 192 KiB ring over its half, so each SM keeps half a row
-    //     in L2 between the passes (BF16 256000: 0.90 against 0.88 for a
-    //     single-CTA ring that pinned the row's first 64 KiB in shared memory;
-    //     FP32 128256: 0.93 against 0.88).  Below 400 KiB the exchange of the
-    //     halves' partials costs more than it saves (BF16 202048: 0.83 against
-    //     0.86; 128256: 0.75 against 0.97).
+    //     each with the 192 KiB ring (4 vectors per thread) over its half, so
+    //     each SM keeps half a row in L2 between the passes (BF16 256000: 0.90
+    //     against 0.81 for the single-CTA ring; FP32 128256: 0.92 against 0.83).
+    //     On shorter rows the exchange of the halves' partials costs more than it
+    //     saves (BF16 205000: 0.82 against 0.90; FP32 102000: 0.86 against 0.88),
+    //     and the pair with 6-8 vectors per thread splits rows into uneven halves
+    //     of whole chunks (0.77-0.87).
     // (Over ring shapes of 4-16 compute warps, 2-8 vectors per thread, 8-64 KiB
     // chunks, 48-224 KiB rings and 1-4 CTAs per SM.)  Where a ring has as many
     // compute threads as the forward kernel has threads per row, every thread
     // takes the same vectors in the same order, whatever its chunk size, so those
     // rows equal ce_forward + ce_backward bit for bit: BF16 rows of 48-64 KiB and
     // FP32 rows of 16-56 KiB (8 warps, the forward's 256 threads), and rows of
-    // 112-400 KiB BF16 or 64-400 KiB FP32 (16 warps, its 512), as the rows up to
+    // 112-448 KiB BF16 or 64-400 KiB FP32 (16 warps, its 512), as the rows up to
     // 16 KiB do.
     const int64_t nvec = vocab / Elem<T>::kVec;
     const int64_t bytes = nvec * 16;
@@ -1662,11 +1666,12 @@ void fused_dispatch(const void* logits, int64_t n_rows, int64_t vocab, int64_t s
         const int grid = fused_grid(n_rows, dev.num_sms, 8);
         if (double(grid) * 2 * row <= l2 * 2.0 / 3.0) fused_launch<T, 128, 8, 4, 2, true>(VCE_FUSED_ARGS, grid);
         else fused_launch<T, 128, 8, 4, 2, false>(VCE_FUSED_ARGS, grid);
-    } else if (bytes > 400 * KiB) {
+    } else if (bytes > (sizeof(T) == 4 ? 400 : 448) * KiB) {
         pair_launch<T, 16, 4, 192, true>(VCE_FUSED_ARGS, dev, diag);
     } else if constexpr (sizeof(T) == 4) {
         if (bytes <= 56 * KiB) ring_launch<T, 8, 8, 96, 2, false>(VCE_FUSED_ARGS, dev, diag);
-        else ring_launch<T, 16, 4, 192, 1, true>(VCE_FUSED_ARGS, dev, diag);
+        else if (bytes <= 128 * KiB) ring_launch<T, 16, 4, 192, 1, true>(VCE_FUSED_ARGS, dev, diag);
+        else ring_launch<T, 16, 8, 192, 1, true>(VCE_FUSED_ARGS, dev, diag);
     } else {
         if (bytes <= 44 * KiB) ring_launch<T, 4, 8, 48, 4, false>(VCE_FUSED_ARGS, dev, diag);
         else if (bytes <= 88 * KiB) ring_launch<T, 8, 7, 112, 2, false>(VCE_FUSED_ARGS, dev, diag);
