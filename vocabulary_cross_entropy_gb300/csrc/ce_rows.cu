@@ -889,7 +889,8 @@ __device__ __forceinline__ void compute_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
 }
 
-// block_merge over the compute threads of the ring kernel
+// group_merge over the compute threads of the cluster kernel (a named barrier
+// that leaves the producer warp out); thread 0 ends with the CTA's partial
 template <int NT, bool kSum>
 __device__ __forceinline__ void compute_merge(OnlineLse& a, float* sm_m, float* sm_s, float* sm_sum) {
     group_merge<NT / 32, kSum>(a, sm_m, sm_s, sm_sum, [] { compute_sync<NT>(); });
@@ -1211,9 +1212,10 @@ ce_fused_ring(const T* logits, int64_t n_rows, int64_t vocab, int64_t stride, co
 }
 
 // Rows whose two passes would keep too much of L2 busy when one SM takes the
-// whole row (above 256 KiB: 152 rows in flight hold 40-80 MB of lines between
-// their first and second reads, and the second pass starts to miss): the two
-// CTAs of a cluster (two SMs) split every row they take.  Rank 0 owns the
+// whole row (BF16 rows above 448 KiB, FP32 above 400 KiB: 152 such rows in
+// flight hold 60-70 MB or more of lines between their first and second reads,
+// and the second pass starts to miss): the two CTAs of a cluster (two SMs)
+// split every row they take.  Rank 0 owns the
 // first half of the row's interior chunks and the head elements before it,
 // rank 1 the rest and the tail elements, so each SM keeps only half a row in
 // L2 between the passes.  Each CTA runs the ring kernel's producer and compute
