@@ -607,6 +607,38 @@ mean_loss_kernel(const float* __restrict__ loss_rows, const int64_t* __restrict_
     }
 }
 
+// N_v alone (no loss to reduce): the count of rows whose target is not
+// ignore_idx, from integer loads only, sixteen in flight per thread, summed with
+// redux.sync per warp and over the warps in shared memory.
+constexpr int kCountThreads = 1024;
+
+__global__ void __launch_bounds__(kCountThreads)
+count_valid_kernel(const int64_t* __restrict__ target, int64_t n, int64_t ignore_idx, int64_t* __restrict__ n_valid) {
+    __shared__ unsigned sm_c[32];
+    constexpr int U = 16;
+    int ci = 0;  // this thread's count (at most n / 1024 + 16)
+    for (int64_t i0 = threadIdx.x; i0 < n; i0 += int64_t(kCountThreads) * U) {
+        int64_t t[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t i = i0 + int64_t(u) * kCountThreads;
+            t[u] = i < n ? target[i] : ignore_idx;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) ci += t[u] != ignore_idx ? 1 : 0;
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const unsigned wc = __reduce_add_sync(0xffffffffu, unsigned(ci));
+    if (lane == 0) sm_c[warp] = wc;
+    __syncthreads();
+    if (warp == 0) {
+        long long c = sm_c[lane];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
+        if (lane == 0) n_valid[0] = c;
+    }
+}
+
 // ---------------------------------------------------------------------------
 // token shift for causal language modelling
 // ---------------------------------------------------------------------------
@@ -1714,7 +1746,10 @@ vce_status launch_shift_targets(const int64_t* target, int64_t n, int64_t seq_le
 vce_status launch_mean_loss(const float* loss_rows, const int64_t* target, int64_t n_rows,
                             int64_t ignore_idx, int reduce, float* loss_out, int64_t* n_valid, cudaStream_t s) {
     count_launch();
-    mean_loss_kernel<<<1, kMeanThreads, 0, s>>>(loss_rows, target, n_rows, ignore_idx, reduce, loss_out, n_valid);
+    if (!loss_rows && !loss_out && n_valid)  // the count alone
+        count_valid_kernel<<<1, kCountThreads, 0, s>>>(target, n_rows, ignore_idx, n_valid);
+    else
+        mean_loss_kernel<<<1, kMeanThreads, 0, s>>>(loss_rows, target, n_rows, ignore_idx, reduce, loss_out, n_valid);
     return cudaGetLastError() == cudaSuccess ? VCE_OK : VCE_ERR_CUDA;
 }
 
