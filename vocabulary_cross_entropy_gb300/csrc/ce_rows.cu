@@ -530,6 +530,9 @@ __device__ __forceinline__ void pair_add(float& hi, float& lo, float h2, float l
     lo = l - (hi - s);
 }
 
+// kCounted: N_v was counted before (the fused call's count), read from
+// ``n_valid``; only the losses are loaded, sixteen per thread per step.
+template <bool kCounted>
 __global__ void __launch_bounds__(kMeanThreads)
 mean_loss_kernel(const float* __restrict__ loss_rows, const int64_t* __restrict__ target,
                  int64_t n, int64_t ignore_idx, int reduce, float* __restrict__ loss_out,
@@ -546,16 +549,17 @@ mean_loss_kernel(const float* __restrict__ loss_rows, const int64_t* __restrict_
     // per launch at 16384 rows against 6.1 us, and converting and adding every
     // row in FP64 took 14 us for 16384 rows and 585 us for 1M rows).
     float fs = 0.f, fc = 0.f;
-    int ci = 0;  // this thread's count (at most n / 1024 + 8)
-    constexpr int U = 8;  // loads in flight per thread, summed as a small tree (16 measured
-                          // 4-10 us slower at 65536-131072 rows)
+    int ci = 0;  // this thread's count (at most n / 1024 + 16)
+    // loads in flight per thread, summed as a small tree (with the targets too,
+    // 16 measured 4-10 us slower than 8 at 65536-131072 rows)
+    constexpr int U = kCounted ? 16 : 8;
     for (int64_t i0 = threadIdx.x; i0 < n; i0 += int64_t(kMeanThreads) * U) {
         float l[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int64_t i = i0 + int64_t(u) * kMeanThreads;
             const bool in = i < n;
-            ci += (in && target[i] != ignore_idx) ? 1 : 0;
+            if (!kCounted) ci += (in && target[i] != ignore_idx) ? 1 : 0;
             l[u] = (in && loss_rows) ? loss_rows[i] : 0.f;
         }
 #pragma unroll
@@ -575,7 +579,7 @@ mean_loss_kernel(const float* __restrict__ loss_rows, const int64_t* __restrict_
     for (int off = 16; off > 0; off >>= 1) {
         const float h2 = __shfl_xor_sync(0xffffffffu, hi, off), l2 = __shfl_xor_sync(0xffffffffu, lo, off);
         pair_add(hi, lo, h2, l2);
-        c += __shfl_xor_sync(0xffffffffu, c, off);
+        if (!kCounted) c += __shfl_xor_sync(0xffffffffu, c, off);
     }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (lane == 0) { sm_h[warp] = hi; sm_l[warp] = lo; sm_c[warp] = c; }
@@ -588,8 +592,9 @@ mean_loss_kernel(const float* __restrict__ loss_rows, const int64_t* __restrict_
         for (int off = 16; off > 0; off >>= 1) {
             const float h2 = __shfl_xor_sync(0xffffffffu, hi, off), l2 = __shfl_xor_sync(0xffffffffu, lo, off);
             pair_add(hi, lo, h2, l2);
-            c += __shfl_xor_sync(0xffffffffu, c, off);
+            if (!kCounted) c += __shfl_xor_sync(0xffffffffu, c, off);
         }
+        if (kCounted) c = n_valid[0];
         if (lane == 0) {
             // mean: (hi + lo) / N_v with one correction step (0/0 = NaN when every
             // row is ignored); sum: the plain total
@@ -602,7 +607,7 @@ mean_loss_kernel(const float* __restrict__ loss_rows, const int64_t* __restrict_
                 out = isfinite(q) ? q + __fdiv_rn(fmaf(-q, cf, hi) + lo, cf) : q;
             }
             if (loss_out) loss_out[0] = out;
-            if (n_valid) n_valid[0] = c;
+            if (n_valid && !kCounted) n_valid[0] = c;
         }
     }
 }
@@ -1749,7 +1754,8 @@ vce_status launch_mean_loss(const float* loss_rows, const int64_t* target, int64
     if (!loss_rows && !loss_out && n_valid)  // the count alone
         count_valid_kernel<<<1, kCountThreads, 0, s>>>(target, n_rows, ignore_idx, n_valid);
     else
-        mean_loss_kernel<<<1, kMeanThreads, 0, s>>>(loss_rows, target, n_rows, ignore_idx, reduce, loss_out, n_valid);
+        mean_loss_kernel<false>
+            <<<1, kMeanThreads, 0, s>>>(loss_rows, target, n_rows, ignore_idx, reduce, loss_out, n_valid);
     return cudaGetLastError() == cudaSuccess ? VCE_OK : VCE_ERR_CUDA;
 }
 
@@ -1810,6 +1816,12 @@ vce_status launch_ce_forward_backward(const void* logits, int dtype, int64_t n_r
             fused_dispatch<float>(logits, n_rows, vocab, row_stride, target, eps, ignore_idx, n_valid,
                                   grad_output, reduce_loss, loss_rows, stats, dlogits, dev_status, s, dev, diag);
         if (cudaGetLastError() != cudaSuccess) return VCE_ERR_CUDA;
+        if (reduce_loss == VCE_REDUCE_MEAN) {  // N_v is in n_valid already: sum the losses alone
+            count_launch();
+            mean_loss_kernel<true>
+                <<<1, kMeanThreads, 0, s>>>(loss_rows, target, n_rows, ignore_idx, reduce_loss, loss, n_valid);
+            return cudaGetLastError() == cudaSuccess ? VCE_OK : VCE_ERR_CUDA;
+        }
     }
     if (reduce_loss || n_valid)
         return launch_mean_loss(reduce_loss ? loss_rows : nullptr, target, n_rows, ignore_idx, reduce_loss,
