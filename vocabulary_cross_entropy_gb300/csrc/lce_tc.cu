@@ -378,6 +378,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();  // 0: issues the pair's MMAs
+    // a GEMM launched as this one's programmatic dependent may be scheduled now:
+    // its CTAs take SMs as this grid's pairs run out of work units and exit
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;");
     const bool leader = rank == 0;
     const int T = args.tiles_m * args.tiles_n * args.k_splits;
 
@@ -599,6 +602,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         tc_fence_after();
         tmem_dealloc_pair(tmem_base, C::kTmemCols);
     }
+    // A GEMM launched to overlap the tail of the previous one (programmatic
+    // dependent launch) completes only after that one: later work on the stream
+    // may then rely on both.  Without such a prerequisite this returns at once.
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -729,10 +736,21 @@ bool map_mnmajor(CUtensorMap* m, const void* base, int64_t mn, int64_t k, int64_
     return make_map(m, base, uint64_t(mn), uint64_t(k), uint64_t(ld) * 2, 64, BK);
 }
 
-// Zeroes a GEMM's work-unit counter (a kernel rather than a memset, so that the
-// reset is ordered on the compute stream like the GEMM and never waits behind
-// copies that another stream has queued on a copy engine).
-__global__ void reset_counter_kernel(int* counter) { *counter = 0; }
+// Zeroes ``count`` work-unit counters (a kernel rather than a memset, so that
+// the reset is ordered on the compute stream like the GEMMs and never waits
+// behind copies that another stream has queued on a copy engine).
+__global__ void reset_counter_kernel(int* counter, int count) {
+    for (int i = 0; i < count; ++i) counter[i] = 0;
+}
+
+// How launch_gemm orders a GEMM after the work before it on the stream.
+enum class After {
+    kReset,    // zero the counter first (one small kernel), then a plain launch
+    kPlain,    // the counter was zeroed earlier; plain launch
+    kOverlap,  // the counter was zeroed earlier; programmatic dependent launch:
+               // the GEMM starts on SMs the previous GEMM's pairs leave, so it
+               // must not read that GEMM's results (it reads none of them)
+};
 
 // Tiles of the fast index per group of the unit order.  The group's strips of the
 // fast-index operand (A when M is fast, B when N is: 256 rows x the unit's K range)
@@ -760,7 +778,7 @@ int raster_group(int tiles_fast, int64_t strip_bytes, double aspect, const Devic
 template <class Epi, bool kAMn, bool kBMn, int BN>
 vce_status launch_gemm(const CUtensorMap& a, const CUtensorMap& b, int64_t M, int64_t N, int64_t K, int m_fastest,
                        int k_splits, const Epi& epi, int* counter, int* dev_status, cudaStream_t s,
-                       const DeviceInfo& dev, const PipeDiag& diag = PipeDiag()) {
+                       const DeviceInfo& dev, const PipeDiag& diag = PipeDiag(), After after = After::kReset) {
     using C = PairCfg<BN>;
     auto kern = tc_gemm_kernel<Epi, kAMn, kBMn, BN>;
     // the shared-memory limit is a per-device attribute of the kernel: raise it
@@ -802,9 +820,25 @@ vce_status launch_gemm(const CUtensorMap& a, const CUtensorMap& b, int64_t M, in
     if (units <= 0 || args.k_blocks <= 0) return VCE_OK;
     const int64_t pairs = dev.num_sms / 2;
     const int grid = 2 * int(units < pairs ? units : pairs);
+    if (after == After::kReset) {
+        count_launch();
+        reset_counter_kernel<<<1, 1, 0, s>>>(counter, 1);
+    }
     count_launch();
-    reset_counter_kernel<<<1, 1, 0, s>>>(counter);
-    count_launch();
+    if (after == After::kOverlap) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = C::kSmemBytes;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, kern, a, b, args, epi) == cudaSuccess) return VCE_OK;
+        (void)cudaGetLastError();  // not accepted here: the plain launch below
+    }
     kern<<<grid, kThreads, C::kSmemBytes, s>>>(a, b, args, epi);
     return cudaGetLastError() == cudaSuccess ? VCE_OK : VCE_ERR_CUDA;
 }
@@ -921,7 +955,7 @@ int64_t slab_ld(int64_t slab) { return (slab + 7) / 8 * 8; }
 
 // Backward workspace: the BF16 dZ slab, then (unless one slab and one K chunk
 // let dX be written directly) the FP32 dX partial sums of every K chunk, then
-// 256 bytes for the GEMMs' work-unit counter.
+// 256 bytes for the GEMMs' work-unit counters (the forward's and dZ's in the first int, dX's and dW's in the first two).
 struct BwdPlan {
     int64_t ld;      // dZ slab leading dimension
     int splits;      // K chunks of the dX GEMM
@@ -1039,24 +1073,31 @@ vce_status launch_lce_backward(const void* X, const void* W, int64_t n, int64_t 
                 launch_gemm<DzEpi, false, false, kVocabTile>(tx_k, tws_k, n, vs, h, 1, 1, de, counter, dev_status, s,
                                                              dev))
             return st;
-        // dW_slab = dZ^T X: M = vs, N = h, K = n (both operands MN-major)
-        StoreEpi we{dWb + v0 * h, h, nullptr, 0, 0, 0, vs, h, 1, dev_status};
-        if (vce_status st =
-                dw_tile(n, h) == 512
-                    ? launch_gemm<StoreEpi, true, true, 512>(tdz_mn, tx_mn, vs, h, n, 0, 1, we, counter, dev_status, s,
-                                                             dev)
-                    : launch_gemm<StoreEpi, true, true, 256>(tdz_mn, tx_mn, vs, h, n, 0, 1, we, counter, dev_status, s,
-                                                             dev))
-            return st;
+        // dX and dW both read only the dZ slab.  dX goes first, on counter[0]: its
+        // few long work units leave pairs idle in its last round, and dW, on
+        // counter[1], is launched to overlap that tail (its CTAs take the SMs the
+        // dX pairs leave).  Each GEMM grid completes only after its prerequisite,
+        // so the next slab's dZ and the dX finalize follow both.
+        count_launch();
+        reset_counter_kernel<<<1, 1, 0, s>>>(counter, 2);
         // dX (+)= dZ W_slab: M = n, N = h, K = vs (W_slab read MN-major), K cut into plan.splits chunks
         StoreEpi xe{dXb, h, acc, h, split_stride, plan.direct ? 0 : (v0 == 0 ? 1 : 2), n, h, plan.splits, dev_status};
-        const vce_status st =
+        const vce_status sx =
             plan.tile_n == 512
                 ? launch_gemm<StoreEpi, false, true, 512>(tdz_k, tws_mn, n, h, vs, 1, plan.splits, xe, counter,
-                                                          dev_status, s, dev)
+                                                          dev_status, s, dev, PipeDiag(), After::kPlain)
                 : launch_gemm<StoreEpi, false, true, 256>(tdz_k, tws_mn, n, h, vs, 1, plan.splits, xe, counter,
-                                                          dev_status, s, dev);
-        if (st != VCE_OK) return st;
+                                                          dev_status, s, dev, PipeDiag(), After::kPlain);
+        if (sx != VCE_OK) return sx;
+        // dW_slab = dZ^T X: M = vs, N = h, K = n (both operands MN-major)
+        StoreEpi we{dWb + v0 * h, h, nullptr, 0, 0, 0, vs, h, 1, dev_status};
+        const vce_status sw =
+            dw_tile(n, h) == 512
+                ? launch_gemm<StoreEpi, true, true, 512>(tdz_mn, tx_mn, vs, h, n, 0, 1, we, counter + 1, dev_status, s,
+                                                         dev, PipeDiag(), After::kOverlap)
+                : launch_gemm<StoreEpi, true, true, 256>(tdz_mn, tx_mn, vs, h, n, 0, 1, we, counter + 1, dev_status, s,
+                                                         dev, PipeDiag(), After::kOverlap);
+        if (sw != VCE_OK) return sw;
     }
     if (!plan.direct) {
         const int64_t count4 = n * h / 4;  // h is a multiple of 8
