@@ -42,6 +42,7 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 #include <mutex>
+#include <type_traits>
 
 namespace vce {
 namespace {
@@ -378,9 +379,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();  // 0: issues the pair's MMAs
-    // a GEMM launched as this one's programmatic dependent may be scheduled now:
-    // its CTAs take SMs as this grid's pairs run out of work units and exit
-    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;");
+    // (dX, dW) a GEMM launched as this one's programmatic dependent may be
+    // scheduled now: its CTAs take SMs as this grid's pairs run out of work units
+    // and exit
+    constexpr bool kOverlaps = std::is_same<Epi, StoreEpi>::value;
+    if (kOverlaps && threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;");
     const bool leader = rank == 0;
     const int T = args.tiles_m * args.tiles_n * args.k_splits;
 
@@ -605,7 +608,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // A GEMM launched to overlap the tail of the previous one (programmatic
     // dependent launch) completes only after that one: later work on the stream
     // may then rely on both.  Without such a prerequisite this returns at once.
-    if (threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (kOverlaps && threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------
