@@ -58,8 +58,8 @@ CSRC = os.path.join(ROOT, "vocabulary_cross_entropy_gb300", "csrc")
 # the sources still hash to that digest; after any change it is null until the
 # counters are taken again.
 TRAFFIC_SOURCES = {
-    "gemm": (("lce_tc.cu", "sm100_ptx.cuh", "vce_internal.cuh"), "e2ece49ca408bd59"),
-    "rows": (("ce_rows.cu", "sm100_ptx.cuh", "vce_internal.cuh"), "c178914cff35593d"),
+    "gemm": (("lce_tc.cu", "sm100_ptx.cuh", "vce_internal.cuh"), "c918968bd6e5a2a3"),
+    "rows": (("ce_rows.cu", "sm100_ptx.cuh", "vce_internal.cuh"), "b0bbe2173a3eeba5"),
 }
 
 
@@ -86,7 +86,7 @@ def FWD_GEMM_TRAFFIC_BYTES(wl):
     N = H = 4096, V = 131072, scaled to this workload's V: the X bytes stay, the W
     bytes and the per-tile partials grow with V.  None for workloads outside that
     N = H = 4096 family."""
-    captured_v, read_bytes, write_bytes = 131072, 1.109051e+09, 1.988096e+07
+    captured_v, read_bytes, write_bytes = 131072, 1.108277e+09, 1.997773e+07
     if wl.n != 4096 or wl.hidden != 4096 or not traffic_current("gemm"):
         return None
     x_bytes = wl.n * wl.hidden * 2
@@ -98,9 +98,9 @@ def FWD_GEMM_TRAFFIC_BYTES(wl):
 # captures (dram__bytes_read.sum, dram__bytes_write.sum) of 2048 rows of
 # V = 128256 BF16 with 5% of the rows ignored
 LOGITS_CAPTURED_TRAFFIC = {
-    "forward": (502.379264e6, 3.015168e6),
-    "backward": (502.329344e6, 464.443904e6),
-    "fused": (505.524736e6, 464.567040e6),
+    "forward": (502.429696e6, 2.713344e6),
+    "backward": (502.315520e6, 465.096448e6),
+    "fused": (505.406720e6, 464.416512e6),
 }
 
 
