@@ -97,6 +97,9 @@ def test_lce_host_validation(lib):
     assert call(ws_bytes=16) == WORKSPACE
     assert call(v=0) == INVALID
     lib.lce_workspace_size.restype = ctypes.c_size_t
-    full = lib.lce_workspace_size(I64(4096), I64(4096), I64(131072), 1, ctypes.c_size_t(0))
-    capped = lib.lce_workspace_size(I64(4096), I64(4096), I64(131072), 1, ctypes.c_size_t(1 << 28))
-    assert full >= 4096 * 131072 * 2 and capped < full
+    ws = lambda cap: lib.lce_workspace_size(I64(4096), I64(4096), I64(131072), 1, ctypes.c_size_t(cap))
+    # SIZE_MAX (VCE_SLAB_UNCAPPED): one dZ slab over the whole vocabulary; 0: the
+    # default 256 MiB cap; an explicit cap below it is smaller still
+    full, default, capped = ws((1 << 64) - 1), ws(0), ws(64 << 20)
+    assert full >= 4096 * 131072 * 2
+    assert default == ws(256 << 20) and default < full and capped < default

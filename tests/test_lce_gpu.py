@@ -264,7 +264,7 @@ def test_dz_slab_beyond_2_31_elements_sampled():
                            label_smoothing=0.1, reduce_loss=True)
     assert wl.n * ((wl.vocab + 7) // 8 * 8) > 2 ** 31
     inp = wk.make_linear_inputs(wl)
-    f, b = run(inp.x, inp.w, inp.target, wl.label_smoothing, wl.reduce_loss, inp.grad, 0, False)
+    f, b = run(inp.x, inp.w, inp.target, wl.label_smoothing, wl.reduce_loss, inp.grad, vce.SLAB_UNCAPPED, False)
     _sampled_check(wl, inp, f, b, False)
 
 

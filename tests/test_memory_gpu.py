@@ -24,8 +24,9 @@ def _peak_rise(fn):
     return torch.cuda.max_memory_allocated() - base
 
 
-@pytest.mark.parametrize("max_slab_bytes", [0, 256 * MiB])
+@pytest.mark.parametrize("max_slab_bytes", [vce.SLAB_UNCAPPED, 0, 64 * MiB])
 def test_linear_headline_extra_memory(max_slab_bytes):
+    # one slab over the whole vocabulary, the default 256 MiB cap, a 64 MiB cap
     n, h, v = 4096, 4096, 131072
     g = torch.Generator(device=DEV).manual_seed(7)
     x = torch.randn(n, h, device=DEV, generator=g).to(torch.bfloat16)
@@ -46,10 +47,11 @@ def test_linear_headline_extra_memory(max_slab_bytes):
     # plus lse [N] and a few words; the caching allocator rounds each block up
     assert rise <= 2 * ws_bytes + n * 4 + 4 * MiB, (rise, ws_bytes)
     assert rise < n * v * 4
-    if max_slab_bytes:
+    if max_slab_bytes != vce.SLAB_UNCAPPED:
         # the dZ slab cap bounds the workspace (slab + at most four FP32 dX partials),
         # and with it the extra memory: below even one BF16 copy of the logits
-        assert ws_bytes <= max_slab_bytes + 4 * n * h * 4
+        cap = max_slab_bytes or vce.DEFAULT_SLAB_BYTES
+        assert ws_bytes <= cap + 4 * n * h * 4
         assert rise < n * v * 2
     assert torch.isfinite(loss).all()
 

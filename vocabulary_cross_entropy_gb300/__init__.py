@@ -15,6 +15,8 @@ from ._binding import (  # noqa: F401
     DEVSTATUS_BAD_TARGET,
     DEVSTATUS_TIMEOUT,
     DEVSTATUS_BOUNDS,
+    DEFAULT_SLAB_BYTES,
+    SLAB_UNCAPPED,
     REDUCE_NONE,
     REDUCE_MEAN,
     REDUCE_SUM,

@@ -17,6 +17,10 @@ F32 = 1
 DEVSTATUS_BAD_TARGET = 1
 DEVSTATUS_TIMEOUT = 2
 DEVSTATUS_BOUNDS = 4
+# max_slab_bytes: 0 selects the library's default cap (VCE_DEFAULT_SLAB_BYTES);
+# SLAB_UNCAPPED lets one dZ slab cover the whole vocabulary
+DEFAULT_SLAB_BYTES = 256 << 20
+SLAB_UNCAPPED = (1 << 64) - 1
 REDUCE_NONE, REDUCE_MEAN, REDUCE_SUM = 0, 1, 2
 
 _c_i64 = ctypes.c_int64

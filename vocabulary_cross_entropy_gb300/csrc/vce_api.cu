@@ -174,11 +174,9 @@ size_t lce_workspace_size(int64_t n, int64_t h, int64_t v, int reduce_loss,
                           size_t max_slab_bytes) {
     if (n <= 0 || h <= 0 || v <= 0) return 0;
     const size_t fwd = lce_forward_ws_bytes(n, v, reduce_loss);
-    int64_t slab = v;
-    if (max_slab_bytes > 0) {
-        const int64_t cap = int64_t(max_slab_bytes / (size_t(n) * 2)) / 256 * 256;
-        slab = cap < 256 ? 256 : (cap < v ? cap : v);
-    }
+    if (max_slab_bytes == 0) max_slab_bytes = VCE_DEFAULT_SLAB_BYTES;
+    const int64_t cap = int64_t(max_slab_bytes / (size_t(n) * 2)) / 256 * 256;  // at most 2^63 - 1
+    const int64_t slab = cap < 256 ? 256 : (cap < v ? cap : v);
     const size_t bwd = lce_backward_ws_bytes(n, h, v, slab);
     return fwd > bwd ? fwd : bwd;
 }
