@@ -941,6 +941,9 @@ def main():
                     help="also time the model-shape sweep (Qwen3-30B-A3B, Llama 4, DeepSeek-V3 heads at M=8192)")
     ap.add_argument("--no-large", dest="large", action="store_false",
                     help="skip the 16384x4096x128256 workload (throughput and peak extra memory)")
+    ap.add_argument("--slab-cap", default="default",
+                    help="dZ slab cap of the linear step: 'default' (the library's 256 MiB), 'uncapped' "
+                         "(one slab over the whole vocabulary) or a number of bytes")
     ap.add_argument("--shape", default=None,
                     help="linear workload N,H,V instead of the headline (e.g. a small profiling case)")
     ap.add_argument("--logits-rows", type=int, default=None,
@@ -1035,7 +1038,10 @@ def main():
         return 0
 
     lin = linear_workload(args)
-    st = LinearStep(lin, dev)
+    slab_cap = {"default": 0, "uncapped": SLAB_UNCAPPED}.get(args.slab_cap)
+    if slab_cap is None:
+        slab_cap = int(args.slab_cap)
+    st = LinearStep(lin, dev, max_slab_bytes=slab_cap)
     with Clocks(local) as ck:
         total, ph = time_steps(st, args.steps, args.warmup, pg)
     clocks = ck.summary()
@@ -1070,7 +1076,7 @@ def main():
         "config": {"workload": st.wl.name, "n": st.wl.n, "h": st.wl.hidden, "v": st.wl.vocab,
                    "reduce_loss": True, "label_smoothing": 0.0,
                    "l2": "inputs larger than L2 (W is 1 GiB), no flush",
-                   "max_slab_bytes": "library default (256 MiB)",
+                   "max_slab_bytes": {0: "library default (256 MiB)", SLAB_UNCAPPED: "uncapped"}.get(slab_cap, slab_cap),
                    "workspace_bytes": st.ws_bytes},
         "fwd_ms": ph["forward"], "bwd_ms": ph["backward"], "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
         # the timed region is K steps of ~10 ms, far shorter than the seconds-long loop
@@ -1127,7 +1133,8 @@ def main():
             line["linear_large"]["cpu_baseline"] = cpu_baseline_linear(big.wl)
         del big
         torch.cuda.empty_cache()
-        line["slab_caps"] = slab_cap_sweep(dev, args, pg, local, headline_ms)
+        if slab_cap == 0:  # the sweep's runs are compared with the default cap
+            line["slab_caps"] = slab_cap_sweep(dev, args, pg, local, headline_ms)
     if args.large and lin is wk.LINEAR_HEADLINE:
         # the two small configurations: the tiny FP32 logits case (launch latency)
         # and the 4096 x 2048 x 32000 linear case (per-token loss, 2% ignored)
