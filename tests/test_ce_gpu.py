@@ -389,6 +389,23 @@ def test_fused_bit_identical_where_threads_match(vocab, dtype):
     assert torch.equal(r.dlogits.view(torch.int16), dz.view(torch.int16))
 
 
+@pytest.mark.parametrize("n,vocab,dtype", [(20000, 2000, "bf16"), (17000, 9001, "f32")])
+def test_fused_mean_bit_identical_many_rows(n, vocab, dtype):
+    # More rows than the mean kernel's 1024 threads x 8 rows per step: the fused
+    # call's mean (N_v counted before its pass) groups and compensates each
+    # thread's rows exactly as ce_forward's mean does, so the loss matches bit for
+    # bit where the rows do (short rows here; FP32 16-56 KiB rows on the ring)
+    z = wk.normal_matrix(n + vocab, wk.TID_LOGITS, n, vocab, 3.0, dtype == "bf16")
+    target = wk.uniform_targets(n + vocab, n, vocab, 0.1)
+    logits = to_dev(z, dtype)
+    grad = np.ones(1, np.float32)
+    f, dz = run_gpu(logits, target, 0.1, True, grad)
+    r = run_fused(logits, target, 0.1, True, grad)
+    assert int(r.n_valid.item()) == int(f.n_valid.item())
+    assert torch.equal(r.stats, f.stats)
+    assert torch.equal(r.loss.view(torch.int32), f.loss.view(torch.int32))
+
+
 FUSED = [
     # n, vocab, dtype, eps, reduce, inplace
     (128, 1024, "f32", 0.0, False, False),

@@ -531,7 +531,7 @@ __device__ __forceinline__ void pair_add(float& hi, float& lo, float h2, float l
 }
 
 // kCounted: N_v was counted before (the fused call's count), read from
-// ``n_valid``; only the losses are loaded, sixteen per thread per step.
+// ``n_valid``; only the losses are loaded.
 template <bool kCounted>
 __global__ void __launch_bounds__(kMeanThreads)
 mean_loss_kernel(const float* __restrict__ loss_rows, const int64_t* __restrict__ target,
@@ -549,10 +549,12 @@ mean_loss_kernel(const float* __restrict__ loss_rows, const int64_t* __restrict_
     // per launch at 16384 rows against 6.1 us, and converting and adding every
     // row in FP64 took 14 us for 16384 rows and 585 us for 1M rows).
     float fs = 0.f, fc = 0.f;
-    int ci = 0;  // this thread's count (at most n / 1024 + 16)
-    // loads in flight per thread, summed as a small tree (with the targets too,
-    // 16 measured 4-10 us slower than 8 at 65536-131072 rows)
-    constexpr int U = kCounted ? 16 : 8;
+    int ci = 0;  // this thread's count (at most n / 1024 + 8)
+    // rows per thread per step, summed as a small tree before the compensated
+    // addition: the same grouping with and without the count, so the fused call's
+    // mean equals ce_forward's bit for bit (16 with the targets measured 4-10 us
+    // slower at 65536-131072 rows)
+    constexpr int U = 8;
     for (int64_t i0 = threadIdx.x; i0 < n; i0 += int64_t(kMeanThreads) * U) {
         float l[U];
 #pragma unroll
