@@ -1172,7 +1172,7 @@ def main():
         torch.cuda.empty_cache()
         line["sweep"] = []
         for shp in wk.MODEL_SHAPES:
-            stp = LinearStep(shp, dev)
+            stp = LinearStep(shp, dev, max_slab_bytes=slab_cap)
             ks = max(3, args.steps // 3)
             with Clocks(local) as cks:
                 ts, phs = time_steps(stp, ks, args.warmup, pg)
@@ -1182,6 +1182,7 @@ def main():
                 "value": stp.units() * world * ks / (ts / 1e3), "unit": "TFLOP/s", "ms_per_step": ts / ks,
                 "fwd_ms": phs["forward"], "bwd_ms": phs["backward"], "steps": ks,
                 "pages_tp1_fb_ms_b300": PUBLISHED_MODEL_SHAPES_FB_MS.get(shp.name),
+                "max_slab_bytes": {0: "library default (256 MiB)", SLAB_UNCAPPED: "uncapped"}.get(slab_cap, slab_cap),
                 "workspace_bytes": stp.ws_bytes, "clocks": cks.summary()})
             del stp
             torch.cuda.empty_cache()

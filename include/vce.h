@@ -246,9 +246,11 @@ vce_status ce_forward_noalloc(const void* logits, int dtype, int64_t n_rows, int
  * Backward recomputes the logits one vocabulary slab at a time and keeps that
  * slab's gradient dZ [n, slab] in BF16; ``max_slab_bytes`` caps that buffer.
  * 0 selects VCE_DEFAULT_SLAB_BYTES (256 MiB): at N = H = 4096, V = 131072 that
- * is four slabs, whose backward measured 0.2% slower than one slab's with 1.0
- * GB less workspace (each extra slab adds an FP32 pass over the dX partials and
- * its own GEMM launches).  VCE_SLAB_UNCAPPED lets one slab cover the whole
+ * is four slabs, whose step measured 0.2-0.4% slower than one slab's with 1.0
+ * GB less workspace; at 8192 tokens of H = 2048-7168, V = 129280-202048 it is
+ * 8-13 slabs and 3.4-4.3% slower, with 336-503 MB against 2.1-3.8 GB (each
+ * extra slab adds an FP32 pass over the dX partials and its own GEMM
+ * launches).  VCE_SLAB_UNCAPPED lets one slab cover the whole
  * vocabulary (an N x V BF16 buffer).  The slab is at least 256 vocabulary
  * rows.  dX = dZ W has few output tiles, so its vocabulary
  * range is cut into 1-4 chunks (chosen from the tile count and the SM count
