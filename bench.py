@@ -849,6 +849,22 @@ def cpu_baseline_logits(wl):
 # MiB (4 slabs) that the headline line uses; the large workload at 256 MiB (16
 # slabs) against the 1 GiB slabs of its own line
 SLAB_UNCAPPED = (1 << 64) - 1
+
+
+def parse_slab_cap(text):
+    """--slab-cap: 'default' -> 0 (the library's 256 MiB), 'uncapped' -> SLAB_UNCAPPED,
+    else a positive number of bytes."""
+    special = {"default": 0, "uncapped": SLAB_UNCAPPED}
+    if text in special:
+        return special[text]
+    cap = int(text)
+    if cap <= 0:
+        raise ValueError("--slab-cap takes 'default', 'uncapped' or a positive number of bytes")
+    return cap
+
+
+def slab_cap_label(cap):
+    return {0: "library default (256 MiB)", SLAB_UNCAPPED: "uncapped"}.get(cap, cap)
 SLAB_CAPS = (("headline", SLAB_UNCAPPED), ("headline", 64 << 20), ("large", 256 << 20))
 
 
@@ -1038,9 +1054,7 @@ def main():
         return 0
 
     lin = linear_workload(args)
-    slab_cap = {"default": 0, "uncapped": SLAB_UNCAPPED}.get(args.slab_cap)
-    if slab_cap is None:
-        slab_cap = int(args.slab_cap)
+    slab_cap = parse_slab_cap(args.slab_cap)
     st = LinearStep(lin, dev, max_slab_bytes=slab_cap)
     with Clocks(local) as ck:
         total, ph = time_steps(st, args.steps, args.warmup, pg)
@@ -1076,7 +1090,7 @@ def main():
         "config": {"workload": st.wl.name, "n": st.wl.n, "h": st.wl.hidden, "v": st.wl.vocab,
                    "reduce_loss": True, "label_smoothing": 0.0,
                    "l2": "inputs larger than L2 (W is 1 GiB), no flush",
-                   "max_slab_bytes": {0: "library default (256 MiB)", SLAB_UNCAPPED: "uncapped"}.get(slab_cap, slab_cap),
+                   "max_slab_bytes": slab_cap_label(slab_cap),
                    "workspace_bytes": st.ws_bytes},
         "fwd_ms": ph["forward"], "bwd_ms": ph["backward"], "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
         # the timed region is K steps of ~10 ms, far shorter than the seconds-long loop
@@ -1182,7 +1196,7 @@ def main():
                 "value": stp.units() * world * ks / (ts / 1e3), "unit": "TFLOP/s", "ms_per_step": ts / ks,
                 "fwd_ms": phs["forward"], "bwd_ms": phs["backward"], "steps": ks,
                 "pages_tp1_fb_ms_b300": PUBLISHED_MODEL_SHAPES_FB_MS.get(shp.name),
-                "max_slab_bytes": {0: "library default (256 MiB)", SLAB_UNCAPPED: "uncapped"}.get(slab_cap, slab_cap),
+                "max_slab_bytes": slab_cap_label(slab_cap),
                 "workspace_bytes": stp.ws_bytes, "clocks": cks.summary()})
             del stp
             torch.cuda.empty_cache()

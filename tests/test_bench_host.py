@@ -1,8 +1,11 @@
-"""Host logic of bench.py that needs no GPU: the clock-sample window."""
+"""Host logic of bench.py that needs no GPU: the clock-sample window, the traffic
+provenance digests and the --slab-cap option."""
 import datetime
 import importlib.util
 import os
 import time
+
+import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -64,3 +67,17 @@ def test_traffic_figures_go_null_when_the_kernel_source_changes(monkeypatch):
     names, _ = b.TRAFFIC_SOURCES["rows"]
     monkeypatch.setitem(b.TRAFFIC_SOURCES, "rows", (names, "0" * 16))
     assert b.LOGITS_TRAFFIC_BYTES(b.wk.LOGITS_MEMBOUND, "fused") is None
+
+
+def test_slab_cap_option():
+    # --slab-cap: the library default (0), one slab (SIZE_MAX) or a byte count
+    bench = _bench()
+    assert bench.parse_slab_cap("default") == 0
+    assert bench.parse_slab_cap("uncapped") == (1 << 64) - 1
+    assert bench.parse_slab_cap("67108864") == 64 << 20
+    for bad in ("0", "-5", "lots"):
+        with pytest.raises(ValueError):
+            bench.parse_slab_cap(bad)
+    assert bench.slab_cap_label(0).startswith("library default")
+    assert bench.slab_cap_label(bench.SLAB_UNCAPPED) == "uncapped"
+    assert bench.slab_cap_label(64 << 20) == 64 << 20
